@@ -1,0 +1,182 @@
+"""fp64 CPU oracle for the tile-level GEMM C = A*B.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only tests/, __graft_entry__.smoke()
+and the cpu_baseline / reference legs of bench.py may import this package.
+The product path (hierarchical_gemm_gb300) never imports it and shares no
+code with it.
+
+The operation is the one the TileLang GEMM skeleton computes ("TileScale 与
+TileLang比较", section 核心抽象与编程模型对比): C is cleared, every BK-slice
+product of A (M x K, row-major) and B (K x N, row-major) is added into it, and
+the result is copied out.  Up to the order of additions this is
+C[i][j] = sum_k A[i][k] * B[k][j]; the C library in oracle_gemm.c writes that
+sum out in double precision in the order k = 0..K-1.
+
+Inputs and outputs here are numpy arrays of raw bits (uint16 for fp16/bf16,
+float32 for fp32 outputs), so the oracle decodes the exact values itself.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+F16, BF16, F32 = 0, 1, 2
+_NAMES = {"f16": F16, "fp16": F16, "float16": F16,
+          "bf16": BF16, "bfloat16": BF16,
+          "f32": F32, "fp32": F32, "float32": F32}
+
+_lib = None
+
+
+def dtype_code(d):
+    if isinstance(d, int):
+        return d
+    return _NAMES[str(d).lower()]
+
+
+def lib():
+    """Load (building first if needed) the oracle's shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.oracle_decode.restype = ctypes.c_double
+        L.oracle_decode.argtypes = [ctypes.c_uint16, i32]
+        L.oracle_round16.restype = ctypes.c_uint16
+        L.oracle_round16.argtypes = [ctypes.c_double, i32]
+        L.oracle_decode_n.argtypes = [vp, i64, i32, vp]
+        L.oracle_round16_n.argtypes = [vp, i64, i32, vp]
+        L.oracle_round32_n.argtypes = [vp, i64, vp]
+        L.oracle_gemm.restype = i32
+        L.oracle_gemm.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32]
+        L.oracle_gemm_sampled.argtypes = [i64, i64, i64, vp, vp, i32, i64, vp,
+                                          vp, vp, vp]
+        L.oracle_default_threads.restype = i32
+        _lib = L
+    return _lib
+
+
+def _c(a, dt):
+    a = np.ascontiguousarray(a, dtype=dt)
+    return a, a.ctypes.data
+
+
+def default_threads():
+    return lib().oracle_default_threads()
+
+
+def decode(bits, dtype):
+    """Exact float64 values of an array of 16-bit float bit patterns."""
+    bits, p = _c(bits, np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib().oracle_decode_n(p, bits.size, dtype_code(dtype), out.ctypes.data)
+    return out
+
+
+def round_out(x, dtype_out):
+    """Round float64 values to the output format, ties to even.
+
+    Returns uint16 bit patterns for f16/bf16 and float32 values for f32.
+    """
+    x, p = _c(x, np.float64)
+    code = dtype_code(dtype_out)
+    if code == F32:
+        out = np.empty(x.shape, dtype=np.float32)
+        lib().oracle_round32_n(p, x.size, out.ctypes.data)
+    else:
+        out = np.empty(x.shape, dtype=np.uint16)
+        lib().oracle_round16_n(p, x.size, code, out.ctypes.data)
+    return out
+
+
+def gemm(A_bits, B_bits, dtype_in, nthreads=0):
+    """ref = A*B and sabs = |A|*|B| (elementwise products), both float64.
+
+    A_bits: (M, K) uint16, B_bits: (K, N) uint16, both row-major.
+    Returns (ref, sabs, threads_used).
+    """
+    A_bits, pa = _c(A_bits, np.uint16)
+    B_bits, pb = _c(B_bits, np.uint16)
+    M, K = A_bits.shape
+    K2, N = B_bits.shape
+    assert K == K2, "inner dimensions differ"
+    ref = np.empty((M, N), dtype=np.float64)
+    sabs = np.empty((M, N), dtype=np.float64)
+    used = lib().oracle_gemm(M, N, K, pa, pb, dtype_code(dtype_in),
+                             ref.ctypes.data, sabs.ctypes.data, int(nthreads))
+    if used < 0:
+        raise MemoryError("oracle_gemm could not allocate its decoded B")
+    return ref, sabs, used
+
+
+def gemm_sampled(A_bits, B_bits, dtype_in, rows, cols):
+    """ref and sabs at the positions (rows[s], cols[s]) only."""
+    A_bits, pa = _c(A_bits, np.uint16)
+    B_bits, pb = _c(B_bits, np.uint16)
+    M, K = A_bits.shape
+    K2, N = B_bits.shape
+    assert K == K2, "inner dimensions differ"
+    rows, pr = _c(rows, np.int64)
+    cols, pc = _c(cols, np.int64)
+    assert rows.shape == cols.shape
+    assert rows.size == 0 or (rows.min() >= 0 and rows.max() < M)
+    assert cols.size == 0 or (cols.min() >= 0 and cols.max() < N)
+    ref = np.empty(rows.shape, dtype=np.float64)
+    sabs = np.empty(rows.shape, dtype=np.float64)
+    lib().oracle_gemm_sampled(M, N, K, pa, pb, dtype_code(dtype_in), rows.size,
+                              pr, pc, ref.ctypes.data, sabs.ctypes.data)
+    return ref, sabs
+
+
+# Acceptance rule for a GEMM result against the oracle:
+#   * exact mode (integer-valued inputs whose fp32 partial sums are all
+#     exact): the output must equal the oracle's sum rounded to the output
+#     format, bit for bit;
+#   * otherwise |C - ref| <= RTOL * sabs + ATOL per element.
+RTOL = 1e-3
+ATOL = 1e-5
+
+
+def output_values(C, dtype_out):
+    """float64 values of a GEMM output given as raw bits (u16) or float32."""
+    code = dtype_code(dtype_out)
+    if code == F32:
+        return np.asarray(C, dtype=np.float32).astype(np.float64)
+    return decode(np.asarray(C).view(np.uint16), code)
+
+
+def accept(C, ref, sabs, dtype_out, exact=False):
+    """Compare an output against the oracle.
+
+    Returns (ok, info) where info holds the worst error and its position.
+    """
+    code = dtype_code(dtype_out)
+    if exact:
+        want = round_out(ref, code)
+        if code == F32:
+            got = np.asarray(C, dtype=np.float32).view(np.uint32)
+            want = want.view(np.uint32)
+        else:
+            got = np.asarray(C).view(np.uint16)
+        bad = got != want
+        nbad = int(bad.sum())
+        info = {"mismatches": nbad}
+        if nbad:
+            idx = np.argwhere(bad)[0]
+            info["first"] = tuple(int(v) for v in idx)
+        return nbad == 0, info
+    cv = output_values(C, code)
+    err = np.abs(cv - ref)
+    bound = RTOL * sabs + ATOL
+    bad = ~(err <= bound)  # NaN counts as bad
+    nbad = int(bad.sum())
+    ratio = err / bound
+    worst = int(np.nanargmax(ratio)) if ratio.size else 0
+    info = {"mismatches": nbad,
+            "max_err_over_bound": float(np.nanmax(ratio)) if ratio.size else 0.0,
+            "worst_index": tuple(int(v) for v in np.unravel_index(worst, ratio.shape))
+            if ratio.size else ()}
+    return nbad == 0, info
