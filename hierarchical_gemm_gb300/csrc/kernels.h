@@ -1,0 +1,15 @@
+// kernels.h -- host-visible handles to the compiled GEMM kernels.
+#pragma once
+
+#include <stdint.h>
+
+namespace tsg {
+
+// Kernel entry for a tile width (64/128/192/256) and output kind
+// (0 fp16, 1 bf16, 2 fp32); null for an unsupported combination.
+const void* kernel_1sm(int block_n, int out_kind);
+
+// Dynamic shared memory the kernel above uses with `stages` ring slots.
+int64_t kernel_1sm_smem_bytes(int block_n, int stages);
+
+}  // namespace tsg

@@ -1,0 +1,30 @@
+// planner.h -- host-side validation and configuration choice for a GEMM
+// problem (tile width, split factor, pipeline depth, raster group, grid).
+#pragma once
+
+#include <stdint.h>
+
+#include "tsgemm.h"
+
+namespace tsg {
+
+// Shared-memory budget of one CTA on sm_103a (227 KiB opt-in maximum).
+constexpr int64_t kSmemPerCtaMax = 232448;
+
+// Validate a problem description without touching a GPU.
+tsgemm_status_t validate_problem(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
+                                 int layout);
+
+// Fill *out with the configuration for the problem on a device with
+// `num_sms` SMs, honouring every non-zero field of `force` (may be null).
+tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
+                              int layout, int num_sms, const tsgemm_config_t* force,
+                              tsgemm_config_t* out);
+
+// Dynamic shared memory a 1-SM kernel with this tile width and depth needs.
+int64_t smem_bytes_for(int block_n, int stages);
+
+// Deepest ring that fits the shared-memory budget for this tile width.
+int max_stages_for(int block_n);
+
+}  // namespace tsg

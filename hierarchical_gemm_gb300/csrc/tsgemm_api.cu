@@ -1,0 +1,338 @@
+// tsgemm_api.cu -- the C ABI: plans, operand descriptors (TMA tensor maps),
+// launches and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "gemm_sm103.cuh"
+#include "kernels.h"
+#include "planner.h"
+#include "tsgemm.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the installed driver, looked up through the
+// runtime so that the library does not link libcuda directly.
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// tcgen05 instruction descriptor, kind::f16:
+//   bits  4-5  accumulator format (1 = fp32)
+//   bits  7-9  A format (0 = fp16, 1 = bf16)
+//   bits 10-12 B format
+//   bit  15    A major (0 = K-major)
+//   bit  16    B major (1 = MN-major: B is K x N with N contiguous)
+//   bits 17-22 N >> 3
+//   bits 24-28 M >> 4
+uint32_t make_idesc(int dtype_in, int m, int n) {
+    const uint32_t fmt = dtype_in == TSGEMM_BF16 ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+int out_kind(int dtype_out) {
+    return dtype_out == TSGEMM_F16 ? tsg::kOutF16 : (dtype_out == TSGEMM_BF16 ? tsg::kOutBF16 : tsg::kOutF32);
+}
+
+int64_t elem_bytes(int dt) { return dt == TSGEMM_F32 ? 4 : 2; }
+
+}  // namespace
+
+struct tsgemm_plan_s {
+    int64_t M, N, K;
+    int dtype_in, dtype_out;
+    tsgemm_config_t cfg;
+    int device;
+    const void* kernel;
+    int64_t smem;
+    int* status_d;
+    float* ws;
+    int* counters;
+    int64_t num_tiles;
+    const void* last_a;
+    const void* last_b;
+    const void* last_c;
+    alignas(64) CUtensorMap tmA;
+    alignas(64) CUtensorMap tmB;
+    tsg::GemmParams params;
+};
+
+static void plan_free(tsgemm_plan_s* p) {
+    if (!p) return;
+    if (p->status_d) cudaFree(p->status_d);
+    if (p->ws) cudaFree(p->ws);
+    if (p->counters) cudaFree(p->counters);
+    delete p;
+}
+
+extern "C" {
+
+const char* tsgemm_status_string(tsgemm_status_t s) {
+    switch (s) {
+        case TSGEMM_OK: return "success";
+        case TSGEMM_ERR_INVALID_ARG: return "invalid argument";
+        case TSGEMM_ERR_UNSUPPORTED: return "unsupported problem, configuration or device";
+        case TSGEMM_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
+        case TSGEMM_ERR_CUDA: return "CUDA call failed";
+        case TSGEMM_ERR_TIMEOUT: return "a bounded device wait expired";
+        case TSGEMM_ERR_OOM: return "out of device memory";
+        default: return "unknown status";
+    }
+}
+
+tsgemm_status_t tsgemm_choose_config(int64_t M, int64_t N, int64_t K, tsgemm_dtype_t dtype_in,
+                                     tsgemm_dtype_t dtype_out, tsgemm_layout_t layout,
+                                     int32_t num_sms, const tsgemm_config_t* force,
+                                     tsgemm_config_t* out) {
+    return tsg::choose_config(M, N, K, dtype_in, dtype_out, layout, num_sms, force, out);
+}
+
+tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t K,
+                               tsgemm_dtype_t dtype_in, tsgemm_dtype_t dtype_out,
+                               tsgemm_layout_t layout, const tsgemm_config_t* force) {
+    if (!out) return TSGEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    tsgemm_status_t st = tsg::validate_problem(M, N, K, dtype_in, dtype_out, layout);
+    if (st != TSGEMM_OK) return st;
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return TSGEMM_ERR_UNSUPPORTED;
+    if (!encode_fn()) return TSGEMM_ERR_CUDA;
+
+    tsgemm_config_t cfg{};
+    st = tsg::choose_config(M, N, K, dtype_in, dtype_out, layout, sms, force, &cfg);
+    if (st != TSGEMM_OK) return st;
+
+    const void* kern = tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out));
+    const int64_t need = tsg::kernel_1sm_smem_bytes(cfg.block_n, cfg.stages);
+    if (!kern || need != tsg::smem_bytes_for(cfg.block_n, cfg.stages) || need > tsg::kSmemPerCtaMax)
+        return TSGEMM_ERR_UNSUPPORTED;
+    // Ask for more than half the SM's shared memory even when the ring is
+    // shallow, so one CTA owns each SM and its tensor memory.
+    const int64_t smem = need > tsg::kSmemPerCtaMax / 2 + 1024 ? need : tsg::kSmemPerCtaMax / 2 + 1024;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+
+    // value-initialised; operator new honours the 64-byte alignment the
+    // tensor maps need
+    tsgemm_plan_s* p = new (std::nothrow) tsgemm_plan_s();
+    if (!p) return TSGEMM_ERR_OOM;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->dtype_in = dtype_in;
+    p->dtype_out = dtype_out;
+    p->cfg = cfg;
+    p->device = dev;
+    p->kernel = kern;
+    p->smem = smem;
+    p->num_tiles = ((M + 127) / 128) * ((N + cfg.block_n - 1) / cfg.block_n);
+
+    if (cudaMalloc(&p->status_d, sizeof(int)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        plan_free(p);
+        return TSGEMM_ERR_OOM;
+    }
+    if (cudaMemset(p->status_d, 0, sizeof(int)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        plan_free(p);
+        return TSGEMM_ERR_CUDA;
+    }
+    if (cfg.splits > 1) {
+        if (cudaMalloc(&p->ws, static_cast<size_t>(cfg.workspace_bytes)) != cudaSuccess ||
+            cudaMalloc(&p->counters, static_cast<size_t>(p->num_tiles) * sizeof(int)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            plan_free(p);
+            return TSGEMM_ERR_OOM;
+        }
+        if (cudaMemset(p->counters, 0, static_cast<size_t>(p->num_tiles) * sizeof(int)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            plan_free(p);
+            return TSGEMM_ERR_CUDA;
+        }
+    }
+
+    tsg::GemmParams& gp = p->params;
+    gp.M = static_cast<int32_t>(M);
+    gp.N = static_cast<int32_t>(N);
+    gp.K = static_cast<int32_t>(K);
+    gp.tiles_m = static_cast<int32_t>((M + 127) / 128);
+    gp.tiles_n = static_cast<int32_t>((N + cfg.block_n - 1) / cfg.block_n);
+    gp.splits = cfg.splits;
+    gp.kblocks = static_cast<int32_t>((K + 63) / 64);
+    gp.group_m = cfg.group_m;
+    gp.stages = cfg.stages;
+    gp.debug_flags = cfg.debug_flags;
+    gp.units = cfg.units;
+    gp.idesc = make_idesc(dtype_in, 128, cfg.block_n);
+    gp.C = nullptr;
+    gp.ws = p->ws;
+    gp.counters = p->counters;
+    gp.status = p->status_d;
+    gp.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms) * 1000000ull;
+    *out = p;
+    return TSGEMM_OK;
+}
+
+tsgemm_status_t tsgemm_plan(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t K,
+                            tsgemm_dtype_t dtype_in, tsgemm_dtype_t dtype_out,
+                            tsgemm_layout_t layout) {
+    return tsgemm_plan_ex(out, M, N, K, dtype_in, dtype_out, layout, nullptr);
+}
+
+tsgemm_status_t tsgemm_get_config(tsgemm_plan_t plan, tsgemm_config_t* out) {
+    if (!plan || !out) return TSGEMM_ERR_INVALID_ARG;
+    *out = plan->cfg;
+    return TSGEMM_OK;
+}
+
+static tsgemm_status_t check_device_ptr(const void* ptr, int device) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return TSGEMM_ERR_INVALID_ARG;
+    if (a.type == cudaMemoryTypeDevice && a.device != device) return TSGEMM_ERR_INVALID_ARG;
+    return TSGEMM_OK;
+}
+
+static bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+}
+
+static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* B) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return TSGEMM_ERR_CUDA;
+    const CUtensorMapDataType dt =
+        p->dtype_in == TSGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint32_t estr[2] = {1, 1};
+    {
+        // A: inner dimension K, outer M; box 64 x 128 (one 128-byte swizzle row per M row)
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->K) * 2};
+        const cuuint32_t box[2] = {64, 128};
+        if (enc(&p->tmA, dt, 2, const_cast<void*>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TSGEMM_ERR_CUDA;
+    }
+    {
+        // B: inner dimension N, outer K; box 64 x 64 (64 columns = 128 bytes)
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->K)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->N) * 2};
+        const cuuint32_t box[2] = {64, 64};
+        if (enc(&p->tmB, dt, 2, const_cast<void*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TSGEMM_ERR_CUDA;
+    }
+    return TSGEMM_OK;
+}
+
+tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, void* C, void* stream) {
+    if (!plan || !A || !B || !C) return TSGEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15u)
+        return TSGEMM_ERR_ALIGNMENT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    if (dev != plan->device) return TSGEMM_ERR_INVALID_ARG;
+    const int64_t a_bytes = plan->M * plan->K * 2, b_bytes = plan->K * plan->N * 2;
+    const int64_t c_bytes = plan->M * plan->N * elem_bytes(plan->dtype_out);
+    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)) return TSGEMM_ERR_INVALID_ARG;
+
+    if (A != plan->last_a || B != plan->last_b) {
+        tsgemm_status_t st = check_device_ptr(A, plan->device);
+        if (st == TSGEMM_OK) st = check_device_ptr(B, plan->device);
+        if (st != TSGEMM_OK) return st;
+        plan->last_a = nullptr;
+        plan->last_b = nullptr;
+        st = encode_maps(plan, A, B);
+        if (st != TSGEMM_OK) return st;
+        plan->last_a = A;
+        plan->last_b = B;
+    }
+    if (C != plan->last_c) {
+        tsgemm_status_t st = check_device_ptr(C, plan->device);
+        if (st != TSGEMM_OK) return st;
+        plan->last_c = C;
+    }
+    plan->params.C = C;
+
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(plan->cfg.grid), 1, 1);
+    lc.blockDim = dim3(tsg::kThreads, 1, 1);
+    lc.dynamicSmemBytes = static_cast<size_t>(plan->smem);
+    lc.stream = static_cast<cudaStream_t>(stream);
+    lc.attrs = nullptr;
+    lc.numAttrs = 0;
+    void* args[3] = {&plan->tmA, &plan->tmB, &plan->params};
+    if (cudaLaunchKernelExC(&lc, plan->kernel, args) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    return TSGEMM_OK;
+}
+
+tsgemm_status_t tsgemm_status(tsgemm_plan_t plan) {
+    if (!plan) return TSGEMM_ERR_INVALID_ARG;
+    int word = 0;
+    if (cudaMemcpy(&word, plan->status_d, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    if (word == TSGEMM_OK) return TSGEMM_OK;
+    // A run gave up: clear the word and the split-K tile counters it may
+    // have left behind, so the plan can run again.
+    if (cudaMemset(plan->status_d, 0, sizeof(int)) != cudaSuccess ||
+        (plan->counters &&
+         cudaMemset(plan->counters, 0, static_cast<size_t>(plan->num_tiles) * sizeof(int)) != cudaSuccess) ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    return static_cast<tsgemm_status_t>(word);
+}
+
+tsgemm_status_t tsgemm_destroy(tsgemm_plan_t plan) {
+    plan_free(plan);
+    return TSGEMM_OK;
+}
+
+}  // extern "C"

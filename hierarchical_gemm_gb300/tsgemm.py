@@ -1,0 +1,205 @@
+"""Python binding of the tsgemm C ABI (ctypes).
+
+Argument marshalling only: every step of C = A * B runs in the CUDA kernels
+of libtsgemm.so.  There is no fallback path; if the library has not been
+built, importing this module raises ImportError.
+"""
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libtsgemm.so")
+
+F16, BF16, F32 = 0, 1, 2
+LAYOUT_RRR = 0
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_ALIGNMENT = 3
+ERR_CUDA = 4
+ERR_TIMEOUT = 5
+ERR_OOM = 6
+
+DEBUG_SKIP_FIRST_LOAD = 1
+
+_DTYPE_NAMES = {"f16": F16, "fp16": F16, "float16": F16, "half": F16,
+                "bf16": BF16, "bfloat16": BF16,
+                "f32": F32, "fp32": F32, "float32": F32, "float": F32}
+
+# Every entry point include/tsgemm.h declares.
+EXPORTS = ("tsgemm_plan", "tsgemm_plan_ex", "tsgemm_run", "tsgemm_destroy",
+           "tsgemm_status", "tsgemm_get_config", "tsgemm_choose_config",
+           "tsgemm_status_string")
+
+
+class Config(ctypes.Structure):
+    """Mirror of tsgemm_config_t."""
+    _fields_ = [("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("splits", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("group_m", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("timeout_ms", ctypes.c_int32), ("debug_flags", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libtsgemm.so is not built (%s); run hierarchical_gemm_gb300.build.build() "
+            "or __graft_entry__.build() first" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    cfgp = ctypes.POINTER(Config)
+    L.tsgemm_plan.restype = i32
+    L.tsgemm_plan.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32, i32, i32]
+    L.tsgemm_plan_ex.restype = i32
+    L.tsgemm_plan_ex.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i32, i32, i32, cfgp]
+    L.tsgemm_run.restype = i32
+    L.tsgemm_run.argtypes = [vp, vp, vp, vp, vp]
+    L.tsgemm_destroy.restype = i32
+    L.tsgemm_destroy.argtypes = [vp]
+    L.tsgemm_status.restype = i32
+    L.tsgemm_status.argtypes = [vp]
+    L.tsgemm_get_config.restype = i32
+    L.tsgemm_get_config.argtypes = [vp, cfgp]
+    L.tsgemm_choose_config.restype = i32
+    L.tsgemm_choose_config.argtypes = [i64, i64, i64, i32, i32, i32, i32, cfgp, cfgp]
+    L.tsgemm_status_string.restype = ctypes.c_char_p
+    L.tsgemm_status_string.argtypes = [i32]
+    return L
+
+
+lib = _load()
+
+
+class TsgemmError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+def status_string(code):
+    return lib.tsgemm_status_string(int(code)).decode()
+
+
+def _check(code, what):
+    if code != OK:
+        raise TsgemmError(code, what)
+
+
+def dtype_code(d):
+    """tsgemm dtype code from a name, a code or a torch dtype."""
+    if isinstance(d, int):
+        return d
+    s = str(d).lower().replace("torch.", "")
+    return _DTYPE_NAMES[s]
+
+
+def _force(kw):
+    c = Config()
+    for k, v in kw.items():
+        if not hasattr(c, k):
+            raise TypeError("unknown configuration field %r" % k)
+        setattr(c, k, int(v))
+    return c
+
+
+def choose_config(M, N, K, dtype_in, dtype_out, num_sms, **force):
+    """The planner's configuration for a problem (host only, no GPU)."""
+    out = Config()
+    f = _force(force)
+    _check(lib.tsgemm_choose_config(M, N, K, dtype_code(dtype_in), dtype_code(dtype_out),
+                                    LAYOUT_RRR, int(num_sms), ctypes.byref(f), ctypes.byref(out)),
+           "tsgemm_choose_config")
+    return out.as_dict()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Plan:
+    """A planned GEMM C (M x N) = A (M x K) * B (K x N) on the current device."""
+
+    def __init__(self, M, N, K, dtype_in, dtype_out, **force):
+        self._h = ctypes.c_void_p()
+        self.M, self.N, self.K = int(M), int(N), int(K)
+        self.dtype_in, self.dtype_out = dtype_code(dtype_in), dtype_code(dtype_out)
+        if force:
+            f = _force(force)
+            code = lib.tsgemm_plan_ex(ctypes.byref(self._h), self.M, self.N, self.K,
+                                      self.dtype_in, self.dtype_out, LAYOUT_RRR, ctypes.byref(f))
+        else:
+            code = lib.tsgemm_plan(ctypes.byref(self._h), self.M, self.N, self.K,
+                                   self.dtype_in, self.dtype_out, LAYOUT_RRR)
+        _check(code, "tsgemm_plan")
+
+    @property
+    def config(self):
+        out = Config()
+        _check(lib.tsgemm_get_config(self._h, ctypes.byref(out)), "tsgemm_get_config")
+        return out.as_dict()
+
+    def run(self, A, B, C, stream=None):
+        """Enqueue C = A * B; A, B, C are CUDA tensors (or raw device pointers)."""
+        _check(lib.tsgemm_run(self._h, _ptr(A), _ptr(B), _ptr(C), _stream_handle(stream)),
+               "tsgemm_run")
+        return C
+
+    def status(self):
+        """Device status word after the runs have completed (0 = OK)."""
+        return lib.tsgemm_status(self._h)
+
+    def close(self):
+        if self._h:
+            lib.tsgemm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_TORCH_OUT = {F16: "float16", BF16: "bfloat16", F32: "float32"}
+_plans = {}
+
+
+def gemm(A, B, out_dtype=None, C=None, stream=None):
+    """C = A @ B for row-major CUDA tensors A (M x K) and B (K x N) of dtype
+    float16 or bfloat16; plans are cached per shape and dtype."""
+    import torch
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("expected A (M x K) and B (K x N)")
+    if A.dtype != B.dtype:
+        raise ValueError("A and B must have the same dtype")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be row-major contiguous")
+    din = dtype_code(A.dtype)
+    dout = dtype_code(out_dtype) if out_dtype is not None else (F32 if C is None else dtype_code(C.dtype))
+    M, K = A.shape
+    N = B.shape[1]
+    key = (A.device.index, M, N, K, din, dout)
+    plan = _plans.get(key)
+    if plan is None:
+        plan = _plans[key] = Plan(M, N, K, din, dout)
+    if C is None:
+        C = torch.empty((M, N), dtype=getattr(torch, _TORCH_OUT[dout]), device=A.device)
+    return plan.run(A, B, C, stream)

@@ -1,0 +1,151 @@
+/*
+ * tsgemm.h -- C ABI of the GB300 (sm_103a) tile-level GEMM library.
+ *
+ * Operation.  C = A * B with A (M x K) and B (K x N) in row-major order and
+ * C (M x N) row-major, accumulated in fp32.  This is the tile-level GEMM of
+ * the TileLang single-device skeleton ("TileScale 与 TileLang比较",
+ * yaopepe.com, section 核心抽象与编程模型对比): the accumulator tile is
+ * cleared, every BK-slice product of an A tile and a B tile is added into it,
+ * and the tile is copied to C.  C is overwritten; there is no alpha or beta.
+ * The cluster form (two SMs computing one tile as a pair, which the TileScale
+ * README, section on T.Scale, calls a distributed GEMM on two SMs sharing
+ * operands over distributed shared memory) and the K split with a reduction
+ * (TileScale README, "Example of GEMM": warpgroups split along K and reduce)
+ * are implementation choices of the plan; they do not change the result
+ * beyond the fp32 summation order.
+ *
+ * Supported (dtype_in, dtype_out): (F16, F32), (F16, F16), (BF16, BF16),
+ * (BF16, F32).  Everything else returns TSGEMM_ERR_UNSUPPORTED.
+ *
+ * Numerics.  Products of the 16-bit inputs are exact; sums are fp32 in an
+ * order fixed by the plan (tensor-core order inside a K-slice, K-slices in
+ * increasing k, split-K partials added in split order 0..S-1), so results
+ * are reproducible run to run.  fp32 -> bf16/fp16 output conversion rounds
+ * to nearest, ties to even.
+ *
+ * Memory.  A, B and C are device pointers owned by the caller, on the device
+ * that was current when the plan was made, 16-byte aligned, with C not
+ * overlapping A or B.  Row strides must be multiples of 16 bytes: K * 2 and
+ * N * 2 (the A and B rows) and N * sizeof(out) (the C rows); otherwise
+ * TSGEMM_ERR_ALIGNMENT.
+ *
+ * Errors.  Every call returns a tsgemm_status_t.  Argument, alignment and
+ * device errors are detected on the host before anything is launched.  A
+ * kernel never waits without bound: each wait on the device gives up after
+ * a time limit (default 1 s), records TSGEMM_ERR_TIMEOUT in the plan's
+ * device status word and returns; tsgemm_status() reads that word after the
+ * caller has synchronised the stream.
+ */
+#ifndef TSGEMM_H
+#define TSGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TSGEMM_API __attribute__((visibility("default")))
+#else
+#define TSGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tsgemm_plan_s* tsgemm_plan_t;
+
+typedef enum {
+    TSGEMM_F16 = 0,  /* IEEE binary16 */
+    TSGEMM_BF16 = 1, /* bfloat16 */
+    TSGEMM_F32 = 2   /* IEEE binary32 (outputs only) */
+} tsgemm_dtype_t;
+
+typedef enum {
+    /* A M x K row-major, B K x N row-major, C M x N row-major */
+    TSGEMM_LAYOUT_RRR = 0
+} tsgemm_layout_t;
+
+typedef enum {
+    TSGEMM_OK = 0,
+    TSGEMM_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad enum */
+    TSGEMM_ERR_UNSUPPORTED = 2, /* dtype pair, layout, or device not CC 10.3 */
+    TSGEMM_ERR_ALIGNMENT = 3,   /* pointer or row stride not 16-byte aligned */
+    TSGEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+    TSGEMM_ERR_TIMEOUT = 5,     /* a bounded device wait expired */
+    TSGEMM_ERR_OOM = 6          /* plan could not allocate its buffers */
+} tsgemm_status_t;
+
+/* Execution configuration of a plan.  In tsgemm_plan_ex every field left at
+ * 0 is chosen by the planner; a non-zero field forces that value. */
+typedef struct {
+    int32_t block_m;      /* rows of C per MMA tile: 128 (one SM) or 256 (SM pair) */
+    int32_t block_n;      /* columns of C per tile: 64, 128, 192 or 256 */
+    int32_t splits;       /* K split factor S (1 = no split) */
+    int32_t stages;       /* depth of the shared-memory operand ring */
+    int32_t group_m;      /* tile rows per raster group (L2 reuse) */
+    int32_t grid;         /* CTAs launched (persistent) */
+    int64_t units;        /* work units = tiles * splits */
+    int64_t workspace_bytes; /* split-K partial buffer owned by the plan */
+    int32_t timeout_ms;   /* limit of every device-side wait */
+    int32_t debug_flags;  /* tests only: TSGEMM_DEBUG_* */
+} tsgemm_config_t;
+
+/* Tests only: the producer skips the first operand load of the first work
+ * unit, so the consumer's wait runs out; the launch ends with
+ * TSGEMM_ERR_TIMEOUT in the status word instead of hanging. */
+#define TSGEMM_DEBUG_SKIP_FIRST_LOAD 1
+
+/* Validate the problem, check that the current device is CC 10.3, choose the
+ * tile shape, split factor and grid, and allocate the plan's device buffers
+ * (status word; split-K workspace and tile counters when S > 1).  The plan
+ * owns those buffers.  On success *out holds the plan; on failure *out is
+ * NULL. */
+TSGEMM_API tsgemm_status_t tsgemm_plan(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t K,
+                            tsgemm_dtype_t dtype_in, tsgemm_dtype_t dtype_out,
+                            tsgemm_layout_t layout);
+
+/* tsgemm_plan with some configuration fields forced (see tsgemm_config_t).
+ * `force` may be NULL.  A forced value the kernel cannot run returns
+ * TSGEMM_ERR_UNSUPPORTED. */
+TSGEMM_API tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t K,
+                               tsgemm_dtype_t dtype_in, tsgemm_dtype_t dtype_out,
+                               tsgemm_layout_t layout, const tsgemm_config_t* force);
+
+/* Enqueue C = A * B on `stream` (a cudaStream_t; NULL is the legacy default
+ * stream).  Asynchronous: returns after the launch.  Checks pointer
+ * alignment and that A, B, C are device memory on the plan's device.  The
+ * operand descriptors are re-encoded only when a pointer changed since the
+ * previous call.  A plan may be in flight on one stream at a time (its
+ * split-K workspace is not re-entrant). */
+TSGEMM_API tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, void* C,
+                           void* stream);
+
+/* Free the plan and its device buffers.  The caller must make sure no run of
+ * the plan is still executing.  NULL is accepted. */
+TSGEMM_API tsgemm_status_t tsgemm_destroy(tsgemm_plan_t plan);
+
+/* The device status word of the plan: TSGEMM_OK, or TSGEMM_ERR_TIMEOUT when a
+ * bounded wait of an earlier run expired.  Call after synchronising the
+ * stream of the runs.  Reading a timeout clears the word and resets the
+ * split-K tile counters so the plan can run again. */
+TSGEMM_API tsgemm_status_t tsgemm_status(tsgemm_plan_t plan);
+
+/* The configuration the plan runs with. */
+TSGEMM_API tsgemm_status_t tsgemm_get_config(tsgemm_plan_t plan, tsgemm_config_t* out);
+
+/* The planner alone, host only (no GPU needed): the configuration
+ * tsgemm_plan_ex would choose for this problem on a device with `num_sms`
+ * SMs.  Same validation and return codes as tsgemm_plan_ex, except that the
+ * device is not queried. */
+TSGEMM_API tsgemm_status_t tsgemm_choose_config(int64_t M, int64_t N, int64_t K,
+                                     tsgemm_dtype_t dtype_in, tsgemm_dtype_t dtype_out,
+                                     tsgemm_layout_t layout, int32_t num_sms,
+                                     const tsgemm_config_t* force, tsgemm_config_t* out);
+
+/* A static English description of a status code. */
+TSGEMM_API const char* tsgemm_status_string(tsgemm_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSGEMM_H */

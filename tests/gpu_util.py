@@ -1,0 +1,39 @@
+"""Helpers shared by the GPU tests: move 16-bit input bits to the device, run
+a plan through the C ABI and bring the output back as raw bits."""
+import numpy as np
+import torch
+
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def to_dev(bits, din, device="cuda"):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+    return t.view(TORCH_DT[din])
+
+
+def from_dev(C, dout):
+    c = C.cpu()
+    if dout == "f32":
+        return c.numpy()
+    return c.view(torch.int16).numpy().view(np.uint16)
+
+
+def run_gemm(A_bits, B_bits, din, dout, device="cuda", repeat=1, **force):
+    """C = A * B through tsgemm; returns (C bits/values, plan config)."""
+    from hierarchical_gemm_gb300 import tsgemm
+    M, K = A_bits.shape
+    N = B_bits.shape[1]
+    plan = tsgemm.Plan(M, N, K, din, dout, **force)
+    A = to_dev(A_bits, din, device)
+    B = to_dev(B_bits, din, device)
+    C = torch.full((M, N), float("nan"), dtype=TORCH_DT[dout], device=device)
+    outs = []
+    for _ in range(repeat):
+        plan.run(A, B, C)
+        torch.cuda.synchronize()
+        st = plan.status()
+        assert st == 0, "device status %d (%s)" % (st, tsgemm.status_string(st))
+        outs.append(from_dev(C, dout))
+    cfg = plan.config
+    plan.close()
+    return (outs if repeat > 1 else outs[0]), cfg

@@ -1,0 +1,138 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every entry point the header declares, status strings, argument
+validation and the planner's choices."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tsgemm.h")
+
+
+@pytest.fixture(scope="module")
+def ts():
+    from hierarchical_gemm_gb300 import build
+    build.build()
+    from hierarchical_gemm_gb300 import tsgemm
+    return tsgemm
+
+
+def _declared():
+    text = open(HEADER).read()
+    return set(re.findall(r"TSGEMM_API\s+[\w\s\*]+?\b(tsgemm_\w+)\s*\(", text))
+
+
+def test_library_exports_every_declared_symbol(ts):
+    names = _declared()
+    assert {"tsgemm_plan", "tsgemm_run", "tsgemm_destroy"} <= names
+    lib = ctypes.CDLL(ts.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert names == set(ts.EXPORTS)
+
+
+def test_status_strings(ts):
+    seen = set()
+    for code in range(7):
+        s = ts.status_string(code)
+        assert s and s != "unknown status"
+        seen.add(s)
+    assert len(seen) == 7
+    assert ts.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 64, 64, "bf16", "bf16"), 1),
+    ((64, -1, 64, "bf16", "bf16"), 1),
+    ((64, 64, 0, "bf16", "bf16"), 1),
+    ((64, 64, 64, "f16", "bf16"), 2),
+    ((64, 64, 64, "bf16", "f16"), 2),
+    ((64, 64, 64, "f32", "f32"), 2),
+    ((64, 64, 12, "bf16", "bf16"), 3),   # A row = 24 bytes
+    ((64, 12, 64, "bf16", "f32"), 3),    # B row = 24 bytes
+    ((64, 64, 2 ** 31, "bf16", "bf16"), 2),
+])
+def test_choose_config_validation(ts, args, code):
+    with pytest.raises(ts.TsgemmError) as e:
+        ts.choose_config(*args, num_sms=152)
+    assert e.value.status == code
+
+
+def test_choose_config_rejects_bad_forced_values(ts):
+    for force, code in [({"block_n": 96}, 2), ({"block_n": 320}, 2), ({"block_m": 64}, 2),
+                        ({"splits": 100}, 2), ({"stages": 1}, 2), ({"stages": 40}, 2),
+                        ({"splits": -1}, 1), ({"units": 5}, 1)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(128, 128, 1024, "bf16", "bf16", 152, **force)
+        assert e.value.status == code, force
+
+
+def test_bad_layout_and_null_output(ts):
+    cfg = ts.Config()
+    f = ts.Config()
+    assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, 1, 152, ctypes.byref(f), ctypes.byref(cfg)) == 2
+    assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, -1, 152, ctypes.byref(f), ctypes.byref(cfg)) == 1
+    assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, 0, 152, ctypes.byref(f), None) == 1
+    assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, 0, 0, ctypes.byref(f), ctypes.byref(cfg)) == 1
+
+
+def _ceil(a, b):
+    return (a + b - 1) // b
+
+
+@pytest.mark.parametrize("shape", [
+    (256, 256, 256, "f16", "f32"), (4096, 4096, 4096, "bf16", "bf16"),
+    (128, 28672, 8192, "bf16", "bf16"), (16384, 16384, 8192, "bf16", "bf16"),
+    (1024, 1024, 65536, "bf16", "f32"), (129, 264, 72, "f16", "f16"), (1, 8, 8, "bf16", "bf16")])
+@pytest.mark.parametrize("sms", [148, 152])
+def test_planner_invariants(ts, shape, sms):
+    M, N, K, din, dout = shape
+    c = ts.choose_config(M, N, K, din, dout, sms)
+    tiles = _ceil(M, 128) * _ceil(N, c["block_n"])
+    assert c["block_m"] == 128 and c["block_n"] in (64, 128, 192, 256)
+    assert c["units"] == tiles * c["splits"]
+    assert 1 <= c["splits"] <= _ceil(K, 64)
+    assert 1 <= c["grid"] <= min(sms, c["units"])
+    assert c["workspace_bytes"] == (tiles * c["splits"] * 128 * c["block_n"] * 4 if c["splits"] > 1 else 0)
+    stage = 128 * 64 * 2 + c["block_n"] * 64 * 2
+    assert 1024 + c["stages"] * stage + 8 * (2 * c["stages"] + 6) + 16 <= 232448
+    assert c["timeout_ms"] == 1000
+
+
+def test_planner_choices_for_the_workloads(ts):
+    # The skinny weight-streaming shape fills the GPU with one wave of
+    # 128 x 192 tiles and no split; the long-K shape is split.
+    c = ts.choose_config(128, 28672, 8192, "bf16", "bf16", 152)
+    assert c["block_n"] == 192 and c["splits"] == 1 and c["grid"] == 150
+    c = ts.choose_config(1024, 1024, 65536, "bf16", "f32", 152)
+    assert c["splits"] > 1
+    c = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152)
+    assert c["splits"] == 1
+
+
+def test_forced_fields_are_honoured(ts):
+    c = ts.choose_config(1000, 1000, 4096, "bf16", "bf16", 152, block_n=128, splits=5, stages=3,
+                         group_m=4, grid=7, timeout_ms=50)
+    assert (c["block_n"], c["splits"], c["stages"], c["group_m"], c["grid"], c["timeout_ms"]) == \
+        (128, 5, 3, 4, 7, 50)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_plan_without_a_gpu_fails_cleanly(ts):
+    with pytest.raises(ts.TsgemmError) as e:
+        ts.Plan(128, 128, 128, "bf16", "bf16")
+    assert e.value.status == ts.ERR_CUDA
+
+
+def test_run_and_status_reject_null_plan(ts):
+    assert ts.lib.tsgemm_run(None, 16, 16, 16, None) == ts.ERR_INVALID_ARG
+    assert ts.lib.tsgemm_status(None) == ts.ERR_INVALID_ARG
+    assert ts.lib.tsgemm_get_config(None, None) == ts.ERR_INVALID_ARG
+    assert ts.lib.tsgemm_destroy(None) == ts.OK
+    h = ctypes.c_void_p(1)
+    assert ts.lib.tsgemm_plan(ctypes.byref(h), 0, 8, 8, 1, 1, 0) == ts.ERR_INVALID_ARG
+    assert h.value is None  # *out is cleared on failure
+    assert ts.lib.tsgemm_plan(None, 8, 8, 8, 1, 1, 0) == ts.ERR_INVALID_ARG
