@@ -135,9 +135,25 @@ def gemm_sampled(A_bits, B_bits, dtype_in, rows, cols):
 #   * exact mode (integer-valued inputs whose fp32 partial sums are all
 #     exact): the output must equal the oracle's sum rounded to the output
 #     format, bit for bit;
-#   * otherwise |C - ref| <= RTOL * sabs + ATOL per element.
+#   * otherwise |C - ref| <= RTOL * sabs + ATOL per element for the fp32
+#     accumulated value; a 16-bit output is that value rounded once more
+#     (to nearest, ties to even), which may add up to half a unit in the
+#     last place of the output format, so for f16/bf16 outputs the bound is
+#     RTOL * sabs + ATOL + half_ulp(max(|ref|, |C|)).
 RTOL = 1e-3
 ATOL = 1e-5
+
+# (fraction bits, smallest normal exponent) of the 16-bit output formats
+_FMT = {F16: (10, -14), BF16: (7, -126)}
+
+
+def half_ulp(x, dtype_out):
+    """Half the spacing of the 16-bit format's numbers at |x| (elementwise)."""
+    fb, emin = _FMT[dtype_code(dtype_out)]
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    _, e2 = np.frexp(a)            # a = m * 2^e2, m in [0.5, 1)
+    E = np.where(a > 0, np.maximum(e2 - 1, emin), emin)  # subnormals and 0 share emin
+    return np.ldexp(1.0, E - fb - 1)
 
 
 def output_values(C, dtype_out):
@@ -171,6 +187,9 @@ def accept(C, ref, sabs, dtype_out, exact=False):
     cv = output_values(C, code)
     err = np.abs(cv - ref)
     bound = RTOL * sabs + ATOL
+    if code != F32:
+        with np.errstate(invalid="ignore"):
+            bound = bound + half_ulp(np.fmax(np.abs(ref), np.abs(cv)), code)
     bad = ~(err <= bound)  # NaN counts as bad
     nbad = int(bad.sum())
     ratio = err / bound

@@ -356,3 +356,38 @@ def test_planted_mistakes_are_caught():
     assert _pins_pass(good)
     for bad in (drops_last_k, transposes_B, flips_sign, wrong_format):
         assert not _pins_pass(bad), bad.__name__
+
+
+def test_half_ulp_matches_the_format_spacing():
+    # spacing of bf16 numbers in [1, 2) is 2^-7; of fp16 is 2^-10
+    assert oracle.half_ulp(1.0, BF16) == 2.0 ** -8
+    assert oracle.half_ulp(1.99, BF16) == 2.0 ** -8
+    assert oracle.half_ulp(2.0, BF16) == 2.0 ** -7
+    assert oracle.half_ulp(1.0, F16) == 2.0 ** -11
+    assert oracle.half_ulp(-65504.0, F16) == 16.0
+    # subnormal range: fixed spacing 2^-24 (fp16), 2^-133 (bf16)
+    assert oracle.half_ulp(2.0 ** -20, F16) == 2.0 ** -25
+    assert oracle.half_ulp(0.0, BF16) == 2.0 ** -134
+    # neighbouring representable values are two half-ulps apart
+    for dt, one_up in ((BF16, 0x3F81), (F16, 0x3C01)):
+        gap = oracle.decode(np.array([one_up], dtype=np.uint16), dt)[0] - 1.0
+        assert gap == 2 * oracle.half_ulp(1.0, dt)
+
+
+def test_accept_admits_the_correctly_rounded_16_bit_output():
+    # With K small |ref| can approach sabs, where half a bf16 ulp exceeds
+    # 1e-3 * sabs; the correctly rounded output must still be accepted and
+    # one ulp further must not.
+    r = _rng(80)
+    ref = r.uniform(-4, 4, 5000)
+    sabs = np.abs(ref) * 1.0001
+    for dt in (BF16, F16):
+        C = oracle.round_out(ref, dt)
+        ok, info = oracle.accept(C, ref, sabs, dt)
+        assert ok, info
+        # move one element far enough that it exceeds 1e-3 * sabs plus half
+        # an ulp: 2 bf16 ulps (2^-6 relative) or 8 fp16 ulps (2^-7 relative)
+        off = C.copy()
+        off[0] = off[0] + (2 if dt == BF16 else 8)
+        ok, info = oracle.accept(off, ref, sabs, dt)
+        assert not ok and info["mismatches"] == 1
