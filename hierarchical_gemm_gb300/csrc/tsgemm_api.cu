@@ -139,8 +139,10 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     // Ask for more than half the SM's shared memory even when the ring is
     // shallow, so one CTA owns each SM and its tensor memory.
     const int64_t smem = need > tsg::kSmemPerCtaMax / 2 + 1024 ? need : tsg::kSmemPerCtaMax / 2 + 1024;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess) {
+    // The attribute is per kernel, shared by every plan that uses it: set it
+    // to the largest size any launch asks for, never lower.
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(tsg::kSmemPerCtaMax)) != cudaSuccess) {
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;
     }
