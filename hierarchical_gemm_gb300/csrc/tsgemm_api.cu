@@ -98,6 +98,7 @@ const char* tsgemm_status_string(tsgemm_status_t s) {
         case TSGEMM_ERR_CUDA: return "CUDA call failed";
         case TSGEMM_ERR_TIMEOUT: return "a bounded device wait expired";
         case TSGEMM_ERR_OOM: return "out of device memory";
+        case TSGEMM_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch of the no-allocation entry point";
         default: return "unknown status";
     }
 }

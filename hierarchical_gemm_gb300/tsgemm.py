@@ -20,6 +20,7 @@ ERR_ALIGNMENT = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
 ERR_OOM = 6
+ERR_SCRATCH_LIMIT = 7
 
 DEBUG_SKIP_FIRST_LOAD = 1
 
@@ -30,7 +31,7 @@ _DTYPE_NAMES = {"f16": F16, "fp16": F16, "float16": F16, "half": F16,
 # Every entry point include/tsgemm.h declares.
 EXPORTS = ("tsgemm_plan", "tsgemm_plan_ex", "tsgemm_run", "tsgemm_destroy",
            "tsgemm_status", "tsgemm_get_config", "tsgemm_choose_config",
-           "tsgemm_status_string")
+           "tsgemm_status_string", "tsgemm_run_splitk_noalloc")
 
 
 class Config(ctypes.Structure):
@@ -69,6 +70,8 @@ def _load():
     L.tsgemm_choose_config.argtypes = [i64, i64, i64, i32, i32, i32, i32, cfgp, cfgp]
     L.tsgemm_status_string.restype = ctypes.c_char_p
     L.tsgemm_status_string.argtypes = [i32]
+    L.tsgemm_run_splitk_noalloc.restype = i32
+    L.tsgemm_run_splitk_noalloc.argtypes = [i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp]
     return L
 
 
@@ -203,3 +206,18 @@ def gemm(A, B, out_dtype=None, C=None, stream=None):
     if C is None:
         C = torch.empty((M, N), dtype=getattr(torch, _TORCH_OUT[dout]), device=A.device)
     return plan.run(A, B, C, stream)
+
+
+def run_splitk_noalloc(A, B, C, splits=0, status=None, stream=None):
+    """C = A * B through the entry point that allocates nothing (its split-K
+    scratch is a fixed device array inside the library).  A (M x K), B
+    (K x N), C (M x N) are CUDA tensors or raw device pointers; `status` an
+    optional device int tensor that receives a device-side timeout."""
+    M, K = A.shape
+    N = B.shape[1]
+    din = dtype_code(A.dtype)
+    dout = dtype_code(C.dtype)
+    _check(lib.tsgemm_run_splitk_noalloc(M, N, K, din, dout, int(splits), _ptr(A), _ptr(B),
+                                         _ptr(C), _ptr(status), _stream_handle(stream)),
+           "tsgemm_run_splitk_noalloc")
+    return C

@@ -71,7 +71,9 @@ typedef enum {
     TSGEMM_ERR_ALIGNMENT = 3,   /* pointer or row stride not 16-byte aligned */
     TSGEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
     TSGEMM_ERR_TIMEOUT = 5,     /* a bounded device wait expired */
-    TSGEMM_ERR_OOM = 6          /* plan could not allocate its buffers */
+    TSGEMM_ERR_OOM = 6,         /* plan could not allocate its buffers */
+    TSGEMM_ERR_SCRATCH_LIMIT = 7 /* problem needs more than the fixed scratch of
+                                    tsgemm_run_splitk_noalloc */
 } tsgemm_status_t;
 
 /* Execution configuration of a plan.  In tsgemm_plan_ex every field left at
@@ -143,6 +145,54 @@ TSGEMM_API tsgemm_status_t tsgemm_choose_config(int64_t M, int64_t N, int64_t K,
 
 /* A static English description of a status code. */
 TSGEMM_API const char* tsgemm_status_string(tsgemm_status_t s);
+
+/* ---- Split-K GEMM without any allocation -------------------------------
+ *
+ * The pages this library follows have no counterpart of this entry point;
+ * it exists for callers that cannot allocate device memory.  tsgemm_plan
+ * allocates its split-K workspace, tile counters and status word with
+ * cudaMalloc.  Some callers cannot do that: code that runs inside another
+ * framework's allocator or memory hooks (where allocating would re-enter
+ * it), plug-ins that are handed their buffers and own no allocator, and
+ * real-time loops that forbid cudaMalloc/cudaFree after start-up because
+ * those calls can synchronise the whole device.  This entry point needs no
+ * plan: the split-K scratch lives in one fixed device array inside the
+ * library (TSGEMM_NOALLOC_SCRATCH_BYTES, about 32 MiB), which every GPU that
+ * loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Computes C = A * B exactly like tsgemm_run with the K dimension split in
+ * `splits` parts (0 lets the planner choose; 1 means no split).  A, B, C as
+ * for tsgemm_run: device memory of the current device, 16-byte aligned, C
+ * overlapping neither A nor B.  `status` may be NULL; otherwise it is a
+ * device int (or mapped pinned host int) the kernel sets to
+ * TSGEMM_ERR_TIMEOUT if a bounded device wait expires (it is cleared to 0
+ * on `stream` before the launch).
+ *
+ * Limits: at most TSGEMM_NOALLOC_MAX_TILES output tiles and at most
+ * TSGEMM_NOALLOC_WS_BYTES of fp32 partials (S * tiles * 128 * block_n * 4
+ * bytes); larger problems return TSGEMM_ERR_SCRATCH_LIMIT before anything is
+ * enqueued.
+ *
+ * Every call uses the same scratch array, which keeps the previous call's
+ * contents; each call clears the tile counters it needs on `stream` before
+ * its launch.  Calls whose kernels overlap on the GPU (on different streams,
+ * or from different host threads without ordering) race on that array and
+ * give wrong results: order them on one stream.
+ *
+ * The first call on each device does a one-time set-up with that device
+ * current (it looks up the device address of the scratch array and sets the
+ * kernels' shared-memory limit); make that first call before any stream
+ * capture.  Asynchronous otherwise: returns after the launch. */
+#define TSGEMM_NOALLOC_MAX_TILES 16384
+#define TSGEMM_NOALLOC_WS_BYTES (32u << 20)
+#define TSGEMM_NOALLOC_SCRATCH_BYTES (256u + TSGEMM_NOALLOC_MAX_TILES * 4u + TSGEMM_NOALLOC_WS_BYTES)
+
+TSGEMM_API tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K,
+                                                     tsgemm_dtype_t dtype_in,
+                                                     tsgemm_dtype_t dtype_out, int32_t splits,
+                                                     const void* A, const void* B, void* C,
+                                                     int* status, void* stream);
 
 #ifdef __cplusplus
 }

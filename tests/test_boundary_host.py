@@ -36,11 +36,11 @@ def test_library_exports_every_declared_symbol(ts):
 
 def test_status_strings(ts):
     seen = set()
-    for code in range(7):
+    for code in range(8):
         s = ts.status_string(code)
         assert s and s != "unknown status"
         seen.add(s)
-    assert len(seen) == 7
+    assert len(seen) == 8
     assert ts.status_string(99) == "unknown status"
 
 
