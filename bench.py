@@ -41,8 +41,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # Source files whose change invalidates a stored ncu traffic figure.
 KERNEL_SOURCES = ["hierarchical_gemm_gb300/csrc/gemm_sm103.cuh",
+                  "hierarchical_gemm_gb300/csrc/gemm_sm103_2sm.cuh",
                   "hierarchical_gemm_gb300/csrc/ptx.cuh",
-                  "hierarchical_gemm_gb300/csrc/kernels_1sm.cu"]
+                  "hierarchical_gemm_gb300/csrc/kernels_1sm.cu",
+                  "hierarchical_gemm_gb300/csrc/kernels_2sm.cu"]
 
 
 def parse_args(argv=None):
@@ -57,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=0, help="default: min(steps, 50)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--plan", default="",
+                    help="force plan fields, e.g. block_m=256,block_n=128,splits=1")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -305,7 +309,8 @@ def run_ours(args):
     A = torch.from_numpy(A_np.view(np.int16)).to(dev).view(tdt[din])
     B = torch.from_numpy(B_np.view(np.int16)).to(dev).view(tdt[din])
     C = torch.empty((M, N), dtype=tdt[dout], device=dev)
-    plan = tsgemm.Plan(M, N, K, din, dout)
+    force = {k: int(v) for k, v in (kv.split("=") for kv in args.plan.split(",") if kv)}
+    plan = tsgemm.Plan(M, N, K, din, dout, **force)
     cfg = plan.config
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -404,7 +409,7 @@ def run_ours(args):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": stored_traffic(w["name"]),
                 "peak_kind": peak_kind + " bf16 burst (cuBLAS-class torch.matmul)",
-                "kernel": "gemm_sm103_1sm<BN=%d>" % cfg["block_n"],
+                "kernel": "gemm_sm103_%s<BN=%d>" % ("2sm" if cfg["block_m"] == 256 else "1sm", cfg["block_n"]),
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": 2 * (M * K + K * N) + (4 if dout == "f32" else 2) * M * N}
 

@@ -24,9 +24,10 @@
 //   * persistent thread blocks (TileScale roadmap, resource control): every
 //     CTA walks a static list of work units;
 //   * the K split with a reduction (TileScale README, "Example of GEMM",
-//     warpgroups split along K and reduce): work units may cover a K range
-//     of a tile; partial tiles go to an fp32 workspace and the CTA that
-//     finishes a tile last adds the partials in split order 0..S-1.
+//     warpgroups split along K and reduce): a work unit may cover a K range
+//     of a tile (all tiles, or only those of the last, partial wave);
+//     partial tiles go to an fp32 workspace and the CTA that finishes a
+//     tile last adds the partials in split order 0..S-1.
 //
 // Every wait is bounded in time (see WaitCtl); a CTA that gives up records a
 // timeout in the status word, lets its in-flight copies and MMAs finish,
@@ -49,72 +50,211 @@ enum OutKind { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2 };
 struct GemmParams {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n;
-    int32_t splits;       // S
+    int32_t splits;       // S: K parts of each split tile
     int32_t kblocks;      // ceil(K / kBK)
     int32_t group_m;      // raster group height in tiles
     int32_t stages;
     int32_t debug_flags;
-    int64_t units;        // tiles_m * tiles_n * S
+    int64_t full_tiles;   // tiles [0, full_tiles) of the schedule are not split
+    int64_t units;        // full_tiles + (tiles - full_tiles) * S
     uint32_t idesc;       // tcgen05 instruction descriptor
     uint32_t pad_;
     void* C;
-    float* ws;            // [tile][split][kBM][BN] fp32 partials (S > 1)
-    int* counters;        // [tile] arrival counters, zero between launches
+    float* ws;            // fp32 partials of the split tiles (S > 1)
+    int* counters;        // arrival counters of the split tiles, zero between launches
     int* status;          // plan status word
     uint64_t timeout_ns;
 };
 
-// Work unit u -> (tile row tm, tile column tn, split, linear tile).  Units
-// of one tile are adjacent so its splits run at the same time; tiles are
+// One work unit: a whole tile, or one of the S K-parts of a split tile.
+struct Unit {
+    int tm, tn;      // tile row and column
+    int split;       // K part of this unit
+    int nsplit;      // 1: the whole tile
+    int kb0, kb1;    // K-slices [kb0, kb1)
+    int64_t slot;    // index of the tile among the split tiles (nsplit > 1)
+};
+
+// Work unit u of the static schedule.  The first full_tiles units are whole
+// tiles; after them come the split tiles, their S parts adjacent so that
+// they run at the same time (the split tiles are the schedule's last, so
+// splitting fills the last, partial wave of tiles).  Linear tiles are
 // rastered in groups of `group_m` tile rows so that concurrently running
-// CTAs share B panels (and A panels) in L2.
-__device__ __forceinline__ void unit_coords(const GemmParams& p, int64_t u, int& tm, int& tn,
-                                            int& split, int64_t& tile) {
-    tile = u / p.splits;
-    split = static_cast<int>(u - tile * p.splits);
+// CTAs share A and B panels in L2.
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int64_t u) {
+    Unit r;
+    int64_t tile;
+    if (u < p.full_tiles || p.splits == 1) {
+        tile = u;
+        r.split = 0;
+        r.nsplit = 1;
+        r.slot = -1;
+    } else {
+        const int64_t v = u - p.full_tiles;
+        const int64_t t = v / p.splits;
+        tile = p.full_tiles + t;
+        r.split = static_cast<int>(v - t * p.splits);
+        r.nsplit = p.splits;
+        r.slot = t;
+    }
     const int64_t span = static_cast<int64_t>(p.group_m) * p.tiles_n;
     const int64_t group = tile / span;
     const int first_m = static_cast<int>(group * p.group_m);
     const int gm = min(p.tiles_m - first_m, p.group_m);
-    const int64_t r = tile - group * span;
-    tm = first_m + static_cast<int>(r % gm);
-    tn = static_cast<int>(r / gm);
+    const int64_t rr = tile - group * span;
+    r.tm = first_m + static_cast<int>(rr % gm);
+    r.tn = static_cast<int>(rr / gm);
+    r.kb0 = static_cast<int>(static_cast<int64_t>(r.split) * p.kblocks / r.nsplit);
+    r.kb1 = static_cast<int>(static_cast<int64_t>(r.split + 1) * p.kblocks / r.nsplit);
+    return r;
 }
 
-__device__ __forceinline__ void split_range(const GemmParams& p, int split, int& kb0, int& kb1) {
-    kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks / p.splits);
-    kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks / p.splits);
-}
+// Shared-memory staging of the output: each epilogue warp owns two buffers
+// of one 32 x 32 block (rows = its 32 accumulator lanes, 32 columns), filled
+// from registers and written to C by a TMA tensor store, so that global
+// writes are whole lines and rows or columns past the edge of C are clipped
+// by the copy engine.  The block is laid out in the tensor map's swizzle
+// (128-byte for fp32 rows, 64-byte for 16-bit rows); buffers are 1024-byte
+// aligned, as the swizzle patterns require.
+constexpr uint32_t kEpiBufBytes = 32 * 32 * 4;              // fp32 block (largest)
+constexpr uint32_t kEpiSmemBytes = (kEpiThreads / 32) * 2 * kEpiBufBytes;  // 32 KiB
 
-// Store 32 consecutive fp32 accumulator columns of one row of C, starting at
-// column col0, converted to the output format.  Columns at or past N are
-// skipped 16 bytes at a time (N * 2 is a multiple of 16, so a 16-byte vector
-// is either wholly inside the row or wholly outside).
 template <int kOut>
-__device__ __forceinline__ void store_row32(const GemmParams& p, int row, int col0,
-                                            const uint32_t (&r)[32]) {
-    if (row >= p.M) return;
-    if constexpr (kOut == kOutF32) {
-        float* dst = static_cast<float*>(p.C) + static_cast<int64_t>(row) * p.N + col0;
+struct CStager {
+    uint32_t buf0;   // this warp's first buffer; the second follows it
+    uint32_t which;  // buffer to fill next
+    int lane;
+
+    // Convert 32 fp32 values (this lane's row, 32 consecutive columns) and
+    // store the warp's 32 x 32 block at (row0, col0) of C.
+    __device__ __forceinline__ void put(const GemmParams& p, const CUtensorMap* tmC, int row0, int col0,
+                                        const uint32_t (&r)[32]) {
+        const uint32_t buf = buf0 + which * kEpiBufBytes;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that used `buf` last has read it
+        __syncwarp();
+        if constexpr (kOut == kOutF32) {
+            // 128-byte rows in the TMA 128-byte swizzle: 16-byte chunk j of
+            // row l sits at chunk position j ^ (l mod 8), so the 8 lanes of
+            // each store phase hit distinct banks
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-            if (col0 + 4 * v < p.N) st_global_v4(dst + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-    } else {
-        uint16_t* dst = static_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.N + col0;
+            for (int j = 0; j < 8; ++j)
+                st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                             r[4 * j + 3]);
+        } else {
+            uint32_t w[16];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            if (col0 + 8 * v < p.N) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float lo = __uint_as_float(r[8 * v + 2 * i]);
-                    const float hi = __uint_as_float(r[8 * v + 2 * i + 1]);
-                    w[i] = kOut == kOutBF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
-                }
-                st_global_v4(dst + 8 * v, w[0], w[1], w[2], w[3]);
+            for (int i = 0; i < 16; ++i) {
+                const float lo = __uint_as_float(r[2 * i]), hi = __uint_as_float(r[2 * i + 1]);
+                w[i] = kOut == kOutBF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
             }
+            // 64-byte rows in the TMA 64-byte swizzle: chunk j of row l sits
+            // at chunk position j ^ ((l / 2) mod 4)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                             w[4 * j + 3]);
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+            if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, buf, col0, row0);
+            bulk_commit_group();  // (an empty group when the block is wholly outside C)
+        }
+        which ^= 1u;
+    }
+
+    // All of this warp's stores have completed.
+    __device__ __forceinline__ void drain() {
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+};
+
+// Drain one work unit's accumulator (128 rows x BN columns of tensor memory
+// at `tbase`; this thread holds row `row_local`, and its warp's 32 rows
+// start at row `row0` of C).
+//   * A whole tile is converted and stored to C.
+//   * Part s of a tile split along K adds itself to the running sum of the
+//     parts before it: it waits until the tile's counter says parts
+//     0..s-1 are done, reads the running sum from the workspace, adds its
+//     own accumulator (running + own, in fp32), and either writes the sum
+//     back and advances the counter, or -- the last part -- stores C and
+//     resets the counter.  The sum is thus p_0 + p_1 + ... + p_{S-1}, added
+//     in split order, the same bits on every run.
+// `h` indexes the workspace tile and counter of this 128-row half;
+// `epi_sync` is the epilogue warpgroup's bounded barrier and `release` hands
+// the accumulator back to the MMA issuer.  Returns false if the CTA is
+// aborting.
+template <int BN, int kOut, class Sync, class Release>
+__device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
+                                           const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
+                                           int etid, volatile int* flag, const WaitCtl& ctl, Sync&& epi_sync,
+                                           Release&& release) {
+    const int col0 = un.tn * BN;
+    if (un.nsplit == 1) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c, r);
+            tmem_ld_wait();
+            if (c + 32 >= BN) release();  // the accumulator is in registers now
+            out.put(p, tmC, row0, col0 + c, r);
+        }
+        return true;
+    }
+    if (un.split > 0) {
+        if (etid == 0) *flag = wait_flag_bounded(p.counters + h, un.split, ctl) ? 1 : 0;
+        if (!epi_sync()) return false;
+        if (!*flag) return false;
+        __threadfence();
+    }
+    const bool last = un.split == un.nsplit - 1;
+    // The running sum of a 128 x BN half tile is stored in the order the
+    // epilogue warps hold it, so that every warp access is 512 contiguous
+    // bytes: [BN/32 column chunks][4 lane quarters][8 float4][32 lanes].
+    const int q = row_local >> 5, lane = row_local & 31;
+    float* run = p.ws + h * (kBM * BN) + q * (8 * 128) + lane * 4;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c, r);
+        float* rc = run + (c >> 5) * (4 * 8 * 128);  // this chunk, this thread
+        if (un.split > 0) {
+            float4 prev[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) prev[v] = ld_global_cg_f4(rc + v * 128);
+            tmem_ld_wait();
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                r[4 * v] = __float_as_uint(__fadd_rn(prev[v].x, __uint_as_float(r[4 * v])));
+                r[4 * v + 1] = __float_as_uint(__fadd_rn(prev[v].y, __uint_as_float(r[4 * v + 1])));
+                r[4 * v + 2] = __float_as_uint(__fadd_rn(prev[v].z, __uint_as_float(r[4 * v + 2])));
+                r[4 * v + 3] = __float_as_uint(__fadd_rn(prev[v].w, __uint_as_float(r[4 * v + 3])));
+            }
+        } else {
+            tmem_ld_wait();
+            // the sum starts from a cleared (+0) accumulator
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fadd_rn(0.0f, __uint_as_float(r[i])));
+        }
+        if (last) {
+            out.put(p, tmC, row0, col0 + c, r);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                st_global_v4(rc + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
         }
     }
+    release();
+    if (!last) {
+        __threadfence();  // the running sum is visible before the counter moves
+        if (!epi_sync()) return false;
+        if (etid == 0) st_release_gpu(p.counters + h, un.split + 1);
+    } else if (etid == 0) {
+        p.counters[h] = 0;  // ready for the next launch
+    }
+    // no thread may still be reading `flag` when the next unit rewrites it
+    return epi_sync();
 }
 
 template <int BN>
@@ -132,14 +272,14 @@ struct TileShape {
 // Bytes of dynamic shared memory the kernel needs for `stages` slots.
 template <int BN>
 __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
-    return 1024u /* alignment slack */ + stages * TileShape<BN>::kStageBytes +
+    return 1024u /* alignment slack */ + stages * TileShape<BN>::kStageBytes + kEpiSmemBytes +
            8u * (2 * stages + 6) /* barriers */ + 16u /* tmem holder, flags */;
 }
 
 template <int BN, int kOut>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_sm103_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     using TS = TileShape<BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -147,14 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
     const int S = p.stages;
 
-    const uint32_t bars = base + S * TS::kStageBytes;
+    const uint32_t epi_smem = base + S * TS::kStageBytes;  // output staging
+    const uint32_t bars = epi_smem + kEpiSmemBytes;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     const uint32_t epi_bar = bars + 8u * (2 * S + 5);
-    uint8_t* misc = base_ptr + S * TS::kStageBytes + 8u * (2 * S + 6);
+    uint8_t* misc = base_ptr + S * TS::kStageBytes + kEpiSmemBytes + 8u * (2 * S + 6);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
@@ -178,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
     }
     if (warp == 1) tmem_alloc<1>(smem_u32(tmem_holder), TS::kTmemCols);
     tc_fence_before();
@@ -188,19 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
+        // (lane 0 alone runs the loop; the warp reconverges below)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t outstanding = 0, out_parity = 0;  // loads not yet seen complete
+            uint32_t outstanding = 0, out_parity = 0;  // loads issued, per slot
             bool skip = (p.debug_flags & 1) && blockIdx.x == 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int tm, tn, split;
-                int64_t tile;
-                unit_coords(p, u, tm, tn, split, tile);
-                int kb0, kb1;
-                split_range(p, split, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const Unit un = decode_unit(p, u);
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, ctl)) {
                         ok = false;
                         break;
@@ -210,11 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const uint32_t a_dst = base + stage * TS::kStageBytes;
                         mbar_arrive_expect_tx(full_bar(stage), TS::kStageBytes);
-                        tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, tm * kBM);
+                        tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, un.tm * kBM);
 #pragma unroll
                         for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(a_dst + TS::kABytes + j * 8192u, &tmB, full_bar(stage),
-                                        tn * BN + j * 64, kb * kBK);
+                            tma_load_2d(a_dst + TS::kABytes + j * 8192u, &tmB, full_bar(stage), un.tn * BN + j * 64,
+                                        kb * kBK);
                         outstanding |= 1u << stage;
                         out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -238,15 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int tm, tn, split;
-                int64_t tile;
-                unit_coords(p, u, tm, tn, split, tile);
-                int kb0, kb1;
-                split_range(p, split, kb0, kb1);
+                const Unit un = decode_unit(p, u);
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, ctl)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * TS::kAccCols;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, ctl)) {
                         ok = false;
                         break;
@@ -262,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         //    groups 1024 B apart (SBO); the k-th step is 16 rows.
                         const uint64_t ad = smem_desc_sw128(a_addr + k * 32u, 16u, 1024u);
                         const uint64_t bd = smem_desc_sw128(b_addr + k * 2048u, 8192u, 1024u);
-                        umma_f16<1>(d_tmem, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        umma_f16<1>(d_tmem, ad, bd, p.idesc, (kb > un.kb0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));  // slot free once these MMAs have read it
                     if (++stage == S) {
@@ -287,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;              // TMEM lane quarter of this warp
         const int etid = threadIdx.x - 64;   // 0..127
         const int row_local = q * 32 + lane;
+        CStager<kOut> out{epi_smem + static_cast<uint32_t>(warp - 2) * 2u * kEpiBufBytes, 0u, lane};
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t epi_phase = 0;
@@ -305,85 +441,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             return good != 0;
         };
         for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-            int tm, tn, split;
-            int64_t tile;
-            unit_coords(p, u, tm, tn, split, tile);
+            const Unit un = decode_unit(p, u);
+            const int tm = un.tm, tn = un.tn;
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, ctl) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            const int row = tm * kBM + row_local;
+            const int row0 = tm * kBM + q * 32;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TS::kAccCols;
-            if (p.splits == 1) {
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + c, r);
-                    tmem_ld_wait();
-                    store_row32<kOut>(p, row, tn * BN + c, r);
-                }
+            auto release = [&]() {
                 tc_fence_before();
                 mbar_arrive(tempty_bar(acc));
-            } else {
-                float* wsp = p.ws + (tile * p.splits + split) * (kBM * BN) + row_local * BN;
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + c, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        st_global_v4(wsp + c + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-                }
-                tc_fence_before();
-                mbar_arrive(tempty_bar(acc));
-                // Publish the partial, then count arrivals for this tile.
-                __threadfence();
-                if (!epi_sync()) break;
-                if (etid == 0) {
-                    const int old = atomicAdd(p.counters + tile, 1);
-                    *last_flag = (old == p.splits - 1) ? 1 : 0;
-                }
-                if (!epi_sync()) break;
-                if (*last_flag) {
-                    // Last CTA of this tile: C = p_0 + p_1 + ... + p_{S-1}.
-                    __threadfence();
-                    const float* t0 = p.ws + tile * p.splits * (kBM * BN) + row_local * BN;
-#pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
-                        uint32_t r[32];
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int s = 0; s < p.splits; ++s) {
-                                const float4 x = ld_global_cg_f4(t0 + static_cast<int64_t>(s) * (kBM * BN) + c + 4 * v);
-                                a4.x += x.x;
-                                a4.y += x.y;
-                                a4.z += x.z;
-                                a4.w += x.w;
-                            }
-                            r[4 * v] = __float_as_uint(a4.x);
-                            r[4 * v + 1] = __float_as_uint(a4.y);
-                            r[4 * v + 2] = __float_as_uint(a4.z);
-                            r[4 * v + 3] = __float_as_uint(a4.w);
-                        }
-                        store_row32<kOut>(p, row, tn * BN + c, r);
-                    }
-                    if (etid == 0) p.counters[tile] = 0;  // ready for the next launch
-                }
-            }
+            };
+            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, etid, last_flag, ctl,
+                                      epi_sync, release))
+                break;
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
+        out.drain();  // this warp's output stores have landed
     }
 
     // ------------------------------------------------------------ exit --
+    // A non-aligned barrier: it counts threads one by one, so warps whose
+    // lane 0 ran a role loop alone may arrive in any convergence state.
     tc_fence_before();
-    __syncthreads();
+    cta_barrier_any();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

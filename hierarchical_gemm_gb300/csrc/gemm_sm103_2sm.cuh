@@ -1,0 +1,272 @@
+// gemm_sm103_2sm.cuh -- the CTA-pair form of the persistent GEMM kernel.
+//
+// The TileScale README (section on T.Scale) describes the Blackwell
+// cluster-level GEMM as a distributed GEMM running on two SMs, and names a
+// cluster-scale GEMM primitive built on distributed shared memory.  Here two
+// CTAs of a 2 x 1 cluster compute one 256 x BN output tile together:
+//   * CTA r of the pair loads rows [128 r, 128 r + 128) of the tile's A
+//     panel and columns [r BN/2, (r + 1) BN/2) of its B panel into its own
+//     shared memory (so each SM fetches half the B bytes it would for a
+//     128 x BN tile of its own);
+//   * the pair's leader (r = 0) issues tcgen05.mma.cta_group::2 with M = 256:
+//     the tensor cores of both SMs read the A rows and B columns held by
+//     both CTAs' shared memory -- the on-chip "network" of the cluster --
+//     and each CTA's tensor memory receives its own 128 rows of the result;
+//   * both CTAs' TMA loads complete on the leader's full barrier, which
+//     expects the bytes of both; the leader's commits arrive on the empty
+//     and accumulator-full barriers of both CTAs (multicast);
+//   * each CTA's epilogue warpgroup drains its own 128 rows and tells the
+//     leader (remote mbarrier arrive) when the accumulator is free again.
+// Everything else -- the persistent schedule over work units, the split-K
+// workspace reduction, the bounded waits -- is the one-SM kernel's.
+#pragma once
+
+#include "gemm_sm103.cuh"
+
+namespace tsg {
+
+template <int BN>
+struct PairShape {
+    static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
+    static constexpr uint32_t kABytes = kBM * kBK * 2;      // this CTA's 128 rows: 16 KiB
+    static constexpr uint32_t kBCols = BN / 2;              // this CTA's B columns
+    static constexpr uint32_t kBBytes = kBCols * kBK * 2;   // kBCols / 64 boxes of 8 KiB
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kAccCols = BN <= 128 ? 128 : 256;
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+
+template <int BN>
+__host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
+    return 1024u + stages * PairShape<BN>::kStageBytes + kEpiSmemBytes + 8u * (2 * stages + 6) + 16u;
+}
+
+template <int BN, int kOut>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_sm103_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    using PS = PairShape<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const int S = p.stages;
+
+    const uint32_t epi_smem = base + S * PS::kStageBytes;  // output staging
+    const uint32_t bars = epi_smem + kEpiSmemBytes;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * S + 4);
+    const uint32_t epi_bar = bars + 8u * (2 * S + 5);
+    uint8_t* misc = base_ptr + S * PS::kStageBytes + kEpiSmemBytes + 8u * (2 * S + 6);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: leader, 1: peer
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);   // the leader's producer arrives once
+            mbar_init(empty_bar(s), 1);  // one multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);                    // one multicast commit
+            mbar_init(tempty_bar(a), 2 * kEpiThreads / 32);  // every epilogue warp of the pair
+        }
+        mbar_init(drain_bar, 1);
+        mbar_init(epi_bar, kEpiThreads / 32);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
+    }
+    if (warp == 1) tmem_alloc<2>(smem_u32(tmem_holder), PS::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised before either uses them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    ctl.peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+
+    const int64_t cluster_id = blockIdx.x >> 1;
+    const int64_t nclusters = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------------------- TMA producer (both) --
+        // (lane 0 alone runs the loop; the warp reconverges below)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t outstanding = 0, out_parity = 0;
+            bool ok = true;
+            for (int64_t u = cluster_id; ok && u < p.units; u += nclusters) {
+                const Unit un = decode_unit(p, u);
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    {
+                        const uint32_t a_dst = base + stage * PS::kStageBytes;
+                        const int32_t arow = un.tm * (2 * kBM) + static_cast<int32_t>(rank) * kBM;
+                        const int32_t bcol = un.tn * BN + static_cast<int32_t>(rank) * PS::kBCols;
+                        if (leader) {
+                            mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
+                            tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, arow);
+#pragma unroll
+                            for (int j = 0; j < static_cast<int>(PS::kBCols) / 64; ++j)
+                                tma_load_2d(a_dst + PS::kABytes + j * 8192u, &tmB, full_bar(stage), bcol + j * 64,
+                                            kb * kBK);
+                        } else {
+                            const uint32_t lbar = mapa_shared(full_bar(stage), 0u);
+                            tma_load_2d_pair(a_dst, &tmA, lbar, kb * kBK, arow);
+#pragma unroll
+                            for (int j = 0; j < static_cast<int>(PS::kBCols) / 64; ++j)
+                                tma_load_2d_pair(a_dst + PS::kABytes + j * 8192u, &tmB, lbar, bcol + j * 64,
+                                                 kb * kBK);
+                        }
+                    }
+                    outstanding |= 1u << stage;
+                    out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (int s = 0; s < S; ++s) {
+                if (!(outstanding & (1u << s))) continue;
+                const uint32_t par = (out_parity >> s) & 1u;
+                wait_bounded(leader ? full_bar(s) : empty_bar(s), par, ctl, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------ MMA issuer (leader) --
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int64_t u = cluster_id; ok && u < p.units; u += nclusters) {
+                const Unit un = decode_unit(p, u);
+                if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, ctl)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * PS::kAccCols;
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    {
+                        const uint32_t a_addr = base + stage * PS::kStageBytes;
+                        const uint32_t b_addr = a_addr + PS::kABytes;
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            const uint64_t ad = smem_desc_sw128(a_addr + k * 32u, 16u, 1024u);
+                            const uint64_t bd = smem_desc_sw128(b_addr + k * 2048u, 8192u, 1024u);
+                            umma_f16<2>(d_tmem, ad, bd, p.idesc, (kb > un.kb0 || k > 0) ? 1u : 0u);
+                        }
+                        umma_commit_pair(empty_bar(stage), 0x3);
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(tfull_bar(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            umma_commit_pair(drain_bar, 0x1);
+            wait_bounded(drain_bar, 0u, ctl, false);
+        }
+        __syncwarp();
+    } else {
+        // ----------------------------------------------- epilogue (both) --
+        const int q = warp & 3;
+        const int etid = threadIdx.x - 64;
+        const int row_local = q * 32 + lane;
+        CStager<kOut> out{epi_smem + static_cast<uint32_t>(warp - 2) * 2u * kEpiBufBytes, 0u, lane};
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t epi_phase = 0;
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            int good = 1;
+            if (lane == 0) {
+                mbar_arrive(epi_bar);
+                good = wait_bounded(epi_bar, epi_phase, ctl) ? 1 : 0;
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            epi_phase ^= 1u;
+            return good != 0;
+        };
+        // Release accumulator `a` to the leader's MMA issuer.
+        auto release_acc = [&](int a) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(tempty_bar(a));
+                else
+                    mbar_arrive_cluster(tempty_bar(a), 0u);
+            }
+        };
+        for (int64_t u = cluster_id; u < p.units; u += nclusters) {
+            const Unit un = decode_unit(p, u);
+            const int tm = un.tm, tn = un.tn;
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, ctl) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            const int row0 = tm * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PS::kAccCols;
+            // workspace tile and counter of this CTA's 128-row half
+            const int64_t half = un.slot * 2 + rank;
+            const int a_now = acc;
+            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, half, etid, last_flag, ctl,
+                                      epi_sync, [&]() { release_acc(a_now); }))
+                break;
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        out.drain();  // this warp's output stores have landed
+    }
+
+    // ------------------------------------------------------------ exit --
+    // Neither CTA leaves while the other may still read its shared memory
+    // or signal its barriers; tensor memory of the pair is freed together.
+    // The barriers here are the non-aligned forms, which count threads one
+    // by one, so warps whose lane 0 ran a role loop alone may arrive in any
+    // convergence state.
+    tc_fence_before();
+    cta_barrier_any();
+    cluster_barrier_any();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc<2>(tmem_base, PS::kTmemCols);
+    }
+}
+
+}  // namespace tsg

@@ -146,6 +146,7 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
 
     tsgemm_config_t force{};
     force.splits = splits;
+    force.block_m = 128;  // the one-SM kernel
     tsgemm_config_t cfg{};
     st = tsg::choose_config(M, N, K, dtype_in, dtype_out, TSGEMM_LAYOUT_RRR, ds->num_sms, &force, &cfg);
     if (st != TSGEMM_OK) return st;
@@ -186,8 +187,9 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
         attr = true;
     }
 
-    alignas(64) CUtensorMap tmA;
-    alignas(64) CUtensorMap tmB;
+    CUtensorMap tmA;  // the type carries the alignment the encoder requires
+    CUtensorMap tmB;
+    CUtensorMap tmC;
     const CUtensorMapDataType dt =
         dtype_in == TSGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint32_t estr[2] = {1, 1};
@@ -207,6 +209,21 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
         if (enc(&tmB, dt, 2, const_cast<void*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TSGEMM_ERR_CUDA;
+    }
+
+    {
+        const CUtensorMapDataType dc = dtype_out == TSGEMM_F32
+                                           ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                           : (dtype_out == TSGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N * (dtype_out == TSGEMM_F32 ? 4 : 2))};
+        const cuuint32_t box[2] = {32, 32};
+        const bool dtype_out_is_f32 = dtype_out == TSGEMM_F32;
+        if (enc(&tmC, dc, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            (dtype_out_is_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B),
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return TSGEMM_ERR_CUDA;
     }
 
@@ -234,6 +251,7 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     gp.stages = cfg.stages;
     gp.debug_flags = 0;
     gp.units = cfg.units;
+    gp.full_tiles = tiles - cfg.split_tiles;
     gp.idesc = idesc_for(dtype_in, cfg.block_n);
     gp.C = C;
     gp.ws = ws;
@@ -246,7 +264,7 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     lc.blockDim = dim3(tsg::kThreads, 1, 1);
     lc.dynamicSmemBytes = static_cast<size_t>(smem);
     lc.stream = s;
-    void* args[3] = {&tmA, &tmB, &gp};
+    void* args[4] = {&tmA, &tmB, &tmC, &gp};
     if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;

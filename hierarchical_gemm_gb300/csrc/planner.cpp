@@ -6,7 +6,7 @@
 //     MMA   = 128 * BN * 64 / 4096 cycles (4096 bf16 MACs per SM per cycle),
 //     load  = (A slice + B slice bytes) / kL2BytesPerCycle;
 //   * a CTA runs ceil(units / grid) units back to back (wave quantisation);
-//   * a split tile adds the last CTA's read of S fp32 partial tiles;
+//   * a split tile adds S - 1 hand-overs of an fp32 running sum;
 //   * the whole job can go no faster than its HBM traffic allows.
 // The model only ranks candidates; the tile widths it picks are the
 // measured-best ones on the shapes this library is tuned for.
@@ -21,8 +21,9 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
+constexpr int64_t kEpiStagingBytes = 32768;  // output staging of the epilogue warps
 constexpr double kMacsPerCycle = 4096.0;
-constexpr double kL2BytesPerCycle = 96.0;     // operand feed per SM (model)
+constexpr double kL2BytesPerCycle = 72.0;     // operand feed per SM (measured ballpark)
 constexpr double kHbmBytesPerCycle = 3500.0;  // whole GPU (model)
 constexpr double kReduceBytesPerCycle = 64.0; // split-K partial reads per SM (model)
 constexpr double kUnitOverhead = 600.0;       // pipeline fill / drain per unit (model)
@@ -44,25 +45,36 @@ struct Estimate {
     double compute;
 };
 
-Estimate estimate(int64_t M, int64_t N, int64_t K, int dout, int bn, int splits, int num_sms) {
-    const int64_t tiles = ceil_div(M, kBM) * ceil_div(N, bn);
-    const int64_t units = tiles * splits;
-    const int64_t grid = std::min<int64_t>(units, num_sms);
-    const int64_t waves = ceil_div(units, grid);
+// bm = 128: one CTA per 128 x bn tile; bm = 256: a CTA pair per 256 x bn
+// tile, each SM computing 128 rows and loading half of the B slice.  The
+// last `split_tiles` tiles of the schedule are split into `splits` K parts
+// (all of them, or only the tail wave's, or none).
+Estimate estimate(int64_t M, int64_t N, int64_t K, int dout, int bm, int bn, int splits,
+                  int64_t split_tiles, int num_sms) {
+    const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
+    const int64_t full = tiles - split_tiles;
+    const int64_t units = full + split_tiles * splits;
+    const int64_t slots = bm == 256 ? std::max(1, num_sms / 2) : num_sms;
+    const int64_t grid = std::min<int64_t>(units, slots);
     const int64_t kblocks = ceil_div(K, kBK);
-    const double kb_per_unit = std::ceil(static_cast<double>(kblocks) / splits);
+    const double kb_split = std::ceil(static_cast<double>(kblocks) / splits);
     const double mma = kBM * bn * static_cast<double>(kBK) / kMacsPerCycle;
-    const double load = (kBM * kBK * 2.0 + bn * kBK * 2.0) / kL2BytesPerCycle;
-    const double per_unit = kb_per_unit * std::max(mma, load) + kUnitOverhead;
-    double compute = waves * per_unit;
-    if (splits > 1) compute += splits * static_cast<double>(kBM) * bn * 4.0 / kReduceBytesPerCycle;
+    const double b_bytes = (bm == 256 ? bn / 2 : bn) * kBK * 2.0;
+    const double load = (kBM * kBK * 2.0 + b_bytes) / kL2BytesPerCycle;
+    const double per_kb = std::max(mma, load);
+    // round-robin over `grid` slots: whole tiles first, then split parts
+    const double whole_rounds = static_cast<double>(ceil_div(full, grid));
+    const double split_rounds = static_cast<double>(ceil_div(split_tiles * splits, grid));
+    double compute = whole_rounds * (kblocks * per_kb + kUnitOverhead) +
+                     split_rounds * (kb_split * per_kb + kUnitOverhead);
     double bytes = 2.0 * (M * K + K * N) + static_cast<double>(out_bytes(dout)) * M * N;
-    if (splits > 1) {
-        // partials are written and read back once: charged both to the HBM
-        // floor and, since the reduction is not fully hidden, to the time
-        const double ws = 2.0 * 4.0 * splits * static_cast<double>(tiles) * kBM * bn;
+    if (splits > 1 && split_tiles > 0) {
+        // the parts of a split tile add up in order: S - 1 hand-overs of a
+        // running sum (one write and one read of an fp32 tile half each),
+        // one after another at the end of the tile
+        compute += (splits - 1) * 2.0 * kBM * bn * 4.0 / kReduceBytesPerCycle;
+        const double ws = 2.0 * 4.0 * (splits - 1) * static_cast<double>(split_tiles) * bm * bn;
         bytes += ws;
-        compute += ws / kHbmBytesPerCycle;
     }
     const double hbm = bytes / kHbmBytesPerCycle;
     return {std::max(compute, hbm) + 0.05 * compute, compute};
@@ -70,14 +82,15 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int dout, int bn, int splits,
 
 }  // namespace
 
-int64_t smem_bytes_for(int block_n, int stages) {
-    const int64_t stage = static_cast<int64_t>(kBM) * kBK * 2 + static_cast<int64_t>(block_n) * kBK * 2;
-    return 1024 + stages * stage + 8 * (2 * stages + 6) + 16;
+int64_t smem_bytes_for(int block_m, int block_n, int stages) {
+    const int64_t b_cols = block_m == 256 ? block_n / 2 : block_n;
+    const int64_t stage = static_cast<int64_t>(kBM) * kBK * 2 + b_cols * kBK * 2;
+    return 1024 + stages * stage + kEpiStagingBytes + 8 * (2 * stages + 6) + 16;
 }
 
-int max_stages_for(int block_n) {
+int max_stages_for(int block_m, int block_n) {
     int s = 1;
-    while (s < 16 && smem_bytes_for(block_n, s + 1) <= kSmemPerCtaMax) ++s;
+    while (s < 16 && smem_bytes_for(block_m, block_n, s + 1) <= kSmemPerCtaMax) ++s;
     return s;
 }
 
@@ -107,50 +120,86 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     if (num_sms < 1) return TSGEMM_ERR_INVALID_ARG;
     tsgemm_config_t f{};
     if (force) f = *force;
-    if (f.block_m != 0 && f.block_m != kBM) return TSGEMM_ERR_UNSUPPORTED;
+    if (f.block_m != 0 && f.block_m != 128 && f.block_m != 256) return TSGEMM_ERR_UNSUPPORTED;
     if (f.block_n != 0 && (f.block_n % 64 != 0 || f.block_n < 64 || f.block_n > 256))
         return TSGEMM_ERR_UNSUPPORTED;
+    if (f.block_m == 256 && f.block_n != 0 && f.block_n != 128 && f.block_n != 256)
+        return TSGEMM_ERR_UNSUPPORTED;
+    if (f.block_m == 256 && num_sms < 2) return TSGEMM_ERR_UNSUPPORTED;
     if (f.splits < 0 || f.stages < 0 || f.group_m < 0 || f.grid < 0 || f.timeout_ms < 0)
         return TSGEMM_ERR_INVALID_ARG;
     if (f.units != 0 || f.workspace_bytes != 0) return TSGEMM_ERR_INVALID_ARG;  // derived fields
+    if (f.split_tiles < 0 || (f.split_tiles > 0 && f.splits < 2)) return TSGEMM_ERR_INVALID_ARG;
 
     const int64_t kblocks = ceil_div(K, kBK);
     if (f.splits > kblocks || f.splits > 4096) return TSGEMM_ERR_UNSUPPORTED;
 
     // Candidate tile widths: never wider than N rounded up to 64.
     const int64_t n_pad = ceil_div(N, 64) * 64;
-    int best_bn = 0, best_s = 0;
+    int best_bm = 0, best_bn = 0, best_s = 0;
+    int64_t best_st = 0;
     double best = 0;
+    const int bms[2] = {256, 128};  // pairs first: ties go to the pair
     const int bns[4] = {256, 192, 128, 64};
-    for (int bn : bns) {
-        if (f.block_n && bn != f.block_n) continue;
-        if (!f.block_n && bn > n_pad && bn != 64) continue;
-        const int smax = f.splits ? f.splits : static_cast<int>(std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, kblocks / 4)));
-        const int smin = f.splits ? f.splits : 1;
-        for (int s = smin; s <= smax; ++s) {
-            const Estimate e = estimate(M, N, K, dtype_out, bn, s, num_sms);
-            // strict improvement required: ties keep the wider tile / fewer splits
-            if (best_bn == 0 || e.cycles < best * 0.999) {
-                best = e.cycles;
-                best_bn = bn;
-                best_s = s;
+    for (int bm : bms) {
+        if (f.block_m && bm != f.block_m) continue;
+        if (bm == 256 && num_sms < 2) continue;
+        const int64_t slots = bm == 256 ? num_sms / 2 : num_sms;
+        for (int bn : bns) {
+            if (bm == 256 && bn != 128 && bn != 256) continue;
+            if (f.block_n && bn != f.block_n) continue;
+            if (!f.block_n && bn > n_pad && bn != 64 && !(bm == 256 && bn == 128)) continue;
+            const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
+            const int smax = f.splits ? f.splits
+                                      : static_cast<int>(std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, kblocks / 4)));
+            const int smin = f.splits ? f.splits : 1;
+            for (int s = smin; s <= smax; ++s) {
+                // which tiles are split: none (s = 1), a forced count, every
+                // tile, or only the tiles of the last, partial wave
+                int64_t options[2] = {0, -1};
+                if (s > 1) {
+                    if (f.split_tiles) {
+                        options[0] = f.split_tiles;
+                    } else {
+                        options[0] = tiles;
+                        if (!f.splits && tiles > slots && tiles % slots != 0) options[1] = tiles % slots;
+                    }
+                }
+                for (int64_t st : options) {
+                    if (st < 0 || st > tiles) continue;
+                    const Estimate e = estimate(M, N, K, dtype_out, bm, bn, s, st, num_sms);
+                    // strict improvement required: ties keep the earlier candidate
+                    if (best_bn == 0 || e.cycles < best * 0.999) {
+                        best = e.cycles;
+                        best_bm = bm;
+                        best_bn = bn;
+                        best_s = s;
+                        best_st = st;
+                    }
+                }
             }
         }
     }
     if (best_bn == 0) return TSGEMM_ERR_UNSUPPORTED;
 
     tsgemm_config_t c{};
-    c.block_m = kBM;
+    c.block_m = best_bm;
     c.block_n = best_bn;
     c.splits = best_s;
-    const int smax_fit = max_stages_for(best_bn);
+    const int smax_fit = max_stages_for(best_bm, best_bn);
     if (f.stages > smax_fit || (f.stages != 0 && f.stages < 2)) return TSGEMM_ERR_UNSUPPORTED;
     c.stages = f.stages ? f.stages : smax_fit;
     c.group_m = f.group_m ? f.group_m : 8;
-    const int64_t tiles = ceil_div(M, kBM) * ceil_div(N, best_bn);
-    c.units = tiles * best_s;
-    c.grid = static_cast<int32_t>(std::min<int64_t>(c.units, f.grid ? f.grid : num_sms));
-    c.workspace_bytes = best_s > 1 ? tiles * best_s * kBM * static_cast<int64_t>(best_bn) * 4 : 0;
+    const int64_t tiles = ceil_div(M, best_bm) * ceil_div(N, best_bn);
+    c.split_tiles = best_s > 1 ? best_st : 0;
+    c.units = (tiles - c.split_tiles) + c.split_tiles * best_s;
+    // a pair kernel launches two CTAs per unit slot
+    const int64_t ctas_per_slot = best_bm == 256 ? 2 : 1;
+    int64_t slots = (f.grid ? f.grid : num_sms) / ctas_per_slot;
+    if (slots < 1) return TSGEMM_ERR_UNSUPPORTED;
+    c.grid = static_cast<int32_t>(std::min<int64_t>(c.units, slots) * ctas_per_slot);
+    // one fp32 running sum per split tile
+    c.workspace_bytes = c.split_tiles * best_bm * static_cast<int64_t>(best_bn) * 4;
     c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
     c.debug_flags = f.debug_flags;
     *out = c;

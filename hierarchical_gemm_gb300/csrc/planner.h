@@ -21,10 +21,11 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                               int layout, int num_sms, const tsgemm_config_t* force,
                               tsgemm_config_t* out);
 
-// Dynamic shared memory a 1-SM kernel with this tile width and depth needs.
-int64_t smem_bytes_for(int block_n, int stages);
+// Dynamic shared memory per CTA of the kernel for this tile shape (block_m
+// 128: one SM per tile; 256: a CTA pair per tile) and ring depth.
+int64_t smem_bytes_for(int block_m, int block_n, int stages);
 
-// Deepest ring that fits the shared-memory budget for this tile width.
-int max_stages_for(int block_n);
+// Deepest ring that fits the shared-memory budget for this tile shape.
+int max_stages_for(int block_m, int block_n);
 
 }  // namespace tsg

@@ -21,6 +21,44 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// ------------------------------------------------------------- cluster --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address in CTA `cta` of the cluster of the shared-memory location that is
+// at `addr` in the calling CTA.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t cta) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(cta));
+    return r;
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr_cluster, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
+}
+
+// CTA-wide barrier 0 in its non-aligned form: every thread of the CTA
+// arrives on its own, whatever the convergence of its warp.
+__device__ __forceinline__ void cta_barrier_any() {
+    asm volatile("barrier.sync 0;" ::: "memory");
+}
+
+// Cluster-wide barrier in its non-aligned form (every thread of every CTA of
+// the cluster arrives on its own).
+__device__ __forceinline__ void cluster_barrier_any() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Cluster-wide barrier (all threads of all CTAs of the cluster, converged).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 // ------------------------------------------------------------ mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -84,6 +122,7 @@ struct WaitCtl {
     volatile int* abort;   // shared memory
     int* status;           // global status word of the plan
     uint64_t timeout_ns;
+    uint32_t peer_abort = 0;  // shared::cluster address of the peer CTA's flag (pairs), or 0
 };
 
 // Wait for phase `parity` of `bar`, for at most ctl.timeout_ns.  Returns
@@ -102,6 +141,37 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
         if (respect_abort && *ctl.abort) return false;
         if (globaltimer() - t0 > ctl.timeout_ns) {
             *ctl.abort = 1;
+            if (ctl.peer_abort) st_shared_cluster_u32(ctl.peer_abort, 1u);
+            atomicExch(ctl.status, 5 /* TSGEMM_ERR_TIMEOUT */);
+            __threadfence();
+            return false;
+        }
+    }
+}
+
+// Acquire load / release store of a flag in global memory (GPU scope).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until the global flag *p equals `value` (it is set by another CTA),
+// for at most ctl.timeout_ns; false when the limit expired or the CTA is
+// aborting.
+__device__ __forceinline__ bool wait_flag_bounded(const int* p, int value, const WaitCtl& ctl) {
+    if (ld_acquire_gpu(p) == value) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        __nanosleep(32);
+        if (ld_acquire_gpu(p) == value) return true;
+        if (*ctl.abort) return false;
+        if (globaltimer() - t0 > ctl.timeout_ns) {
+            *ctl.abort = 1;
+            if (ctl.peer_abort) st_shared_cluster_u32(ctl.peer_abort, 1u);
             atomicExch(ctl.status, 5 /* TSGEMM_ERR_TIMEOUT */);
             __threadfence();
             return false;
@@ -124,6 +194,48 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(m), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
+}
+
+// The same load issued by either CTA of a CTA pair, completing its bytes on
+// the barrier at `bar_cluster` (a shared::cluster address, which may be in
+// the peer CTA: the pair's leader counts both CTAs' bytes).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(m), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// 2-D tiled store of the box at (c0 = inner, c1 = outer) from shared memory;
+// parts of the box outside the tensor are not written.  Tracked as a bulk
+// async-group of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_group_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
 }
 
 // ------------------------------------------------------------- tcgen05 --

@@ -74,8 +74,9 @@ struct tsgemm_plan_s {
     const void* last_a;
     const void* last_b;
     const void* last_c;
-    alignas(64) CUtensorMap tmA;
-    alignas(64) CUtensorMap tmB;
+    CUtensorMap tmA;  // the type carries the alignment the encoder requires
+    CUtensorMap tmB;
+    CUtensorMap tmC;
     tsg::GemmParams params;
 };
 
@@ -133,9 +134,13 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     st = tsg::choose_config(M, N, K, dtype_in, dtype_out, layout, sms, force, &cfg);
     if (st != TSGEMM_OK) return st;
 
-    const void* kern = tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out));
-    const int64_t need = tsg::kernel_1sm_smem_bytes(cfg.block_n, cfg.stages);
-    if (!kern || need != tsg::smem_bytes_for(cfg.block_n, cfg.stages) || need > tsg::kSmemPerCtaMax)
+    const bool pair = cfg.block_m == 256;
+    const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out))
+                            : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out));
+    const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, cfg.stages)
+                              : tsg::kernel_1sm_smem_bytes(cfg.block_n, cfg.stages);
+    if (!kern || need != tsg::smem_bytes_for(cfg.block_m, cfg.block_n, cfg.stages) ||
+        need > tsg::kSmemPerCtaMax)
         return TSGEMM_ERR_UNSUPPORTED;
     // Ask for more than half the SM's shared memory even when the ring is
     // shallow, so one CTA owns each SM and its tensor memory.
@@ -146,6 +151,20 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
                              static_cast<int>(tsg::kSmemPerCtaMax)) != cudaSuccess) {
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;
+    }
+    if (pair) {
+        // Persistent pairs: launch no more clusters than can be resident at
+        // once (a cluster's two CTAs must share a GPC).
+        cudaLaunchConfig_t lc{};
+        lc.gridDim = dim3(static_cast<unsigned>(cfg.grid), 1, 1);
+        lc.blockDim = dim3(tsg::kThreads, 1, 1);
+        lc.dynamicSmemBytes = static_cast<size_t>(smem);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();
+            return TSGEMM_ERR_UNSUPPORTED;
+        }
+        if (cfg.grid > 2 * clusters) cfg.grid = 2 * clusters;
     }
 
     // value-initialised; operator new honours the 64-byte alignment the
@@ -161,7 +180,9 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     p->device = dev;
     p->kernel = kern;
     p->smem = smem;
-    p->num_tiles = ((M + 127) / 128) * ((N + cfg.block_n - 1) / cfg.block_n);
+    // split-K counters: one per 128-row half of a split tile (pairs reduce
+    // halves)
+    p->num_tiles = cfg.split_tiles * (cfg.block_m / 128);
 
     if (cudaMalloc(&p->status_d, sizeof(int)) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -191,7 +212,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.M = static_cast<int32_t>(M);
     gp.N = static_cast<int32_t>(N);
     gp.K = static_cast<int32_t>(K);
-    gp.tiles_m = static_cast<int32_t>((M + 127) / 128);
+    gp.tiles_m = static_cast<int32_t>((M + cfg.block_m - 1) / cfg.block_m);
     gp.tiles_n = static_cast<int32_t>((N + cfg.block_n - 1) / cfg.block_n);
     gp.splits = cfg.splits;
     gp.kblocks = static_cast<int32_t>((K + 63) / 64);
@@ -199,7 +220,8 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.stages = cfg.stages;
     gp.debug_flags = cfg.debug_flags;
     gp.units = cfg.units;
-    gp.idesc = make_idesc(dtype_in, 128, cfg.block_n);
+    gp.full_tiles = ((M + cfg.block_m - 1) / cfg.block_m) * ((N + cfg.block_n - 1) / cfg.block_n) - cfg.split_tiles;
+    gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n);
     gp.C = nullptr;
     gp.ws = p->ws;
     gp.counters = p->counters;
@@ -266,6 +288,27 @@ static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* 
     return TSGEMM_OK;
 }
 
+// C: inner dimension N, outer M; box 32 x 32 (the block one epilogue warp
+// stores at a time), in the swizzle the kernel writes its staging buffer in.
+static tsgemm_status_t encode_c(tsgemm_plan_s* p, void* C) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return TSGEMM_ERR_CUDA;
+    const CUtensorMapDataType dt = p->dtype_out == TSGEMM_F32
+                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : (p->dtype_out == TSGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->N * elem_bytes(p->dtype_out))};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const bool dtype_out_is_f32 = p->dtype_out == TSGEMM_F32;
+    if (enc(&p->tmC, dt, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            (dtype_out_is_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B),
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return TSGEMM_ERR_CUDA;
+    return TSGEMM_OK;
+}
+
 tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, void* C, void* stream) {
     if (!plan || !A || !B || !C) return TSGEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15u)
@@ -294,6 +337,9 @@ tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, voi
     if (C != plan->last_c) {
         tsgemm_status_t st = check_device_ptr(C, plan->device);
         if (st != TSGEMM_OK) return st;
+        plan->last_c = nullptr;
+        st = encode_c(plan, C);
+        if (st != TSGEMM_OK) return st;
         plan->last_c = C;
     }
     plan->params.C = C;
@@ -305,7 +351,7 @@ tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, voi
     lc.stream = static_cast<cudaStream_t>(stream);
     lc.attrs = nullptr;
     lc.numAttrs = 0;
-    void* args[3] = {&plan->tmA, &plan->tmB, &plan->params};
+    void* args[4] = {&plan->tmA, &plan->tmB, &plan->tmC, &plan->params};
     if (cudaLaunchKernelExC(&lc, plan->kernel, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;

@@ -81,14 +81,18 @@ typedef enum {
 typedef struct {
     int32_t block_m;      /* rows of C per MMA tile: 128 (one SM) or 256 (SM pair) */
     int32_t block_n;      /* columns of C per tile: 64, 128, 192 or 256 */
-    int32_t splits;       /* K split factor S (1 = no split) */
+    int32_t splits;       /* K split factor S of the split tiles (1 = no split) */
     int32_t stages;       /* depth of the shared-memory operand ring */
     int32_t group_m;      /* tile rows per raster group (L2 reuse) */
     int32_t grid;         /* CTAs launched (persistent) */
-    int64_t units;        /* work units = tiles * splits */
-    int64_t workspace_bytes; /* split-K partial buffer owned by the plan */
+    int64_t units;        /* work units = whole tiles + split_tiles * splits */
+    int64_t workspace_bytes; /* split-K running sums owned by the plan:
+                                split_tiles * block_m * block_n * 4 bytes */
     int32_t timeout_ms;   /* limit of every device-side wait */
     int32_t debug_flags;  /* tests only: TSGEMM_DEBUG_* */
+    int64_t split_tiles;  /* tiles split into `splits` K parts: the last ones of
+                             the schedule (all tiles, or the last partial wave).
+                             Forced with splits > 1; 0 then means every tile. */
 } tsgemm_config_t;
 
 /* Tests only: the producer skips the first operand load of the first work
@@ -170,9 +174,9 @@ TSGEMM_API const char* tsgemm_status_string(tsgemm_status_t s);
  * on `stream` before the launch).
  *
  * Limits: at most TSGEMM_NOALLOC_MAX_TILES output tiles and at most
- * TSGEMM_NOALLOC_WS_BYTES of fp32 partials (S * tiles * 128 * block_n * 4
- * bytes); larger problems return TSGEMM_ERR_SCRATCH_LIMIT before anything is
- * enqueued.
+ * TSGEMM_NOALLOC_WS_BYTES of fp32 running sums (split tiles * 128 *
+ * block_n * 4 bytes); larger problems return TSGEMM_ERR_SCRATCH_LIMIT before
+ * anything is enqueued.
  *
  * Every call uses the same scratch array, which keeps the previous call's
  * contents; each call clears the tile counters it needs on `stream` before

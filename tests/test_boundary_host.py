@@ -63,8 +63,10 @@ def test_choose_config_validation(ts, args, code):
 
 def test_choose_config_rejects_bad_forced_values(ts):
     for force, code in [({"block_n": 96}, 2), ({"block_n": 320}, 2), ({"block_m": 64}, 2),
+                        ({"block_m": 256, "block_n": 192}, 2), ({"block_m": 256, "block_n": 64}, 2),
                         ({"splits": 100}, 2), ({"stages": 1}, 2), ({"stages": 40}, 2),
-                        ({"splits": -1}, 1), ({"units": 5}, 1)]:
+                        ({"splits": -1}, 1), ({"units": 5}, 1), ({"split_tiles": 3}, 1),
+                        ({"splits": 2, "split_tiles": 5}, 2)]:
         with pytest.raises(ts.TsgemmError) as e:
             ts.choose_config(128, 128, 1024, "bf16", "bf16", 152, **force)
         assert e.value.status == code, force
@@ -91,13 +93,17 @@ def _ceil(a, b):
 def test_planner_invariants(ts, shape, sms):
     M, N, K, din, dout = shape
     c = ts.choose_config(M, N, K, din, dout, sms)
-    tiles = _ceil(M, 128) * _ceil(N, c["block_n"])
-    assert c["block_m"] == 128 and c["block_n"] in (64, 128, 192, 256)
-    assert c["units"] == tiles * c["splits"]
+    bm, bn = c["block_m"], c["block_n"]
+    tiles = _ceil(M, bm) * _ceil(N, bn)
+    assert (bm, bn) in [(128, 64), (128, 128), (128, 192), (128, 256), (256, 128), (256, 256)]
+    st = c["split_tiles"]
+    assert 0 <= st <= tiles and (st == 0) == (c["splits"] == 1)
+    assert c["units"] == (tiles - st) + st * c["splits"]
     assert 1 <= c["splits"] <= _ceil(K, 64)
-    assert 1 <= c["grid"] <= min(sms, c["units"])
-    assert c["workspace_bytes"] == (tiles * c["splits"] * 128 * c["block_n"] * 4 if c["splits"] > 1 else 0)
-    stage = 128 * 64 * 2 + c["block_n"] * 64 * 2
+    per = bm // 128  # CTAs per unit
+    assert c["grid"] % per == 0 and 1 <= c["grid"] <= per * min(sms // per, c["units"])
+    assert c["workspace_bytes"] == st * bm * bn * 4
+    stage = 128 * 64 * 2 + (bn // per) * 64 * 2
     assert 1024 + c["stages"] * stage + 8 * (2 * c["stages"] + 6) + 16 <= 232448
     assert c["timeout_ms"] == 1000
 
@@ -106,18 +112,26 @@ def test_planner_choices_for_the_workloads(ts):
     # The skinny weight-streaming shape fills the GPU with one wave of
     # 128 x 192 tiles and no split; the long-K shape is split.
     c = ts.choose_config(128, 28672, 8192, "bf16", "bf16", 152)
-    assert c["block_n"] == 192 and c["splits"] == 1 and c["grid"] == 150
+    assert c["block_m"] == 128 and c["block_n"] == 192 and c["splits"] == 1 and c["grid"] == 150
+    # the large square shapes use CTA pairs
+    c = ts.choose_config(16384, 16384, 8192, "bf16", "bf16", 152)
+    assert c["block_m"] == 256 and c["grid"] == 152
     c = ts.choose_config(1024, 1024, 65536, "bf16", "f32", 152)
     assert c["splits"] > 1
+    # 4096^3: the tiles of the last, partial wave are split along K
     c = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152)
-    assert c["splits"] == 1
+    slots = 152 // (c["block_m"] // 128)
+    tiles = (4096 // c["block_m"]) * (4096 // c["block_n"])
+    assert c["splits"] == 1 or c["split_tiles"] == tiles % slots
 
 
 def test_forced_fields_are_honoured(ts):
-    c = ts.choose_config(1000, 1000, 4096, "bf16", "bf16", 152, block_n=128, splits=5, stages=3,
-                         group_m=4, grid=7, timeout_ms=50)
-    assert (c["block_n"], c["splits"], c["stages"], c["group_m"], c["grid"], c["timeout_ms"]) == \
-        (128, 5, 3, 4, 7, 50)
+    c = ts.choose_config(1000, 1000, 4096, "bf16", "bf16", 152, block_m=128, block_n=128, splits=5,
+                         stages=3, group_m=4, grid=7, timeout_ms=50)
+    assert (c["block_m"], c["block_n"], c["splits"], c["stages"], c["group_m"], c["grid"],
+            c["timeout_ms"]) == (128, 128, 5, 3, 4, 7, 50)
+    c = ts.choose_config(1000, 1000, 4096, "bf16", "bf16", 152, block_m=256, grid=7)
+    assert c["block_m"] == 256 and c["grid"] == 6  # whole pairs only
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

@@ -57,8 +57,11 @@ def test_identity_right(din, dout, n):
     _check(C, A, eye, din, dout, exact=True)
 
 
-@pytest.mark.parametrize("block_n", [64, 128, 192, 256])
-def test_permutation_both_sides(block_n):
+TILES = [(128, 64), (128, 128), (128, 192), (128, 256), (256, 128), (256, 256)]
+
+
+@pytest.mark.parametrize("block_m,block_n", TILES)
+def test_permutation_both_sides(block_m, block_n):
     r = np.random.default_rng(3)
     n = 384
     perm = r.permutation(n)
@@ -66,10 +69,11 @@ def test_permutation_both_sides(block_n):
     P[np.arange(n), perm] = 1.0
     Pb = _bits_of(P, "bf16")
     B = _ints(n, 320, 4, -16, 16)
-    C, _ = run_gemm(Pb, B, "bf16", "bf16", block_n=block_n)
+    C, cfg = run_gemm(Pb, B, "bf16", "bf16", block_m=block_m, block_n=block_n)
+    assert (cfg["block_m"], cfg["block_n"]) == (block_m, block_n)
     _check(C, Pb, B, "bf16", "bf16", exact=True)
     A = _ints(256, n, 5, -16, 16)
-    C, _ = run_gemm(A, Pb, "bf16", "bf16", block_n=block_n)
+    C, _ = run_gemm(A, Pb, "bf16", "bf16", block_m=block_m, block_n=block_n)
     _check(C, A, Pb, "bf16", "bf16", exact=True)
 
 
@@ -113,37 +117,63 @@ def test_random_shapes_default_plan(shape, din, dout):
     _check(C, A, B, din, dout, exact=False)
 
 
-@pytest.mark.parametrize("block_n", [64, 128, 192, 256])
+@pytest.mark.parametrize("block_m,block_n", TILES)
 @pytest.mark.parametrize("splits", [1, 2, 7])
 @pytest.mark.parametrize("stages", [2, 0])
-def test_every_tile_width_and_split(block_n, splits, stages):
+def test_every_tile_shape_and_split(block_m, block_n, splits, stages):
     M, N, K = 333, 776, 1096
     A = _ints(M, K, 30, dtype="bf16")
     B = _ints(K, N, 31, dtype="bf16")
-    force = {"block_n": block_n, "splits": splits}
+    force = {"block_m": block_m, "block_n": block_n, "splits": splits}
     if stages:
         force["stages"] = stages
     C, cfg = run_gemm(A, B, "bf16", "f32", **force)
-    assert cfg["block_n"] == block_n and cfg["splits"] == splits
+    assert (cfg["block_m"], cfg["block_n"], cfg["splits"]) == (block_m, block_n, splits)
     _check(C, A, B, "bf16", "f32", exact=True)
 
 
-@pytest.mark.parametrize("grid", [1, 3])
-def test_persistent_loop_with_small_grid(grid):
+@pytest.mark.parametrize("block_m,block_n", TILES)
+@pytest.mark.parametrize("which", ["one", "all_but_one"])
+def test_tail_tiles_split(block_m, block_n, which):
+    # Only the last tiles of the schedule are split along K (the tail wave);
+    # the others are computed whole, in the same launch.
+    M, N, K = 600, 776, 1096
+    tiles = -(-M // block_m) * -(-N // block_n)
+    st = 1 if which == "one" else tiles - 1
+    A = _ints(M, K, 32, dtype="bf16")
+    B = _ints(K, N, 33, dtype="bf16")
+    C, cfg = run_gemm(A, B, "bf16", "f32", block_m=block_m, block_n=block_n, splits=3, split_tiles=st)
+    assert cfg["split_tiles"] == st and cfg["units"] == tiles - st + 3 * st
+    _check(C, A, B, "bf16", "f32", exact=True)
+
+
+@pytest.mark.parametrize("block_m,grid", [(128, 1), (128, 3), (256, 2), (256, 6)])
+def test_persistent_loop_with_small_grid(block_m, grid):
     # Few CTAs walk many units: exercises ring-phase and accumulator-phase
     # wrap-around over many tiles.
     A = _ints(640, 512, 40)
     B = _ints(512, 1024, 41)
-    C, cfg = run_gemm(A, B, "bf16", "bf16", grid=grid, block_n=128, splits=2)
+    C, cfg = run_gemm(A, B, "bf16", "bf16", grid=grid, block_m=block_m, block_n=128, splits=2)
     assert cfg["grid"] == grid
     _check(C, A, B, "bf16", "bf16", exact=True)
 
 
+@pytest.mark.parametrize("M", [1, 128, 200, 257, 511])
+def test_pair_tiles_with_ragged_rows(M):
+    # A pair tile whose second CTA has few or no valid rows.
+    A = _unif(M, 192, 45 + M, "bf16")
+    B = _unif(192, 264, 46, "bf16")
+    C, cfg = run_gemm(A, B, "bf16", "bf16", block_m=256, block_n=256)
+    assert cfg["block_m"] == 256
+    _check(C, A, B, "bf16", "bf16", exact=False)
+
+
 @pytest.mark.parametrize("group_m", [1, 3, 16])
-def test_raster_groups(group_m):
+@pytest.mark.parametrize("block_m,block_n", [(128, 64), (256, 128)])
+def test_raster_groups(group_m, block_m, block_n):
     A = _unif(700, 256, 50, "bf16")
     B = _unif(256, 1280, 51, "bf16")
-    C, _ = run_gemm(A, B, "bf16", "bf16", group_m=group_m, block_n=64)
+    C, _ = run_gemm(A, B, "bf16", "bf16", group_m=group_m, block_m=block_m, block_n=block_n)
     _check(C, A, B, "bf16", "bf16", exact=False)
 
 
@@ -204,6 +234,13 @@ def _workload_case(name, **force):
                                   "skinny_128x28672x8192_bf16", "longk_1024x1024x65536_int_f32"])
 def test_workload_full_compare(name):
     w, A, B, C, _ = _workload_case(name)
+    _check(C, A, B, w["dtype_in"], w["dtype_out"], exact=w["exact"])
+
+
+@pytest.mark.parametrize("name", ["gemm_4096_bf16", "longk_1024x1024x65536_int_f32"])
+def test_workload_full_compare_one_sm_tiles(name):
+    w, A, B, C, cfg = _workload_case(name, block_m=128)
+    assert cfg["block_m"] == 128
     _check(C, A, B, w["dtype_in"], w["dtype_out"], exact=w["exact"])
 
 
