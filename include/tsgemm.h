@@ -95,9 +95,9 @@ typedef struct {
                              Forced with splits > 1; 0 then means every tile. */
 } tsgemm_config_t;
 
-/* Tests only: the producer skips the first operand load of the first work
- * unit, so the consumer's wait runs out; the launch ends with
- * TSGEMM_ERR_TIMEOUT in the status word instead of hanging. */
+/* Tests only: the first CTA (or CTA pair) skips the first operand load of
+ * its first work unit, so the MMA issuer's bounded wait runs out; the launch
+ * ends with TSGEMM_ERR_TIMEOUT in the status word instead of hanging. */
 #define TSGEMM_DEBUG_SKIP_FIRST_LOAD 1
 
 /* Validate the problem, check that the current device is CC 10.3, choose the
