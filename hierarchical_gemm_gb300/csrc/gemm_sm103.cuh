@@ -19,8 +19,9 @@
 //   * T.copy(C_r, C)                                -> tcgen05.ld by an
 //     epilogue warpgroup, fp32 -> output conversion, global stores;
 //   * warp(group) specialisation by rank (TileScale README, T.Scale
-//     "warpgroup" example): warp 0 produces, warp 1 issues MMAs, warps 2-5
-//     drain the accumulator;
+//     "warpgroup" example): warp 0 produces, warp 1 issues MMAs, warps 2-9
+//     (two warpgroups, each taking half of the tile's columns) drain the
+//     accumulator;
 //   * persistent thread blocks (TileScale roadmap, resource control): every
 //     CTA walks a static list of work units;
 //   * the K split with a reduction (TileScale README, "Example of GEMM",
@@ -41,8 +42,9 @@ namespace tsg {
 constexpr int kBM = 128;        // accumulator rows = TMEM lanes
 constexpr int kBK = 64;         // K per slice: one 128-byte swizzle row of 16-bit data
 constexpr int kUmmaK = 16;      // K per tcgen05.mma kind::f16
-constexpr int kThreads = 192;   // 6 warps
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;    // two epilogue warpgroups
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;  // producer warp, MMA warp, epilogue
 constexpr int kMaxStages = 16;
 
 enum OutKind { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2 };
@@ -116,8 +118,14 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int64_t u) {
 // by the copy engine.  The block is laid out in the tensor map's swizzle
 // (128-byte for fp32 rows, 64-byte for 16-bit rows); buffers are 1024-byte
 // aligned, as the swizzle patterns require.
-constexpr uint32_t kEpiBufBytes = 32 * 32 * 4;              // fp32 block (largest)
-constexpr uint32_t kEpiSmemBytes = (kEpiThreads / 32) * 2 * kEpiBufBytes;  // 32 KiB
+template <int kOut>
+__host__ __device__ constexpr uint32_t epi_buf_bytes() {
+    return 32u * 32u * (kOut == kOutF32 ? 4u : 2u);  // one 32 x 32 output block
+}
+template <int kOut>
+__host__ __device__ constexpr uint32_t epi_smem_bytes() {
+    return kEpiWarps * 2u * epi_buf_bytes<kOut>();  // 32 KiB (16-bit), 64 KiB (fp32)
+}
 
 template <int kOut>
 struct CStager {
@@ -129,7 +137,7 @@ struct CStager {
     // store the warp's 32 x 32 block at (row0, col0) of C.
     __device__ __forceinline__ void put(const GemmParams& p, const CUtensorMap* tmC, int row0, int col0,
                                         const uint32_t (&r)[32]) {
-        const uint32_t buf = buf0 + which * kEpiBufBytes;
+        const uint32_t buf = buf0 + which * epi_buf_bytes<kOut>();
         if (lane == 0) bulk_wait_group_read<1>();  // the store that used `buf` last has read it
         __syncwarp();
         if constexpr (kOut == kOutF32) {
@@ -188,16 +196,17 @@ struct CStager {
 template <int BN, int kOut, class Sync, class Release>
 __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
                                            const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
-                                           int etid, volatile int* flag, const WaitCtl& ctl, Sync&& epi_sync,
-                                           Release&& release) {
+                                           int c_begin, int etid, volatile int* flag, const WaitCtl& ctl,
+                                           Sync&& epi_sync, Release&& release) {
     const int col0 = un.tn * BN;
+    const int c_end = c_begin + BN / 2;  // this warpgroup's half of the columns
     if (un.nsplit == 1) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_begin; c < c_end; c += 32) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tbase + c, r);
             tmem_ld_wait();
-            if (c + 32 >= BN) release();  // the accumulator is in registers now
+            if (c + 32 >= c_end) release();  // this thread's accumulator part is in registers
             out.put(p, tmC, row0, col0 + c, r);
         }
         return true;
@@ -214,16 +223,14 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
     // bytes: [BN/32 column chunks][4 lane quarters][8 float4][32 lanes].
     const int q = row_local >> 5, lane = row_local & 31;
     float* run = p.ws + h * (kBM * BN) + q * (8 * 128) + lane * 4;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    constexpr int kChunkFloats = 4 * 8 * 128;  // one 32-column chunk of the half tile
+    // Adds the running sum (if any) to chunk c of this thread's accumulator
+    // row, then passes the chunk on: to the workspace, or (last part) to C.
+    auto chunk = [&](int c, const float4 (&prev)[8]) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c, r);
-        float* rc = run + (c >> 5) * (4 * 8 * 128);  // this chunk, this thread
+        tmem_ld_wait();
         if (un.split > 0) {
-            float4 prev[8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) prev[v] = ld_global_cg_f4(rc + v * 128);
-            tmem_ld_wait();
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
                 r[4 * v] = __float_as_uint(__fadd_rn(prev[v].x, __uint_as_float(r[4 * v])));
@@ -232,7 +239,6 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
                 r[4 * v + 3] = __float_as_uint(__fadd_rn(prev[v].w, __uint_as_float(r[4 * v + 3])));
             }
         } else {
-            tmem_ld_wait();
             // the sum starts from a cleared (+0) accumulator
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fadd_rn(0.0f, __uint_as_float(r[i])));
@@ -240,9 +246,31 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
         if (last) {
             out.put(p, tmC, row0, col0 + c, r);
         } else {
+            float* rc = run + (c >> 5) * kChunkFloats;
 #pragma unroll
             for (int v = 0; v < 8; ++v)
                 st_global_v4(rc + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        }
+    };
+    auto fetch = [&](int c, float4 (&dst)[8]) {
+        if (un.split > 0 && c < c_end) {
+            const float* rc = run + (c >> 5) * kChunkFloats;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) dst[v] = ld_global_cg_f4(rc + v * 128);
+        }
+    };
+    // Two chunks of the running sum are in flight ahead of the one being
+    // added, so the hand-over is bound by bandwidth rather than latency.
+    float4 pa[8], pb[8];
+    fetch(c_begin, pa);
+    fetch(c_begin + 32, pb);
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 64) {
+        chunk(c, pa);
+        fetch(c + 64, pa);
+        if (c + 32 < c_end) {
+            chunk(c + 32, pb);
+            fetch(c + 96, pb);
         }
     }
     release();
@@ -270,9 +298,9 @@ struct TileShape {
 };
 
 // Bytes of dynamic shared memory the kernel needs for `stages` slots.
-template <int BN>
+template <int BN, int kOut>
 __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
-    return 1024u /* alignment slack */ + stages * TileShape<BN>::kStageBytes + kEpiSmemBytes +
+    return 1024u /* alignment slack */ + stages * TileShape<BN>::kStageBytes + epi_smem_bytes<kOut>() +
            8u * (2 * stages + 6) /* barriers */ + 16u /* tmem holder, flags */;
 }
 
@@ -288,14 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = p.stages;
 
     const uint32_t epi_smem = base + S * TS::kStageBytes;  // output staging
-    const uint32_t bars = epi_smem + kEpiSmemBytes;
+    const uint32_t bars = epi_smem + epi_smem_bytes<kOut>();
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     const uint32_t epi_bar = bars + 8u * (2 * S + 5);
-    uint8_t* misc = base_ptr + S * TS::kStageBytes + kEpiSmemBytes + 8u * (2 * S + 6);
+    uint8_t* misc = base_ptr + S * TS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 6);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
@@ -313,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(a), kEpiThreads);
         }
         mbar_init(drain_bar, 1);
-        mbar_init(epi_bar, kEpiThreads / 32);
+        mbar_init(epi_bar, kEpiWarps);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -386,19 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    // (TMA-written operands are visible to the MMA once the
+                    // full barrier completes; no tcgen05 fence is needed.)
                     const uint32_t a_addr = base + stage * TS::kStageBytes;
-                    const uint32_t b_addr = a_addr + TS::kABytes;
-#pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
-                        //    the k-th 16-element step is 32 B along the row.
-                        // B: MN-major, 64-column boxes 8 KiB apart (LBO), 8-row
-                        //    groups 1024 B apart (SBO); the k-th step is 16 rows.
-                        const uint64_t ad = smem_desc_sw128(a_addr + k * 32u, 16u, 1024u);
-                        const uint64_t bd = smem_desc_sw128(b_addr + k * 2048u, 8192u, 1024u);
-                        umma_f16<1>(d_tmem, ad, bd, p.idesc, (kb > un.kb0 || k > 0) ? 1u : 0u);
-                    }
+                    // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
+                    //    the k-th 16-element step is 32 B along the row (+2 in
+                    //    the descriptor's 16-byte address field).
+                    // B: MN-major, 64-column boxes 8 KiB apart (LBO), 8-row
+                    //    groups 1024 B apart (SBO); the k-th step is 16 rows
+                    //    (+2048 B, +128).
+                    const uint64_t ad = smem_desc_sw128(a_addr, 16u, 1024u);
+                    const uint64_t bd = smem_desc_sw128(a_addr + TS::kABytes, 8192u, 1024u);
+                    umma_f16<1>(d_tmem, ad, bd, p.idesc, kb > un.kb0 ? 1u : 0u);
+                    umma_f16<1>(d_tmem, ad + 2, bd + 128, p.idesc, 1u);
+                    umma_f16<1>(d_tmem, ad + 4, bd + 256, p.idesc, 1u);
+                    umma_f16<1>(d_tmem, ad + 6, bd + 384, p.idesc, 1u);
                     umma_commit(empty_bar(stage));  // slot free once these MMAs have read it
                     if (++stage == S) {
                         stage = 0;
@@ -420,9 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // --------------------------------------------------- epilogue --
         const int q = warp & 3;              // TMEM lane quarter of this warp
-        const int etid = threadIdx.x - 64;   // 0..127
+        const int e = warp - 2;              // epilogue warp 0..7
+        const int c_begin = (e >> 2) * (BN / 2);  // warpgroup e/4 drains this half of the columns
+        const int etid = threadIdx.x - 64;   // 0..255
         const int row_local = q * 32 + lane;
-        CStager<kOut> out{epi_smem + static_cast<uint32_t>(warp - 2) * 2u * kEpiBufBytes, 0u, lane};
+        CStager<kOut> out{epi_smem + static_cast<uint32_t>(e) * 2u * epi_buf_bytes<kOut>(), 0u, lane};
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t epi_phase = 0;
@@ -455,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(tempty_bar(acc));
             };
-            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, etid, last_flag, ctl,
-                                      epi_sync, release))
+            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, c_begin, etid,
+                                      last_flag, ctl, epi_sync, release))
                 break;
             if (++acc == 2) {
                 acc = 0;

@@ -37,9 +37,9 @@ struct PairShape {
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-template <int BN>
+template <int BN, int kOut>
 __host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
-    return 1024u + stages * PairShape<BN>::kStageBytes + kEpiSmemBytes + 8u * (2 * stages + 6) + 16u;
+    return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 6) + 16u;
 }
 
 template <int BN, int kOut>
@@ -54,14 +54,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int S = p.stages;
 
     const uint32_t epi_smem = base + S * PS::kStageBytes;  // output staging
-    const uint32_t bars = epi_smem + kEpiSmemBytes;
+    const uint32_t bars = epi_smem + epi_smem_bytes<kOut>();
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     const uint32_t epi_bar = bars + 8u * (2 * S + 5);
-    uint8_t* misc = base_ptr + S * PS::kStageBytes + kEpiSmemBytes + 8u * (2 * S + 6);
+    uint8_t* misc = base_ptr + S * PS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 6);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
@@ -78,10 +78,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);                    // one multicast commit
-            mbar_init(tempty_bar(a), 2 * kEpiThreads / 32);  // every epilogue warp of the pair
+            mbar_init(tempty_bar(a), 2 * kEpiWarps);  // every epilogue warp of the pair
         }
         mbar_init(drain_bar, 1);
-        mbar_init(epi_bar, kEpiThreads / 32);
+        mbar_init(epi_bar, kEpiWarps);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -174,17 +174,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    // (TMA-written operands are visible to the MMA once the
+                    // full barrier completes; no tcgen05 fence is needed.)
                     {
                         const uint32_t a_addr = base + stage * PS::kStageBytes;
-                        const uint32_t b_addr = a_addr + PS::kABytes;
-#pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            const uint64_t ad = smem_desc_sw128(a_addr + k * 32u, 16u, 1024u);
-                            const uint64_t bd = smem_desc_sw128(b_addr + k * 2048u, 8192u, 1024u);
-                            umma_f16<2>(d_tmem, ad, bd, p.idesc, (kb > un.kb0 || k > 0) ? 1u : 0u);
-                        }
-                        umma_commit_pair(empty_bar(stage), 0x3);
+                        const uint64_t ad = smem_desc_sw128(a_addr, 16u, 1024u);
+                        const uint64_t bd = smem_desc_sw128(a_addr + PS::kABytes, 8192u, 1024u);
+                        // the k-th 16-deep step: +32 B of A (+2 in the 16-byte
+                        // address field), +16 rows of B (+2048 B, +128)
+                        umma_f16<2>(d_tmem, ad, bd, p.idesc, kb > un.kb0 ? 1u : 0u);
+                        umma_f16<2>(d_tmem, ad + 2, bd + 128, p.idesc, 1u);
+                        umma_f16<2>(d_tmem, ad + 4, bd + 256, p.idesc, 1u);
+                        umma_f16<2>(d_tmem, ad + 6, bd + 384, p.idesc, 1u);
+                        umma_commit_pair(empty_bar(stage), 0x3);  // slot free in both CTAs
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -204,10 +206,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ----------------------------------------------- epilogue (both) --
-        const int q = warp & 3;
+        const int q = warp & 3;                   // TMEM lane quarter of this warp
+        const int e = warp - 2;                   // epilogue warp 0..7
+        const int c_begin = (e >> 2) * (BN / 2);  // warpgroup e/4 drains this half of the columns
         const int etid = threadIdx.x - 64;
         const int row_local = q * 32 + lane;
-        CStager<kOut> out{epi_smem + static_cast<uint32_t>(warp - 2) * 2u * kEpiBufBytes, 0u, lane};
+        CStager<kOut> out{epi_smem + static_cast<uint32_t>(e) * 2u * epi_buf_bytes<kOut>(), 0u, lane};
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t epi_phase = 0;
@@ -247,8 +251,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // workspace tile and counter of this CTA's 128-row half
             const int64_t half = un.slot * 2 + rank;
             const int a_now = acc;
-            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, half, etid, last_flag, ctl,
-                                      epi_sync, [&]() { release_acc(a_now); }))
+            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, half, c_begin, etid, last_flag,
+                                      ctl, epi_sync, [&]() { release_acc(a_now); }))
                 break;
             if (++acc == 2) {
                 acc = 0;

@@ -10,13 +10,13 @@ namespace tsg {
 const void* kernel_1sm(int block_n, int out_kind);
 
 // Dynamic shared memory the kernel above uses with `stages` ring slots.
-int64_t kernel_1sm_smem_bytes(int block_n, int stages);
+int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages);
 
 // The CTA-pair kernel (256 x block_n tiles, block_n 128 or 256), launched
 // with 2 x 1 clusters; null for an unsupported combination.
 const void* kernel_2sm(int block_n, int out_kind);
 
 // Dynamic shared memory per CTA of the pair kernel with `stages` slots.
-int64_t kernel_2sm_smem_bytes(int block_n, int stages);
+int64_t kernel_2sm_smem_bytes(int block_n, int out_kind, int stages);
 
 }  // namespace tsg

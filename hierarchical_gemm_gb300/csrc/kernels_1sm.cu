@@ -3,6 +3,8 @@
 #include "gemm_sm103.cuh"
 #include "kernels.h"
 
+#include <type_traits>
+
 namespace tsg {
 
 namespace {
@@ -27,12 +29,21 @@ const void* kernel_1sm(int block_n, int out_kind) {
     }
 }
 
-int64_t kernel_1sm_smem_bytes(int block_n, int stages) {
+int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages) {
+    auto pick = [&](auto bn) -> int64_t {
+        constexpr int BN = decltype(bn)::value;
+        switch (out_kind) {
+            case kOutF16: return smem_bytes_1sm<BN, kOutF16>(stages);
+            case kOutBF16: return smem_bytes_1sm<BN, kOutBF16>(stages);
+            case kOutF32: return smem_bytes_1sm<BN, kOutF32>(stages);
+            default: return -1;
+        }
+    };
     switch (block_n) {
-        case 64: return smem_bytes_1sm<64>(stages);
-        case 128: return smem_bytes_1sm<128>(stages);
-        case 192: return smem_bytes_1sm<192>(stages);
-        case 256: return smem_bytes_1sm<256>(stages);
+        case 64: return pick(std::integral_constant<int, 64>{});
+        case 128: return pick(std::integral_constant<int, 128>{});
+        case 192: return pick(std::integral_constant<int, 192>{});
+        case 256: return pick(std::integral_constant<int, 256>{});
         default: return -1;
     }
 }

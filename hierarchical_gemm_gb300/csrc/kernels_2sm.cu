@@ -3,6 +3,8 @@
 #include "gemm_sm103_2sm.cuh"
 #include "kernels.h"
 
+#include <type_traits>
+
 namespace tsg {
 
 namespace {
@@ -25,10 +27,19 @@ const void* kernel_2sm(int block_n, int out_kind) {
     }
 }
 
-int64_t kernel_2sm_smem_bytes(int block_n, int stages) {
+int64_t kernel_2sm_smem_bytes(int block_n, int out_kind, int stages) {
+    auto pick = [&](auto bn) -> int64_t {
+        constexpr int BN = decltype(bn)::value;
+        switch (out_kind) {
+            case kOutF16: return smem_bytes_2sm<BN, kOutF16>(stages);
+            case kOutBF16: return smem_bytes_2sm<BN, kOutBF16>(stages);
+            case kOutF32: return smem_bytes_2sm<BN, kOutF32>(stages);
+            default: return -1;
+        }
+    };
     switch (block_n) {
-        case 128: return smem_bytes_2sm<128>(stages);
-        case 256: return smem_bytes_2sm<256>(stages);
+        case 128: return pick(std::integral_constant<int, 128>{});
+        case 256: return pick(std::integral_constant<int, 256>{});
         default: return -1;
     }
 }

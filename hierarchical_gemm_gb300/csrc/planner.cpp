@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int64_t kEpiStagingBytes = 32768;  // output staging of the epilogue warps
+constexpr int64_t kEpiWarps = 8;  // epilogue warps, each staging two 32 x 32 output blocks
 constexpr double kMacsPerCycle = 4096.0;
 constexpr double kL2BytesPerCycle = 72.0;     // operand feed per SM (measured ballpark)
 constexpr double kHbmBytesPerCycle = 3500.0;  // whole GPU (model)
@@ -82,15 +82,17 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int dout, int bm, int bn, int
 
 }  // namespace
 
-int64_t smem_bytes_for(int block_m, int block_n, int stages) {
+int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages) {
     const int64_t b_cols = block_m == 256 ? block_n / 2 : block_n;
     const int64_t stage = static_cast<int64_t>(kBM) * kBK * 2 + b_cols * kBK * 2;
-    return 1024 + stages * stage + kEpiStagingBytes + 8 * (2 * stages + 6) + 16;
+    // output staging: 8 epilogue warps x 2 buffers of one 32 x 32 block
+    const int64_t staging = kEpiWarps * 2 * 32 * 32 * out_bytes(dtype_out);
+    return 1024 + stages * stage + staging + 8 * (2 * stages + 6) + 16;
 }
 
-int max_stages_for(int block_m, int block_n) {
+int max_stages_for(int block_m, int block_n, int dtype_out) {
     int s = 1;
-    while (s < 16 && smem_bytes_for(block_m, block_n, s + 1) <= kSmemPerCtaMax) ++s;
+    while (s < 16 && smem_bytes_for(block_m, block_n, dtype_out, s + 1) <= kSmemPerCtaMax) ++s;
     return s;
 }
 
@@ -186,7 +188,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     c.block_m = best_bm;
     c.block_n = best_bn;
     c.splits = best_s;
-    const int smax_fit = max_stages_for(best_bm, best_bn);
+    const int smax_fit = max_stages_for(best_bm, best_bn, dtype_out);
     if (f.stages > smax_fit || (f.stages != 0 && f.stages < 2)) return TSGEMM_ERR_UNSUPPORTED;
     c.stages = f.stages ? f.stages : smax_fit;
     c.group_m = f.group_m ? f.group_m : 8;

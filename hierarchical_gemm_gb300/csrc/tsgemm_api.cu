@@ -137,9 +137,9 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     const bool pair = cfg.block_m == 256;
     const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out))
                             : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out));
-    const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, cfg.stages)
-                              : tsg::kernel_1sm_smem_bytes(cfg.block_n, cfg.stages);
-    if (!kern || need != tsg::smem_bytes_for(cfg.block_m, cfg.block_n, cfg.stages) ||
+    const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages)
+                              : tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages);
+    if (!kern || need != tsg::smem_bytes_for(cfg.block_m, cfg.block_n, dtype_out, cfg.stages) ||
         need > tsg::kSmemPerCtaMax)
         return TSGEMM_ERR_UNSUPPORTED;
     // Ask for more than half the SM's shared memory even when the ring is

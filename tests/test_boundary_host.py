@@ -104,7 +104,11 @@ def test_planner_invariants(ts, shape, sms):
     assert c["grid"] % per == 0 and 1 <= c["grid"] <= per * min(sms // per, c["units"])
     assert c["workspace_bytes"] == st * bm * bn * 4
     stage = 128 * 64 * 2 + (bn // per) * 64 * 2
-    assert 1024 + c["stages"] * stage + 8 * (2 * c["stages"] + 6) + 16 <= 232448
+    staging = 8 * 2 * 32 * 32 * (4 if dout == "f32" else 2)  # 8 epilogue warps x 2 blocks
+    smem = 1024 + c["stages"] * stage + staging + 8 * (2 * c["stages"] + 6) + 16
+    assert smem <= 232448
+    # the ring is as deep as the shared memory allows
+    assert smem + stage > 232448 or c["stages"] == 16
     assert c["timeout_ms"] == 1000
 
 
