@@ -49,6 +49,22 @@ constexpr int kMaxStages = 16;
 
 enum OutKind { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2 };
 
+// Operand layouts (the tsgemm_layout_t values): bit 1 set = A stored K x M
+// (column-major A, M contiguous); bit 0 set = B stored N x K (column-major
+// B, K contiguous -- the transpose_B form).  C is always M x N row-major.
+__host__ __device__ constexpr bool a_kmajor(int layout) { return (layout & 2) == 0; }
+__host__ __device__ constexpr bool b_kmajor(int layout) { return (layout & 1) != 0; }
+
+// Shared-memory operand tiles use the 128-byte swizzle either way:
+//   K-major (rows of 64 K-elements, 128 B): 8-row groups 1024 B apart, the
+//     k-th 16-deep MMA step is 32 B along the row (+2 in the descriptor's
+//     16-byte address field);
+//   MN-major (64 M/N-elements per 128-B row, one row per k): 64-wide boxes
+//     8 KiB apart (LBO), 8-row groups 1024 B apart (SBO), the k-th step is
+//     16 rows, 2048 B (+128).
+__host__ __device__ constexpr uint32_t op_lbo(bool kmajor) { return kmajor ? 16u : 8192u; }
+__host__ __device__ constexpr uint64_t op_kstep(bool kmajor) { return kmajor ? 2u : 128u; }
+
 struct GemmParams {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n;
@@ -285,6 +301,48 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
     return epi_sync();
 }
 
+// TMA loads of K-slice kb into a ring slot: A rows [row, row + 128) at
+// a_dst, B columns [col, col + kBCols) at b_dst, in the layout's operand
+// order.  kRemote: the completion goes to a barrier of the peer CTA (the
+// pair's leader), which needs the cta_group::2 form of the copy.
+template <int kLayout, int kBCols, bool kRemote>
+__device__ __forceinline__ void load_slice(uint32_t a_dst, uint32_t b_dst, const CUtensorMap* tmA,
+                                           const CUtensorMap* tmB, uint32_t bar, int kb, int32_t row,
+                                           int32_t col) {
+    auto ld = [&](uint32_t dst, const CUtensorMap* m, int32_t c0, int32_t c1) {
+        if constexpr (kRemote)
+            tma_load_2d_pair(dst, m, bar, c0, c1);
+        else
+            tma_load_2d(dst, m, bar, c0, c1);
+    };
+    if constexpr (a_kmajor(kLayout)) {
+        ld(a_dst, tmA, kb * kBK, row);  // one 64 (K) x 128 (M) box
+    } else {
+        ld(a_dst, tmA, row, kb * kBK);  // two 64 (M) x 64 (K) boxes
+        ld(a_dst + 8192u, tmA, row + 64, kb * kBK);
+    }
+    if constexpr (b_kmajor(kLayout)) {
+        ld(b_dst, tmB, kb * kBK, col);  // one 64 (K) x kBCols (N) box
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBCols / 64; ++j) ld(b_dst + j * 8192u, tmB, col + j * 64, kb * kBK);
+    }
+}
+
+// The four 16-deep MMAs of one K-slice held at a_addr / b_addr.
+template <int kLayout, int kCtaGroup>
+__device__ __forceinline__ void mma_slice(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc,
+                                          uint32_t accumulate) {
+    constexpr bool ak = a_kmajor(kLayout), bk = b_kmajor(kLayout);
+    const uint64_t ad = smem_desc_sw128(a_addr, op_lbo(ak), 1024u);
+    const uint64_t bd = smem_desc_sw128(b_addr, op_lbo(bk), 1024u);
+    constexpr uint64_t as = op_kstep(ak), bs = op_kstep(bk);
+    umma_f16<kCtaGroup>(d_tmem, ad, bd, idesc, accumulate);
+    umma_f16<kCtaGroup>(d_tmem, ad + as, bd + bs, idesc, 1u);
+    umma_f16<kCtaGroup>(d_tmem, ad + 2 * as, bd + 2 * bs, idesc, 1u);
+    umma_f16<kCtaGroup>(d_tmem, ad + 3 * as, bd + 3 * bs, idesc, 1u);
+}
+
 template <int BN>
 struct TileShape {
     static constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KiB
@@ -304,7 +362,7 @@ __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
            8u * (2 * stages + 6) /* barriers */ + 16u /* tmem holder, flags */;
 }
 
-template <int BN, int kOut>
+template <int BN, int kOut, int kLayout>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_sm103_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -377,11 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const uint32_t a_dst = base + stage * TS::kStageBytes;
                         mbar_arrive_expect_tx(full_bar(stage), TS::kStageBytes);
-                        tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, un.tm * kBM);
-#pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(a_dst + TS::kABytes + j * 8192u, &tmB, full_bar(stage), un.tn * BN + j * 64,
-                                        kb * kBK);
+                        load_slice<kLayout, BN, false>(a_dst, a_dst + TS::kABytes, &tmA, &tmB, full_bar(stage), kb,
+                                                       un.tm * kBM, un.tn * BN);
                         outstanding |= 1u << stage;
                         out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -417,18 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // (TMA-written operands are visible to the MMA once the
                     // full barrier completes; no tcgen05 fence is needed.)
                     const uint32_t a_addr = base + stage * TS::kStageBytes;
-                    // A: K-major, rows 128 B apart, 8-row groups 1024 B apart;
-                    //    the k-th 16-element step is 32 B along the row (+2 in
-                    //    the descriptor's 16-byte address field).
-                    // B: MN-major, 64-column boxes 8 KiB apart (LBO), 8-row
-                    //    groups 1024 B apart (SBO); the k-th step is 16 rows
-                    //    (+2048 B, +128).
-                    const uint64_t ad = smem_desc_sw128(a_addr, 16u, 1024u);
-                    const uint64_t bd = smem_desc_sw128(a_addr + TS::kABytes, 8192u, 1024u);
-                    umma_f16<1>(d_tmem, ad, bd, p.idesc, kb > un.kb0 ? 1u : 0u);
-                    umma_f16<1>(d_tmem, ad + 2, bd + 128, p.idesc, 1u);
-                    umma_f16<1>(d_tmem, ad + 4, bd + 256, p.idesc, 1u);
-                    umma_f16<1>(d_tmem, ad + 6, bd + 384, p.idesc, 1u);
+                    mma_slice<kLayout, 1>(d_tmem, a_addr, a_addr + TS::kABytes, p.idesc, kb > un.kb0 ? 1u : 0u);
                     umma_commit(empty_bar(stage));  // slot free once these MMAs have read it
                     if (++stage == S) {
                         stage = 0;

@@ -42,7 +42,7 @@ __host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
     return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 6) + 16u;
 }
 
-template <int BN, int kOut>
+template <int BN, int kOut, int kLayout>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_sm103_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -127,18 +127,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int32_t bcol = un.tn * BN + static_cast<int32_t>(rank) * PS::kBCols;
                         if (leader) {
                             mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
-                            tma_load_2d(a_dst, &tmA, full_bar(stage), kb * kBK, arow);
-#pragma unroll
-                            for (int j = 0; j < static_cast<int>(PS::kBCols) / 64; ++j)
-                                tma_load_2d(a_dst + PS::kABytes + j * 8192u, &tmB, full_bar(stage), bcol + j * 64,
-                                            kb * kBK);
+                            load_slice<kLayout, PS::kBCols, false>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                   full_bar(stage), kb, arow, bcol);
                         } else {
-                            const uint32_t lbar = mapa_shared(full_bar(stage), 0u);
-                            tma_load_2d_pair(a_dst, &tmA, lbar, kb * kBK, arow);
-#pragma unroll
-                            for (int j = 0; j < static_cast<int>(PS::kBCols) / 64; ++j)
-                                tma_load_2d_pair(a_dst + PS::kABytes + j * 8192u, &tmB, lbar, bcol + j * 64,
-                                                 kb * kBK);
+                            load_slice<kLayout, PS::kBCols, true>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                  mapa_shared(full_bar(stage), 0u), kb, arow, bcol);
                         }
                         outstanding |= 1u << stage;
                         out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
@@ -178,14 +171,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // full barrier completes; no tcgen05 fence is needed.)
                     {
                         const uint32_t a_addr = base + stage * PS::kStageBytes;
-                        const uint64_t ad = smem_desc_sw128(a_addr, 16u, 1024u);
-                        const uint64_t bd = smem_desc_sw128(a_addr + PS::kABytes, 8192u, 1024u);
-                        // the k-th 16-deep step: +32 B of A (+2 in the 16-byte
-                        // address field), +16 rows of B (+2048 B, +128)
-                        umma_f16<2>(d_tmem, ad, bd, p.idesc, kb > un.kb0 ? 1u : 0u);
-                        umma_f16<2>(d_tmem, ad + 2, bd + 128, p.idesc, 1u);
-                        umma_f16<2>(d_tmem, ad + 4, bd + 256, p.idesc, 1u);
-                        umma_f16<2>(d_tmem, ad + 6, bd + 384, p.idesc, 1u);
+                        mma_slice<kLayout, 2>(d_tmem, a_addr, a_addr + PS::kABytes, p.idesc,
+                                              kb > un.kb0 ? 1u : 0u);
                         umma_commit_pair(empty_bar(stage), 0x3);  // slot free in both CTAs
                     }
                     if (++stage == S) {

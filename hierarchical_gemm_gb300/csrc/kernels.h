@@ -5,18 +5,29 @@
 
 namespace tsg {
 
-// Kernel entry for a tile width (64/128/192/256) and output kind
-// (0 fp16, 1 bf16, 2 fp32); null for an unsupported combination.
-const void* kernel_1sm(int block_n, int out_kind);
+// Kernel entry for a tile width (64/128/192/256), output kind (0 fp16,
+// 1 bf16, 2 fp32) and operand layout (tsgemm_layout_t); null for an
+// unsupported combination.
+const void* kernel_1sm(int block_n, int out_kind, int layout);
 
 // Dynamic shared memory the kernel above uses with `stages` ring slots.
 int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages);
 
 // The CTA-pair kernel (256 x block_n tiles, block_n 128 or 256), launched
 // with 2 x 1 clusters; null for an unsupported combination.
-const void* kernel_2sm(int block_n, int out_kind);
+const void* kernel_2sm(int block_n, int out_kind, int layout);
 
 // Dynamic shared memory per CTA of the pair kernel with `stages` slots.
 int64_t kernel_2sm_smem_bytes(int block_n, int out_kind, int stages);
+
+// Per-layout tables (one translation unit each).
+const void* kernel_1sm_layout0(int block_n, int out_kind);
+const void* kernel_1sm_layout1(int block_n, int out_kind);
+const void* kernel_1sm_layout2(int block_n, int out_kind);
+const void* kernel_1sm_layout3(int block_n, int out_kind);
+const void* kernel_2sm_layout0(int block_n, int out_kind);
+const void* kernel_2sm_layout1(int block_n, int out_kind);
+const void* kernel_2sm_layout2(int block_n, int out_kind);
+const void* kernel_2sm_layout3(int block_n, int out_kind);
 
 }  // namespace tsg

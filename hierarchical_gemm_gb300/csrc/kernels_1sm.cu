@@ -1,5 +1,6 @@
-// kernels_1sm.cu -- instantiations of the one-SM-per-tile kernel for every
-// tile width and output format, and the lookup the host API uses.
+// kernels_1sm.cu -- the host-side lookup of the one-SM kernel's
+// instantiations (by tile width, output format and operand layout) and of
+// the shared memory each needs.
 #include "gemm_sm103.cuh"
 #include "kernels.h"
 
@@ -7,24 +8,12 @@
 
 namespace tsg {
 
-namespace {
-template <int BN>
-const void* pick_out(int out) {
-    switch (out) {
-        case kOutF16: return reinterpret_cast<const void*>(&gemm_sm103_1sm<BN, kOutF16>);
-        case kOutBF16: return reinterpret_cast<const void*>(&gemm_sm103_1sm<BN, kOutBF16>);
-        case kOutF32: return reinterpret_cast<const void*>(&gemm_sm103_1sm<BN, kOutF32>);
-        default: return nullptr;
-    }
-}
-}  // namespace
-
-const void* kernel_1sm(int block_n, int out_kind) {
-    switch (block_n) {
-        case 64: return pick_out<64>(out_kind);
-        case 128: return pick_out<128>(out_kind);
-        case 192: return pick_out<192>(out_kind);
-        case 256: return pick_out<256>(out_kind);
+const void* kernel_1sm(int block_n, int out_kind, int layout) {
+    switch (layout) {
+        case 0: return kernel_1sm_layout0(block_n, out_kind);
+        case 1: return kernel_1sm_layout1(block_n, out_kind);
+        case 2: return kernel_1sm_layout2(block_n, out_kind);
+        case 3: return kernel_1sm_layout3(block_n, out_kind);
         default: return nullptr;
     }
 }

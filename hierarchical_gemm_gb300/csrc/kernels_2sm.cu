@@ -1,5 +1,6 @@
-// kernels_2sm.cu -- instantiations of the CTA-pair kernel (256 x 128 and
-// 256 x 256 tiles) for every output format.
+// kernels_2sm.cu -- the host-side lookup of the CTA-pair kernel's
+// instantiations (by tile width, output format and operand layout) and of
+// the shared memory each needs.
 #include "gemm_sm103_2sm.cuh"
 #include "kernels.h"
 
@@ -7,22 +8,12 @@
 
 namespace tsg {
 
-namespace {
-template <int BN>
-const void* pick_out_2sm(int out) {
-    switch (out) {
-        case kOutF16: return reinterpret_cast<const void*>(&gemm_sm103_2sm<BN, kOutF16>);
-        case kOutBF16: return reinterpret_cast<const void*>(&gemm_sm103_2sm<BN, kOutBF16>);
-        case kOutF32: return reinterpret_cast<const void*>(&gemm_sm103_2sm<BN, kOutF32>);
-        default: return nullptr;
-    }
-}
-}  // namespace
-
-const void* kernel_2sm(int block_n, int out_kind) {
-    switch (block_n) {
-        case 128: return pick_out_2sm<128>(out_kind);
-        case 256: return pick_out_2sm<256>(out_kind);
+const void* kernel_2sm(int block_n, int out_kind, int layout) {
+    switch (layout) {
+        case 0: return kernel_2sm_layout0(block_n, out_kind);
+        case 1: return kernel_2sm_layout1(block_n, out_kind);
+        case 2: return kernel_2sm_layout2(block_n, out_kind);
+        case 3: return kernel_2sm_layout3(block_n, out_kind);
         default: return nullptr;
     }
 }

@@ -1,0 +1,28 @@
+// kernels_2sm_l2.cu -- instantiations of the CTA-pair kernel for the
+// CRR operand layout, every tile width and output format.
+#include "gemm_sm103_2sm.cuh"
+#include "kernels.h"
+
+namespace tsg {
+
+namespace {
+template <int BN>
+const void* pick(int out) {
+    switch (out) {
+        case kOutF16: return reinterpret_cast<const void*>(&gemm_sm103_2sm<BN, kOutF16, 2>);
+        case kOutBF16: return reinterpret_cast<const void*>(&gemm_sm103_2sm<BN, kOutBF16, 2>);
+        case kOutF32: return reinterpret_cast<const void*>(&gemm_sm103_2sm<BN, kOutF32, 2>);
+        default: return nullptr;
+    }
+}
+}  // namespace
+
+const void* kernel_2sm_layout2(int block_n, int out_kind) {
+    switch (block_n) {
+        case 128: return pick<128>(out_kind);
+        case 256: return pick<256>(out_kind);
+        default: return nullptr;
+    }
+}
+
+}  // namespace tsg

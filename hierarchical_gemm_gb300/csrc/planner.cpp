@@ -101,14 +101,15 @@ tsgemm_status_t validate_problem(int64_t M, int64_t N, int64_t K, int dtype_in, 
     if (M < 1 || N < 1 || K < 1) return TSGEMM_ERR_INVALID_ARG;
     if (dtype_in < TSGEMM_F16 || dtype_in > TSGEMM_F32) return TSGEMM_ERR_INVALID_ARG;
     if (dtype_out < TSGEMM_F16 || dtype_out > TSGEMM_F32) return TSGEMM_ERR_INVALID_ARG;
-    if (layout != TSGEMM_LAYOUT_RRR) return layout < 0 ? TSGEMM_ERR_INVALID_ARG : TSGEMM_ERR_UNSUPPORTED;
+    if (layout < TSGEMM_LAYOUT_RRR || layout > TSGEMM_LAYOUT_CCR) return TSGEMM_ERR_INVALID_ARG;
     if (!dtype_pair_ok(dtype_in, dtype_out)) return TSGEMM_ERR_UNSUPPORTED;
     // Tensor-map coordinates and the kernel's tile indices are 32-bit.
     const int64_t lim = (int64_t{1} << 31) - 1;
     if (M > lim || N > lim || K > lim) return TSGEMM_ERR_UNSUPPORTED;
-    // Row strides of A (K * 2), B (N * 2) and C (N * out) must be multiples
-    // of 16 bytes for TMA and for the 16-byte vector stores.
-    if ((K * 2) % 16 != 0 || (N * 2) % 16 != 0 || (N * out_bytes(dtype_out)) % 16 != 0)
+    // Stored row strides of A, B and C must be multiples of 16 bytes (TMA).
+    const int64_t a_row = (layout & 2) ? M : K;  // A stored K x M, or M x K
+    const int64_t b_row = (layout & 1) ? K : N;  // B stored N x K, or K x N
+    if ((a_row * 2) % 16 != 0 || (b_row * 2) % 16 != 0 || (N * out_bytes(dtype_out)) % 16 != 0)
         return TSGEMM_ERR_ALIGNMENT;
     return TSGEMM_OK;
 }

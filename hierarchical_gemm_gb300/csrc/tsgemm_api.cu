@@ -42,13 +42,15 @@ EncodeTiledFn encode_fn() {
 //   bits  4-5  accumulator format (1 = fp32)
 //   bits  7-9  A format (0 = fp16, 1 = bf16)
 //   bits 10-12 B format
-//   bit  15    A major (0 = K-major)
-//   bit  16    B major (1 = MN-major: B is K x N with N contiguous)
+//   bit  15    A major (0 = K-major: A stored M x K; 1 = MN-major: stored K x M)
+//   bit  16    B major (0 = K-major: B stored N x K; 1 = MN-major: stored K x N)
 //   bits 17-22 N >> 3
 //   bits 24-28 M >> 4
-uint32_t make_idesc(int dtype_in, int m, int n) {
+uint32_t make_idesc(int dtype_in, int m, int n, int layout) {
     const uint32_t fmt = dtype_in == TSGEMM_BF16 ? 1u : 0u;
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
+    const uint32_t a_mn = tsg::a_kmajor(layout) ? 0u : 1u;
+    const uint32_t b_mn = tsg::b_kmajor(layout) ? 0u : 1u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) |
            (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
@@ -63,6 +65,7 @@ int64_t elem_bytes(int dt) { return dt == TSGEMM_F32 ? 4 : 2; }
 struct tsgemm_plan_s {
     int64_t M, N, K;
     int dtype_in, dtype_out;
+    int layout;
     tsgemm_config_t cfg;
     int device;
     const void* kernel;
@@ -135,8 +138,8 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     if (st != TSGEMM_OK) return st;
 
     const bool pair = cfg.block_m == 256;
-    const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out))
-                            : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out));
+    const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out), layout)
+                            : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out), layout);
     const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages)
                               : tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages);
     if (!kern || need != tsg::smem_bytes_for(cfg.block_m, cfg.block_n, dtype_out, cfg.stages) ||
@@ -176,6 +179,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     p->K = K;
     p->dtype_in = dtype_in;
     p->dtype_out = dtype_out;
+    p->layout = layout;
     p->cfg = cfg;
     p->device = dev;
     p->kernel = kern;
@@ -221,7 +225,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.debug_flags = cfg.debug_flags;
     gp.units = cfg.units;
     gp.full_tiles = ((M + cfg.block_m - 1) / cfg.block_m) * ((N + cfg.block_n - 1) / cfg.block_n) - cfg.split_tiles;
-    gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n);
+    gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n, layout);
     gp.C = nullptr;
     gp.ws = p->ws;
     gp.counters = p->counters;
@@ -265,27 +269,25 @@ static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* 
     const CUtensorMapDataType dt =
         p->dtype_in == TSGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint32_t estr[2] = {1, 1};
-    {
-        // A: inner dimension K, outer M; box 64 x 128 (one 128-byte swizzle row per M row)
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->K) * 2};
-        const cuuint32_t box[2] = {64, 128};
-        if (enc(&p->tmA, dt, 2, const_cast<void*>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return TSGEMM_ERR_CUDA;
-    }
-    {
-        // B: inner dimension N, outer K; box 64 x 64 (64 columns = 128 bytes)
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->K)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->N) * 2};
-        const cuuint32_t box[2] = {64, 64};
-        if (enc(&p->tmB, dt, 2, const_cast<void*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return TSGEMM_ERR_CUDA;
-    }
-    return TSGEMM_OK;
+    auto tile_map = [&](CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, cuuint32_t box_inner,
+                        cuuint32_t box_outer) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+        const cuuint32_t box[2] = {box_inner, box_outer};
+        return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    // Every box is 64 elements (128 bytes, one swizzle row) along the
+    // contiguous dimension.
+    //   A stored M x K: 64 (K) x 128 (M) boxes;  A stored K x M: 64 (M) x 64 (K)
+    //   B stored K x N: 64 (N) x 64 (K) boxes;   B stored N x K: 64 (K) x the
+    //   CTA's columns (N) -- block_n, or block_n / 2 for a CTA pair
+    const bool ak = tsg::a_kmajor(p->layout), bk = tsg::b_kmajor(p->layout);
+    const cuuint32_t b_cols = static_cast<cuuint32_t>(p->cfg.block_m == 256 ? p->cfg.block_n / 2 : p->cfg.block_n);
+    const bool ok_a = ak ? tile_map(&p->tmA, A, p->K, p->M, 64, 128) : tile_map(&p->tmA, A, p->M, p->K, 64, 64);
+    const bool ok_b = bk ? tile_map(&p->tmB, B, p->K, p->N, 64, b_cols) : tile_map(&p->tmB, B, p->N, p->K, 64, 64);
+    return ok_a && ok_b ? TSGEMM_OK : TSGEMM_ERR_CUDA;
 }
 
 // C: inner dimension N, outer M; box 32 x 32 (the block one epilogue warp

@@ -11,7 +11,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libtsgemm.so")
 
 F16, BF16, F32 = 0, 1, 2
-LAYOUT_RRR = 0
+# operand storage: A M x K or K x M (column-major), B K x N or N x K
+LAYOUT_RRR, LAYOUT_RCR, LAYOUT_CRR, LAYOUT_CCR = 0, 1, 2, 3
+_LAYOUT_NAMES = {"rrr": LAYOUT_RRR, "rcr": LAYOUT_RCR, "crr": LAYOUT_CRR, "ccr": LAYOUT_CCR}
 
 OK = 0
 ERR_INVALID_ARG = 1
@@ -102,6 +104,13 @@ def dtype_code(d):
     return _DTYPE_NAMES[s]
 
 
+def layout_code(layout):
+    """tsgemm layout code from a code or a name ("rrr", "rcr", "crr", "ccr")."""
+    if isinstance(layout, int):
+        return layout
+    return _LAYOUT_NAMES[str(layout).lower()]
+
+
 def _force(kw):
     c = Config()
     for k, v in kw.items():
@@ -111,12 +120,12 @@ def _force(kw):
     return c
 
 
-def choose_config(M, N, K, dtype_in, dtype_out, num_sms, **force):
+def choose_config(M, N, K, dtype_in, dtype_out, num_sms, layout=LAYOUT_RRR, **force):
     """The planner's configuration for a problem (host only, no GPU)."""
     out = Config()
     f = _force(force)
     _check(lib.tsgemm_choose_config(M, N, K, dtype_code(dtype_in), dtype_code(dtype_out),
-                                    LAYOUT_RRR, int(num_sms), ctypes.byref(f), ctypes.byref(out)),
+                                    layout_code(layout), int(num_sms), ctypes.byref(f), ctypes.byref(out)),
            "tsgemm_choose_config")
     return out.as_dict()
 
@@ -139,19 +148,23 @@ def _stream_handle(stream):
 
 
 class Plan:
-    """A planned GEMM C (M x N) = A (M x K) * B (K x N) on the current device."""
+    """A planned GEMM C (M x N) = A (M x K) * B (K x N) on the current device.
 
-    def __init__(self, M, N, K, dtype_in, dtype_out, **force):
+    `layout` says how A and B are stored (LAYOUT_RRR: A M x K and B K x N
+    row-major; RCR: B stored N x K; CRR: A stored K x M; CCR: both)."""
+
+    def __init__(self, M, N, K, dtype_in, dtype_out, layout=LAYOUT_RRR, **force):
         self._h = ctypes.c_void_p()
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.dtype_in, self.dtype_out = dtype_code(dtype_in), dtype_code(dtype_out)
+        self.layout = layout_code(layout)
         if force:
             f = _force(force)
             code = lib.tsgemm_plan_ex(ctypes.byref(self._h), self.M, self.N, self.K,
-                                      self.dtype_in, self.dtype_out, LAYOUT_RRR, ctypes.byref(f))
+                                      self.dtype_in, self.dtype_out, self.layout, ctypes.byref(f))
         else:
             code = lib.tsgemm_plan(ctypes.byref(self._h), self.M, self.N, self.K,
-                                   self.dtype_in, self.dtype_out, LAYOUT_RRR)
+                                   self.dtype_in, self.dtype_out, self.layout)
         _check(code, "tsgemm_plan")
 
     @property

@@ -25,9 +25,9 @@
  *
  * Memory.  A, B and C are device pointers owned by the caller, on the device
  * that was current when the plan was made, 16-byte aligned, with C not
- * overlapping A or B.  Row strides must be multiples of 16 bytes: K * 2 and
- * N * 2 (the A and B rows) and N * sizeof(out) (the C rows); otherwise
- * TSGEMM_ERR_ALIGNMENT.
+ * overlapping A or B.  Stored row strides must be multiples of 16 bytes: A's
+ * (K * 2, or M * 2 when A is stored K x M), B's (N * 2, or K * 2 when B is
+ * stored N x K) and C's (N * sizeof(out)); otherwise TSGEMM_ERR_ALIGNMENT.
  *
  * Errors.  Every call returns a tsgemm_status_t.  Argument, alignment and
  * device errors are detected on the host before anything is launched.  A
@@ -59,9 +59,14 @@ typedef enum {
     TSGEMM_F32 = 2   /* IEEE binary32 (outputs only) */
 } tsgemm_dtype_t;
 
+/* Operand storage.  C is always M x N row-major.  The transposed-B forms are
+ * the T.gemm(..., transpose_B=True) of the TileScale examples (SUMMA and
+ * Cannon local GEMMs in the project_analysis.md notes). */
 typedef enum {
-    /* A M x K row-major, B K x N row-major, C M x N row-major */
-    TSGEMM_LAYOUT_RRR = 0
+    TSGEMM_LAYOUT_RRR = 0, /* A M x K row-major, B K x N row-major */
+    TSGEMM_LAYOUT_RCR = 1, /* A M x K row-major, B stored N x K row-major (B column-major) */
+    TSGEMM_LAYOUT_CRR = 2, /* A stored K x M row-major (A column-major), B K x N row-major */
+    TSGEMM_LAYOUT_CCR = 3  /* A stored K x M, B stored N x K */
 } tsgemm_layout_t;
 
 typedef enum {

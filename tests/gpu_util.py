@@ -18,14 +18,21 @@ def from_dev(C, dout):
     return c.view(torch.int16).numpy().view(np.uint16)
 
 
-def run_gemm(A_bits, B_bits, din, dout, device="cuda", repeat=1, **force):
-    """C = A * B through tsgemm; returns (C bits/values, plan config)."""
+def run_gemm(A_bits, B_bits, din, dout, device="cuda", repeat=1, layout="rrr", **force):
+    """C = A * B through tsgemm; returns (C bits/values, plan config).
+
+    A_bits (M x K) and B_bits (K x N) are the logical operands; for the
+    column-major layouts they are handed to the library transposed (A stored
+    K x M, B stored N x K)."""
     from hierarchical_gemm_gb300 import tsgemm
     M, K = A_bits.shape
     N = B_bits.shape[1]
-    plan = tsgemm.Plan(M, N, K, din, dout, **force)
-    A = to_dev(A_bits, din, device)
-    B = to_dev(B_bits, din, device)
+    code = tsgemm.layout_code(layout)
+    plan = tsgemm.Plan(M, N, K, din, dout, layout=code, **force)
+    A_store = np.ascontiguousarray(A_bits.T) if code & 2 else A_bits
+    B_store = np.ascontiguousarray(B_bits.T) if code & 1 else B_bits
+    A = to_dev(A_store, din, device)
+    B = to_dev(B_store, din, device)
     C = torch.full((M, N), float("nan"), dtype=TORCH_DT[dout], device=device)
     outs = []
     for _ in range(repeat):

@@ -75,7 +75,9 @@ def test_choose_config_rejects_bad_forced_values(ts):
 def test_bad_layout_and_null_output(ts):
     cfg = ts.Config()
     f = ts.Config()
-    assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, 1, 152, ctypes.byref(f), ctypes.byref(cfg)) == 2
+    for layout in (0, 1, 2, 3):
+        assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, layout, 152, ctypes.byref(f), ctypes.byref(cfg)) == 0
+    assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, 4, 152, ctypes.byref(f), ctypes.byref(cfg)) == 1
     assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, -1, 152, ctypes.byref(f), ctypes.byref(cfg)) == 1
     assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, 0, 152, ctypes.byref(f), None) == 1
     assert ts.lib.tsgemm_choose_config(64, 64, 64, 1, 1, 0, 0, ctypes.byref(f), ctypes.byref(cfg)) == 1
@@ -154,3 +156,21 @@ def test_run_and_status_reject_null_plan(ts):
     assert ts.lib.tsgemm_plan(ctypes.byref(h), 0, 8, 8, 1, 1, 0) == ts.ERR_INVALID_ARG
     assert h.value is None  # *out is cleared on failure
     assert ts.lib.tsgemm_plan(None, 8, 8, 8, 1, 1, 0) == ts.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("layout,shape,code", [
+    ("rrr", (12, 64, 64), 0),   # M is free when A is stored M x K
+    ("crr", (12, 64, 64), 3),   # A stored K x M: a row of 12 bf16 is 24 bytes
+    ("crr", (16, 64, 64), 0),
+    ("rcr", (64, 12, 64), 3),   # N * 2 = 24: C rows misaligned in any layout
+    ("rcr", (64, 64, 12), 3),   # B stored N x K: rows of K = 12
+    ("ccr", (64, 64, 24), 0),
+])
+def test_alignment_rules_per_layout(ts, layout, shape, code):
+    M, N, K = shape
+    if code == 0:
+        ts.choose_config(M, N, K, "bf16", "bf16", 152, layout=layout)
+    else:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(M, N, K, "bf16", "bf16", 152, layout=layout)
+        assert e.value.status == ts.ERR_ALIGNMENT

@@ -147,6 +147,49 @@ def test_tail_tiles_split(block_m, block_n, which):
     _check(C, A, B, "bf16", "f32", exact=True)
 
 
+LAYOUTS = ["rrr", "rcr", "crr", "ccr"]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("block_m,block_n", TILES)
+def test_layouts_every_tile_shape(layout, block_m, block_n):
+    # Operands stored transposed (column-major A: K x M; B: N x K) give the
+    # same product; integer inputs make the comparison bit-exact.
+    M, N, K = 264, 328, 1096
+    A = _ints(M, K, 34, dtype="bf16")
+    B = _ints(K, N, 35, dtype="bf16")
+    C, cfg = run_gemm(A, B, "bf16", "f32", layout=layout, block_m=block_m, block_n=block_n)
+    assert (cfg["block_m"], cfg["block_n"]) == (block_m, block_n)
+    _check(C, A, B, "bf16", "f32", exact=True)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_layouts_permutation_pins(layout):
+    # P * B and A * P with a permutation P, stored in each layout.
+    r = np.random.default_rng(36)
+    n = 256
+    perm = r.permutation(n)
+    P = np.zeros((n, n))
+    P[np.arange(n), perm] = 1.0
+    Pb = _bits_of(P, "f16")
+    B = _ints(n, 200, 37, -16, 16, "f16")
+    C, _ = run_gemm(Pb, B, "f16", "f16", layout=layout)
+    _check(C, Pb, B, "f16", "f16", exact=True)
+    A = _ints(136, n, 38, -16, 16, "f16")
+    C, _ = run_gemm(A, Pb, "f16", "f16", layout=layout)
+    _check(C, A, Pb, "f16", "f16", exact=True)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("splits", [1, 3])
+def test_layouts_random_real_inputs(layout, splits):
+    M, N, K = 520, 776, 2048
+    A = _unif(M, K, 39, "bf16")
+    B = _unif(K, N, 40, "bf16")
+    C, _ = run_gemm(A, B, "bf16", "bf16", layout=layout, splits=splits)
+    _check(C, A, B, "bf16", "bf16", exact=False)
+
+
 @pytest.mark.parametrize("block_m,grid", [(128, 1), (128, 3), (256, 2), (256, 6)])
 def test_persistent_loop_with_small_grid(block_m, grid):
     # Few CTAs walk many units: exercises ring-phase and accumulator-phase
