@@ -198,13 +198,12 @@ struct CStager {
 // at `tbase`; this thread holds row `row_local`, and its warp's 32 rows
 // start at row `row0` of C).
 //   * A whole tile is converted and stored to C.
-//   * Part s of a tile split along K adds itself to the running sum of the
-//     parts before it: it waits until the tile's counter says parts
-//     0..s-1 are done, reads the running sum from the workspace, adds its
-//     own accumulator (running + own, in fp32), and either writes the sum
-//     back and advances the counter, or -- the last part -- stores C and
-//     resets the counter.  The sum is thus p_0 + p_1 + ... + p_{S-1}, added
-//     in split order, the same bits on every run.
+//   * A part s > 0 of a tile split along K writes its fp32 partial and
+//     counts itself in; part 0 waits for the others, adds them to its own
+//     accumulator in split order and stores C.  The sum is p_0 + p_1 + ... +
+//     p_{S-1}, the same bits on every run.  Only part 0 waits, and for
+//     higher-numbered units, so the S parts of a tile must run on S
+//     different CTAs (or pairs): the planner keeps S within the grid.
 // `h` indexes the workspace tile and counter of this 128-row half;
 // `epi_sync` is the epilogue warpgroup's bounded barrier and `release` hands
 // the accumulator back to the MMA issuer.  Returns false if the CTA is
@@ -227,76 +226,91 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
         }
         return true;
     }
-    if (un.split > 0) {
-        if (etid == 0) *flag = wait_flag_bounded(p.counters + h, un.split, ctl) ? 1 : 0;
-        if (!epi_sync()) return false;
-        if (!*flag) return false;
-        __threadfence();
-    }
-    const bool last = un.split == un.nsplit - 1;
-    // The running sum of a 128 x BN half tile is stored in the order the
-    // epilogue warps hold it, so that every warp access is 512 contiguous
-    // bytes: [BN/32 column chunks][4 lane quarters][8 float4][32 lanes].
+    // A tile split along K: part 0 (k = 0) owns it.  Parts 1..S-1 write
+    // their fp32 partials to the workspace and count themselves in; the
+    // owner waits for S - 1 of them and stores C = p_0 + p_1 + ... + p_{S-1},
+    // added in split order.  Each partial of a 128 x BN half tile is stored
+    // in the order the epilogue warps hold it, so every warp access is 512
+    // contiguous bytes: [BN/32 column chunks][4 lane quarters][8 float4][32
+    // lanes].
     const int q = row_local >> 5, lane = row_local & 31;
-    float* run = p.ws + h * (kBM * BN) + q * (8 * 128) + lane * 4;
     constexpr int kChunkFloats = 4 * 8 * 128;  // one 32-column chunk of the half tile
-    // Adds the running sum (if any) to chunk c of this thread's accumulator
-    // row, then passes the chunk on: to the workspace, or (last part) to C.
-    auto chunk = [&](int c, const float4 (&prev)[8]) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c, r);
-        tmem_ld_wait();
-        if (un.split > 0) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                r[4 * v] = __float_as_uint(__fadd_rn(prev[v].x, __uint_as_float(r[4 * v])));
-                r[4 * v + 1] = __float_as_uint(__fadd_rn(prev[v].y, __uint_as_float(r[4 * v + 1])));
-                r[4 * v + 2] = __float_as_uint(__fadd_rn(prev[v].z, __uint_as_float(r[4 * v + 2])));
-                r[4 * v + 3] = __float_as_uint(__fadd_rn(prev[v].w, __uint_as_float(r[4 * v + 3])));
-            }
-        } else {
-            // the sum starts from a cleared (+0) accumulator
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fadd_rn(0.0f, __uint_as_float(r[i])));
-        }
-        if (last) {
-            out.put(p, tmC, row0, col0 + c, r);
-        } else {
-            float* rc = run + (c >> 5) * kChunkFloats;
+    auto part = [&](int s) -> float* {         // partial of part s >= 1, this thread
+        return p.ws + (h * (un.nsplit - 1) + (s - 1)) * (kBM * BN) + q * (8 * 128) + lane * 4;
+    };
+    if (un.split > 0) {
+        float* mine = part(un.split);
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c, r);
+            tmem_ld_wait();
+            if (c + 32 >= c_end) release();
+            float* rc = mine + (c >> 5) * kChunkFloats;
 #pragma unroll
             for (int v = 0; v < 8; ++v)
                 st_global_v4(rc + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
         }
-    };
-    auto fetch = [&](int c, float4 (&dst)[8]) {
-        if (un.split > 0 && c < c_end) {
-            const float* rc = run + (c >> 5) * kChunkFloats;
+        __threadfence();  // the partial is visible before it is counted
+        if (!epi_sync()) return false;
+        if (etid == 0) red_release_gpu_add(p.counters + h, 1);
+        return true;
+    }
+    if (etid == 0) *flag = wait_flag_bounded(p.counters + h, un.nsplit - 1, ctl) ? 1 : 0;
+    if (!epi_sync()) return false;
+    if (!*flag) return false;
+    __threadfence();
+    // Items (chunk, part s = 1..S-1) in order; two items' loads are in
+    // flight ahead of the one being added.
+    const int nparts = un.nsplit - 1;
+    const int nitems = ((c_end - c_begin) >> 5) * nparts;
+    auto fetch = [&](int i, float4 (&dst)[8]) {
+        if (i < nitems) {
+            const int c = c_begin + (i / nparts) * 32, s = i % nparts + 1;
+            const float* rc = part(s) + (c >> 5) * kChunkFloats;
 #pragma unroll
             for (int v = 0; v < 8; ++v) dst[v] = ld_global_cg_f4(rc + v * 128);
         }
     };
-    // Two chunks of the running sum are in flight ahead of the one being
-    // added, so the hand-over is bound by bandwidth rather than latency.
+    float acc[32];
+    auto consume = [&](int i, const float4 (&src)[8]) {
+        const int c = c_begin + (i / nparts) * 32, s = i % nparts + 1;
+        if (s == 1) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c, r);
+            tmem_ld_wait();
+            if (c + 32 >= c_end) release();
+            // the sum starts from a cleared (+0) accumulator
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(0.0f, __uint_as_float(r[j]));
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            acc[4 * v] = __fadd_rn(acc[4 * v], src[v].x);
+            acc[4 * v + 1] = __fadd_rn(acc[4 * v + 1], src[v].y);
+            acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], src[v].z);
+            acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], src[v].w);
+        }
+        if (s == nparts) {
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
+            out.put(p, tmC, row0, col0 + c, r);
+        }
+    };
     float4 pa[8], pb[8];
-    fetch(c_begin, pa);
-    fetch(c_begin + 32, pb);
+    fetch(0, pa);
+    fetch(1, pb);
 #pragma unroll 1
-    for (int c = c_begin; c < c_end; c += 64) {
-        chunk(c, pa);
-        fetch(c + 64, pa);
-        if (c + 32 < c_end) {
-            chunk(c + 32, pb);
-            fetch(c + 96, pb);
+    for (int i = 0; i < nitems; i += 2) {
+        consume(i, pa);
+        fetch(i + 2, pa);
+        if (i + 1 < nitems) {
+            consume(i + 1, pb);
+            fetch(i + 3, pb);
         }
     }
-    release();
-    if (!last) {
-        __threadfence();  // the running sum is visible before the counter moves
-        if (!epi_sync()) return false;
-        if (etid == 0) st_release_gpu(p.counters + h, un.split + 1);
-    } else if (etid == 0) {
-        p.counters[h] = 0;  // ready for the next launch
-    }
+    if (etid == 0) p.counters[h] = 0;  // ready for the next launch
     // no thread may still be reading `flag` when the next unit rewrites it
     return epi_sync();
 }

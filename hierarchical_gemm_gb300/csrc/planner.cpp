@@ -25,7 +25,7 @@ constexpr int64_t kEpiWarps = 8;  // epilogue warps, each staging two 32 x 32 ou
 constexpr double kMacsPerCycle = 4096.0;
 constexpr double kL2BytesPerCycle = 72.0;     // operand feed per SM (measured ballpark)
 constexpr double kHbmBytesPerCycle = 3500.0;  // whole GPU (model)
-constexpr double kReduceBytesPerCycle = 64.0; // split-K partial reads per SM (model)
+constexpr double kReduceBytesPerCycle = 32.0; // split-K partial reads per SM (measured ballpark)
 constexpr double kUnitOverhead = 600.0;       // pipeline fill / drain per unit (model)
 constexpr int kMaxSplits = 32;
 constexpr int kDefaultTimeoutMs = 1000;
@@ -69,10 +69,9 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int dout, int bm, int bn, int
                      split_rounds * (kb_split * per_kb + kUnitOverhead);
     double bytes = 2.0 * (M * K + K * N) + static_cast<double>(out_bytes(dout)) * M * N;
     if (splits > 1 && split_tiles > 0) {
-        // the parts of a split tile add up in order: S - 1 hand-overs of a
-        // running sum (one write and one read of an fp32 tile half each),
-        // one after another at the end of the tile
-        compute += (splits - 1) * 2.0 * kBM * bn * 4.0 / kReduceBytesPerCycle;
+        // parts 1..S-1 write an fp32 partial of their tile half; part 0
+        // reads the S - 1 partials and adds them
+        compute += splits * static_cast<double>(kBM) * bn * 4.0 / kReduceBytesPerCycle;
         const double ws = 2.0 * 4.0 * (splits - 1) * static_cast<double>(split_tiles) * bm * bn;
         bytes += ws;
     }
@@ -154,7 +153,8 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
             if (!f.block_n && bn > n_pad && bn != 64 && !(bm == 256 && bn == 128)) continue;
             const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
             const int smax = f.splits ? f.splits
-                                      : static_cast<int>(std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, kblocks / 4)));
+                                      : static_cast<int>(std::min<int64_t>(
+                                            std::min<int64_t>(kMaxSplits, slots), std::max<int64_t>(1, kblocks / 4)));
             const int smin = f.splits ? f.splits : 1;
             for (int s = smin; s <= smax; ++s) {
                 // which tiles are split: none (s = 1), a forced count, every
@@ -201,8 +201,11 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     int64_t slots = (f.grid ? f.grid : num_sms) / ctas_per_slot;
     if (slots < 1) return TSGEMM_ERR_UNSUPPORTED;
     c.grid = static_cast<int32_t>(std::min<int64_t>(c.units, slots) * ctas_per_slot);
-    // one fp32 running sum per split tile
-    c.workspace_bytes = c.split_tiles * best_bm * static_cast<int64_t>(best_bn) * 4;
+    // part 0 of a split tile waits for parts 1..S-1, which must run on other
+    // CTAs (pairs) at the same time: S may not exceed the grid's slots
+    if (c.split_tiles > 0 && best_s > c.grid / ctas_per_slot) return TSGEMM_ERR_UNSUPPORTED;
+    // S - 1 fp32 partials per split tile
+    c.workspace_bytes = c.split_tiles * (best_s - 1) * best_bm * static_cast<int64_t>(best_bn) * 4;
     c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
     c.debug_flags = f.debug_flags;
     *out = c;

@@ -159,6 +159,11 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
     asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// *p += v with release semantics at GPU scope.
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Wait until the global flag *p equals `value` (it is set by another CTA),
 // for at most ctl.timeout_ns; false when the limit expired or the CTA is
 // aborting.

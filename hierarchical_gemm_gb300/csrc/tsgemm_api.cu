@@ -168,6 +168,8 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
             return TSGEMM_ERR_UNSUPPORTED;
         }
         if (cfg.grid > 2 * clusters) cfg.grid = 2 * clusters;
+        // the parts of a split tile must still run side by side
+        if (cfg.split_tiles > 0 && cfg.splits > cfg.grid / 2) return TSGEMM_ERR_UNSUPPORTED;
     }
 
     // value-initialised; operator new honours the 64-byte alignment the

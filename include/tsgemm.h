@@ -91,8 +91,8 @@ typedef struct {
     int32_t group_m;      /* tile rows per raster group (L2 reuse) */
     int32_t grid;         /* CTAs launched (persistent) */
     int64_t units;        /* work units = whole tiles + split_tiles * splits */
-    int64_t workspace_bytes; /* split-K running sums owned by the plan:
-                                split_tiles * block_m * block_n * 4 bytes */
+    int64_t workspace_bytes; /* split-K partials owned by the plan:
+                                split_tiles * (splits - 1) * block_m * block_n * 4 bytes */
     int32_t timeout_ms;   /* limit of every device-side wait */
     int32_t debug_flags;  /* tests only: TSGEMM_DEBUG_* */
     int64_t split_tiles;  /* tiles split into `splits` K parts: the last ones of
@@ -116,7 +116,9 @@ TSGEMM_API tsgemm_status_t tsgemm_plan(tsgemm_plan_t* out, int64_t M, int64_t N,
 
 /* tsgemm_plan with some configuration fields forced (see tsgemm_config_t).
  * `force` may be NULL.  A forced value the kernel cannot run returns
- * TSGEMM_ERR_UNSUPPORTED. */
+ * TSGEMM_ERR_UNSUPPORTED; that includes a split factor larger than the number
+ * of CTAs (CTA pairs) of the grid, since the parts of a split tile must run
+ * side by side. */
 TSGEMM_API tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t K,
                                tsgemm_dtype_t dtype_in, tsgemm_dtype_t dtype_out,
                                tsgemm_layout_t layout, const tsgemm_config_t* force);
@@ -179,7 +181,7 @@ TSGEMM_API const char* tsgemm_status_string(tsgemm_status_t s);
  * on `stream` before the launch).
  *
  * Limits: at most TSGEMM_NOALLOC_MAX_TILES output tiles and at most
- * TSGEMM_NOALLOC_WS_BYTES of fp32 running sums (split tiles * 128 *
+ * TSGEMM_NOALLOC_WS_BYTES of fp32 partials (split tiles * (S - 1) * 128 *
  * block_n * 4 bytes); larger problems return TSGEMM_ERR_SCRATCH_LIMIT before
  * anything is enqueued.
  *

@@ -104,7 +104,7 @@ def test_planner_invariants(ts, shape, sms):
     assert 1 <= c["splits"] <= _ceil(K, 64)
     per = bm // 128  # CTAs per unit
     assert c["grid"] % per == 0 and 1 <= c["grid"] <= per * min(sms // per, c["units"])
-    assert c["workspace_bytes"] == st * bm * bn * 4
+    assert c["workspace_bytes"] == st * (c["splits"] - 1) * bm * bn * 4
     stage = 128 * 64 * 2 + (bn // per) * 64 * 2
     staging = 8 * 2 * 32 * 32 * (4 if dout == "f32" else 2)  # 8 epilogue warps x 2 blocks
     smem = 1024 + c["stages"] * stage + staging + 8 * (2 * c["stages"] + 6) + 16
@@ -138,6 +138,20 @@ def test_forced_fields_are_honoured(ts):
             c["timeout_ms"]) == (128, 128, 5, 3, 4, 7, 50)
     c = ts.choose_config(1000, 1000, 4096, "bf16", "bf16", 152, block_m=256, grid=7)
     assert c["block_m"] == 256 and c["grid"] == 6  # whole pairs only
+
+
+def test_split_factor_must_fit_the_grid(ts):
+    # the S parts of a split tile run side by side on S CTAs (pairs)
+    c = ts.choose_config(512, 512, 4096, "bf16", "f32", 152, block_m=128, splits=4, grid=4)
+    assert c["grid"] == 4
+    for force in [dict(block_m=128, splits=4, grid=3), dict(block_m=256, splits=3, grid=4)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(512, 512, 4096, "bf16", "f32", 152, **force)
+        assert e.value.status == ts.ERR_UNSUPPORTED
+    for sms in (2, 8, 152):
+        for shape in [(1024, 1024, 65536), (4096, 4096, 4096), (128, 256, 65536)]:
+            c = ts.choose_config(*shape, "bf16", "f32", sms)
+            assert c["splits"] <= c["grid"] // (c["block_m"] // 128)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

@@ -190,7 +190,7 @@ def test_layouts_random_real_inputs(layout, splits):
     _check(C, A, B, "bf16", "bf16", exact=False)
 
 
-@pytest.mark.parametrize("block_m,grid", [(128, 1), (128, 3), (256, 2), (256, 6)])
+@pytest.mark.parametrize("block_m,grid", [(128, 2), (128, 3), (256, 4), (256, 6)])
 def test_persistent_loop_with_small_grid(block_m, grid):
     # Few CTAs walk many units: exercises ring-phase and accumulator-phase
     # wrap-around over many tiles.
