@@ -22,10 +22,12 @@ import numpy as np
 
 from . import build as _build
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
 _NAMES = {"f16": F16, "fp16": F16, "float16": F16,
           "bf16": BF16, "bfloat16": BF16,
-          "f32": F32, "fp32": F32, "float32": F32}
+          "f32": F32, "fp32": F32, "float32": F32,
+          "e4m3": E4M3, "float8_e4m3fn": E4M3, "e5m2": E5M2, "float8_e5m2": E5M2}
+_EIGHT_BIT = (E4M3, E5M2)
 
 _lib = None
 
@@ -55,6 +57,13 @@ def lib():
         L.oracle_gemm_sampled.argtypes = [i64, i64, i64, vp, vp, i32, i64, vp,
                                           vp, vp, vp]
         L.oracle_default_threads.restype = i32
+        L.oracle_decode8.restype = ctypes.c_double
+        L.oracle_decode8.argtypes = [ctypes.c_uint8, i32]
+        L.oracle_decode8_n.argtypes = [vp, i64, i32, vp]
+        L.oracle_gemm8.restype = i32
+        L.oracle_gemm8.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32]
+        L.oracle_gemm8_sampled.argtypes = [i64, i64, i64, vp, vp, i32, i64, vp,
+                                           vp, vp, vp]
         _lib = L
     return _lib
 
@@ -69,10 +78,17 @@ def default_threads():
 
 
 def decode(bits, dtype):
-    """Exact float64 values of an array of 16-bit float bit patterns."""
+    """Exact float64 values of an array of 16-bit (or, for E4M3/E5M2, 8-bit)
+    float bit patterns."""
+    code = dtype_code(dtype)
+    if code in _EIGHT_BIT:
+        bits, p = _c(bits, np.uint8)
+        out = np.empty(bits.shape, dtype=np.float64)
+        lib().oracle_decode8_n(p, bits.size, code, out.ctypes.data)
+        return out
     bits, p = _c(bits, np.uint16)
     out = np.empty(bits.shape, dtype=np.float64)
-    lib().oracle_decode_n(p, bits.size, dtype_code(dtype), out.ctypes.data)
+    lib().oracle_decode_n(p, bits.size, code, out.ctypes.data)
     return out
 
 
@@ -95,18 +111,21 @@ def round_out(x, dtype_out):
 def gemm(A_bits, B_bits, dtype_in, nthreads=0):
     """ref = A*B and sabs = |A|*|B| (elementwise products), both float64.
 
-    A_bits: (M, K) uint16, B_bits: (K, N) uint16, both row-major.
+    A_bits: (M, K), B_bits: (K, N), both row-major bit patterns: uint16 for
+    fp16/bf16, uint8 for the FP8 formats E4M3/E5M2.
     Returns (ref, sabs, threads_used).
     """
-    A_bits, pa = _c(A_bits, np.uint16)
-    B_bits, pb = _c(B_bits, np.uint16)
+    code = dtype_code(dtype_in)
+    eight = code in _EIGHT_BIT
+    A_bits, pa = _c(A_bits, np.uint8 if eight else np.uint16)
+    B_bits, pb = _c(B_bits, np.uint8 if eight else np.uint16)
     M, K = A_bits.shape
     K2, N = B_bits.shape
     assert K == K2, "inner dimensions differ"
     ref = np.empty((M, N), dtype=np.float64)
     sabs = np.empty((M, N), dtype=np.float64)
-    used = lib().oracle_gemm(M, N, K, pa, pb, dtype_code(dtype_in),
-                             ref.ctypes.data, sabs.ctypes.data, int(nthreads))
+    fn = lib().oracle_gemm8 if eight else lib().oracle_gemm
+    used = fn(M, N, K, pa, pb, code, ref.ctypes.data, sabs.ctypes.data, int(nthreads))
     if used < 0:
         raise MemoryError("oracle_gemm could not allocate its decoded B")
     return ref, sabs, used
@@ -114,8 +133,10 @@ def gemm(A_bits, B_bits, dtype_in, nthreads=0):
 
 def gemm_sampled(A_bits, B_bits, dtype_in, rows, cols):
     """ref and sabs at the positions (rows[s], cols[s]) only."""
-    A_bits, pa = _c(A_bits, np.uint16)
-    B_bits, pb = _c(B_bits, np.uint16)
+    code = dtype_code(dtype_in)
+    eight = code in _EIGHT_BIT
+    A_bits, pa = _c(A_bits, np.uint8 if eight else np.uint16)
+    B_bits, pb = _c(B_bits, np.uint8 if eight else np.uint16)
     M, K = A_bits.shape
     K2, N = B_bits.shape
     assert K == K2, "inner dimensions differ"
@@ -126,8 +147,8 @@ def gemm_sampled(A_bits, B_bits, dtype_in, rows, cols):
     assert cols.size == 0 or (cols.min() >= 0 and cols.max() < N)
     ref = np.empty(rows.shape, dtype=np.float64)
     sabs = np.empty(rows.shape, dtype=np.float64)
-    lib().oracle_gemm_sampled(M, N, K, pa, pb, dtype_code(dtype_in), rows.size,
-                              pr, pc, ref.ctypes.data, sabs.ctypes.data)
+    fn = lib().oracle_gemm8_sampled if eight else lib().oracle_gemm_sampled
+    fn(M, N, K, pa, pb, code, rows.size, pr, pc, ref.ctypes.data, sabs.ctypes.data)
     return ref, sabs
 
 

@@ -17,10 +17,10 @@
  * with A (M x K) and B (K x N) row-major, which the TileScale README (section
  * "Example of GEMM") also uses.  This file writes that definition out with no
  * tiling, fusion or reordering: for every (i, j) the K products are added in
- * the order k = 0, 1, ..., K-1 in double precision.  Inputs are 16-bit floats;
- * the product of two of them has at most 22 significant bits, so every product
- * is exact in double and only the additions round (relative error of the sum
- * <= K * 2^-53, far below any tolerance used against it).
+ * the order k = 0, 1, ..., K-1 in double precision.  Inputs are 16-bit or
+ * 8-bit floats; the product of two of them has at most 22 significant bits, so
+ * every product is exact in double and only the additions round (relative
+ * error of the sum <= K * 2^-53, far below any tolerance used against it).
  *
  * It also returns sabs[i][j] = sum_k |A[i][k] * B[k][j]|, the scale that the
  * acceptance rule |C - ref| <= 1e-3 * sabs + 1e-5 is measured against.
@@ -28,6 +28,11 @@
  * Number formats are decoded from their IEEE-style definitions:
  *   binary16 : 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits
  *   bfloat16 : 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits
+ *   FP8 E4M3 : 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; no
+ *              infinities, S.1111.111 is NaN, largest finite 448 (OCP 8-bit
+ *              floating point specification)
+ *   FP8 E5M2 : 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits, with
+ *              IEEE infinities and NaNs (same specification)
  * and the output rounding (fp32 accumulator to a 16-bit output) is
  * round-to-nearest, ties-to-even, written out from the same definitions.
  *
@@ -43,6 +48,8 @@
 #define ORACLE_F16 0
 #define ORACLE_BF16 1
 #define ORACLE_F32 2
+#define ORACLE_E4M3 3
+#define ORACLE_E5M2 4
 
 /* Field widths of the two 16-bit formats. */
 static int frac_bits(int dtype) { return dtype == ORACLE_F16 ? 10 : 7; }
@@ -66,6 +73,34 @@ double oracle_decode(uint16_t bits, int dtype) {
         v = ldexp((double)((1 << fb) + f), e - bias - fb);
     }
     return sign ? -v : v;
+}
+
+/* Exact value of an 8-bit float given by its bit pattern. */
+double oracle_decode8(uint8_t bits, int dtype) {
+    const int sign = (bits >> 7) & 1;
+    double v;
+    if (dtype == ORACLE_E4M3) {
+        const int e = (bits >> 3) & 15, f = bits & 7;
+        if (e == 15 && f == 7)
+            v = NAN;
+        else if (e == 0)
+            v = ldexp((double)f, 1 - 7 - 3);       /* subnormal: f * 2^-9 */
+        else
+            v = ldexp((double)(8 + f), e - 7 - 3); /* (1 + f/8) * 2^(e - 7) */
+    } else {
+        const int e = (bits >> 2) & 31, f = bits & 3;
+        if (e == 31)
+            v = f ? NAN : INFINITY;
+        else if (e == 0)
+            v = ldexp((double)f, 1 - 15 - 2);       /* subnormal: f * 2^-16 */
+        else
+            v = ldexp((double)(4 + f), e - 15 - 2); /* (1 + f/4) * 2^(e - 15) */
+    }
+    return sign ? -v : v;
+}
+
+void oracle_decode8_n(const uint8_t* bits, int64_t n, int dtype, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_decode8(bits[i], dtype);
 }
 
 /* Round a double to the nearest 16-bit float, ties to even; returns the bits.
@@ -123,13 +158,19 @@ void oracle_round32_n(const double* x, int64_t n, float* out) {
 
 typedef struct {
     int64_t M, N, K;
-    const uint16_t* A;
+    const void* A;    /* 16-bit (elem 2) or 8-bit (elem 1) values, M x K row-major */
+    int elem;
     const double* Bd; /* B decoded to double, K x N row-major */
     int dtype_in;
     double* ref;
     double* sabs;
     int64_t row_begin, row_end;
 } gemm_job_t;
+
+static double decode_a(const gemm_job_t* j, int64_t idx) {
+    return j->elem == 1 ? oracle_decode8(((const uint8_t*)j->A)[idx], j->dtype_in)
+                        : oracle_decode(((const uint16_t*)j->A)[idx], j->dtype_in);
+}
 
 /* Rows [row_begin, row_end) of ref and sabs.  For each row i the products
  * A[i][k] * B[k][j] are added into ref[i][j] for k = 0..K-1 in order, so each
@@ -142,7 +183,7 @@ static void* gemm_rows(void* p) {
         double* s = j->sabs + i * N;
         for (int64_t c = 0; c < N; ++c) { r[c] = 0.0; s[c] = 0.0; }
         for (int64_t k = 0; k < K; ++k) {
-            const double a = oracle_decode(j->A[i * K + k], j->dtype_in);
+            const double a = decode_a(j, i * K + k);
             const double* b = j->Bd + k * N;
             for (int64_t c = 0; c < N; ++c) {
                 const double p_ = a * b[c]; /* exact */
@@ -159,21 +200,21 @@ int oracle_default_threads(void) {
     return n > 0 ? (int)n : 1;
 }
 
-/* ref, sabs: M x N row-major outputs.  nthreads <= 0 means one per online
- * core.  Returns the number of threads used, or -1 on allocation failure. */
-int oracle_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A,
-                const uint16_t* B, int dtype_in, double* ref, double* sabs,
-                int nthreads) {
+static int gemm_any(int64_t M, int64_t N, int64_t K, const void* A, const void* B, int elem,
+                    int dtype_in, double* ref, double* sabs, int nthreads) {
     if (nthreads <= 0) nthreads = oracle_default_threads();
     if (nthreads > M) nthreads = (int)(M > 0 ? M : 1);
     double* Bd = (double*)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
     if (!Bd) return -1;
-    oracle_decode_n(B, K * N, dtype_in, Bd);
+    if (elem == 1)
+        oracle_decode8_n((const uint8_t*)B, K * N, dtype_in, Bd);
+    else
+        oracle_decode_n((const uint16_t*)B, K * N, dtype_in, Bd);
     gemm_job_t* jobs = (gemm_job_t*)calloc((size_t)nthreads, sizeof(gemm_job_t));
     pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
     if (!jobs || !th) { free(Bd); free(jobs); free(th); return -1; }
     for (int t = 0; t < nthreads; ++t) {
-        jobs[t] = (gemm_job_t){M, N, K, A, Bd, dtype_in, ref, sabs,
+        jobs[t] = (gemm_job_t){M, N, K, A, elem, Bd, dtype_in, ref, sabs,
                                M * t / nthreads, M * (t + 1) / nthreads};
     }
     int started = 0;
@@ -191,6 +232,22 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A,
     return nthreads;
 }
 
+/* ref, sabs: M x N row-major outputs of A (M x K) times B (K x N), both of
+ * 16-bit floats.  nthreads <= 0 means one per online core.  Returns the
+ * number of threads used, or -1 on allocation failure. */
+int oracle_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* A,
+                const uint16_t* B, int dtype_in, double* ref, double* sabs,
+                int nthreads) {
+    return gemm_any(M, N, K, A, B, 2, dtype_in, ref, sabs, nthreads);
+}
+
+/* The same for 8-bit float inputs (FP8 E4M3 or E5M2). */
+int oracle_gemm8(int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                 const uint8_t* B, int dtype_in, double* ref, double* sabs,
+                 int nthreads) {
+    return gemm_any(M, N, K, A, B, 1, dtype_in, ref, sabs, nthreads);
+}
+
 /* The same definition evaluated only at `count` output positions
  * (rows[s], cols[s]); used where the full product would take too long. */
 void oracle_gemm_sampled(int64_t M, int64_t N, int64_t K, const uint16_t* A,
@@ -204,6 +261,25 @@ void oracle_gemm_sampled(int64_t M, int64_t N, int64_t K, const uint16_t* A,
         for (int64_t k = 0; k < K; ++k) {
             const double p_ = oracle_decode(A[i * K + k], dtype_in) *
                               oracle_decode(B[k * N + c], dtype_in);
+            r += p_;
+            a_ += fabs(p_);
+        }
+        ref[s] = r;
+        sabs[s] = a_;
+    }
+}
+
+void oracle_gemm8_sampled(int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                          const uint8_t* B, int dtype_in, int64_t count,
+                          const int64_t* rows, const int64_t* cols, double* ref,
+                          double* sabs) {
+    (void)M;
+    for (int64_t s = 0; s < count; ++s) {
+        const int64_t i = rows[s], c = cols[s];
+        double r = 0.0, a_ = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double p_ = oracle_decode8(A[i * K + k], dtype_in) *
+                              oracle_decode8(B[k * N + c], dtype_in);
             r += p_;
             a_ += fabs(p_);
         }

@@ -2,7 +2,7 @@
 checks.
 
 This module holds no GEMM arithmetic: it only draws numbers and quantises
-them to the 16-bit input formats.  Both the CUDA path and the oracle are fed
+them to the input formats (fp16, bf16, FP8 E4M3 / E5M2).  Both the CUDA path and the oracle are fed
 the same host bytes produced here.
 
 Generator.  Each matrix has its own 64-bit seed.  Element e (row-major index)
@@ -27,7 +27,8 @@ Distributions:
 Quantisation to the input format: fp16 by numpy's float64 -> float16
 conversion (round to nearest, ties to even); bf16 by float64 -> float32
 (ties to even) and then float32 -> bf16 keeping the upper 16 bits with ties
-to even.  Integers in [-2, 2] and all the values the workloads use are
+to even; FP8 E4M3 / E5M2 by float64 -> float32 -> torch's float8
+conversion (ties to even).  Integers in [-2, 2] and all the values the workloads use are
 representable, so the second rounding only shapes random real inputs.
 """
 import numpy as np
@@ -66,12 +67,28 @@ def bf16_bits(x):
     return ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
 
 
+def fp8_bits(x, dtype):
+    """float64 -> FP8 E4M3 / E5M2 bits via float32 (each step ties to even;
+    values must be within the format's finite range)."""
+    import torch
+    t = torch.from_numpy(np.asarray(x, dtype=np.float64).astype(np.float32))
+    tdt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+    return t.to(tdt).view(torch.uint8).numpy().copy()
+
+
 def quantise(x, dtype):
     if dtype in ("f16", "fp16", "float16"):
         return f16_bits(x)
     if dtype in ("bf16", "bfloat16"):
         return bf16_bits(x)
-    raise ValueError("input dtype must be f16 or bf16, got %r" % (dtype,))
+    if dtype in ("e4m3", "e5m2"):
+        return fp8_bits(x, dtype)
+    raise ValueError("input dtype must be f16, bf16, e4m3 or e5m2, got %r" % (dtype,))
+
+
+def elem_dtype(dtype):
+    """numpy storage type of the input format's bit patterns."""
+    return np.uint8 if dtype in ("e4m3", "e5m2") else np.uint16
 
 
 def _draw(dist, seed, start, count):
@@ -91,15 +108,16 @@ def _draw(dist, seed, start, count):
 
 
 def matrix(rows, cols, dist, seed, dtype, out=None):
-    """A rows x cols row-major matrix of 16-bit input bits (numpy uint16).
+    """A rows x cols row-major matrix of input bits (numpy uint16 for
+    fp16/bf16, uint8 for e4m3/e5m2).
 
     dist is ("uniform", lo, hi), ("normal", sigma) or ("int", lo, hi).
-    `out` may be a preallocated (rows, cols) uint16 array (for example a
-    pinned host buffer viewed through numpy).
+    `out` may be a preallocated (rows, cols) array of that storage type (for
+    example a pinned host buffer viewed through numpy).
     """
     n = rows * cols
     if out is None:
-        out = np.empty((rows, cols), dtype=np.uint16)
+        out = np.empty((rows, cols), dtype=elem_dtype(dtype))
     flat = out.reshape(-1)
     for s in range(0, n, _CHUNK):
         c = min(_CHUNK, n - s)

@@ -391,3 +391,96 @@ def test_accept_admits_the_correctly_rounded_16_bit_output():
         off[0] = off[0] + (2 if dt == BF16 else 8)
         ok, info = oracle.accept(off, ref, sabs, dt)
         assert not ok and info["mismatches"] == 1
+
+
+# ------------------------------------------------------------ FP8 formats --
+
+from oracle import E4M3, E5M2  # noqa: E402
+
+GOLDEN8 = os.path.join(os.path.dirname(__file__), "golden", "float8_formats.txt")
+
+
+def test_decode_fp8_golden_table():
+    n = 0
+    with open(GOLDEN8) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            fmt, hexbits, val = line.split()
+            got = oracle.lib().oracle_decode8(int(hexbits, 16), E4M3 if fmt == "e4m3" else E5M2)
+            if val == "nan":
+                assert np.isnan(got), line
+            else:
+                want = float(val) if val in ("inf", "-inf") else float.fromhex(val)
+                assert got == want and np.signbit(got) == np.signbit(want), line
+            n += 1
+    assert n >= 24
+
+
+@pytest.mark.parametrize("code,tdt", [(E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)])
+def test_decode_fp8_all_patterns_match_torch(code, tdt):
+    bits = np.arange(256, dtype=np.uint8)
+    got = oracle.decode(bits, code)
+    want = torch.from_numpy(bits.copy()).view(tdt).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def _fp8(x, code):
+    t = torch.tensor(np.asarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn if code == E4M3 else torch.float8_e5m2).view(torch.uint8).numpy().copy()
+
+
+@pytest.mark.parametrize("code", [E4M3, E5M2])
+def test_fp8_gemm_pins(code):
+    r = _rng(90)
+    n = 48
+    eye = _fp8(np.eye(n), code)
+    B = _fp8(r.integers(-6, 7, (n, 20)), code)
+    ref, sabs, _ = oracle.gemm(eye, B, code)
+    assert np.array_equal(ref, oracle.decode(B, code))
+    perm = r.permutation(n)
+    P = np.zeros((n, n))
+    P[np.arange(n), perm] = 1.0
+    A = _fp8(r.integers(-6, 7, (15, n)), code)
+    ref, _, _ = oracle.gemm(A, _fp8(P, code), code)
+    want = np.empty_like(ref)
+    want[:, perm] = oracle.decode(A, code)
+    assert np.array_equal(ref, want)
+    u, v = r.integers(-3, 4, 9), r.integers(-3, 4, 11)
+    p_, q_ = r.integers(-2, 3, 200), r.integers(-2, 3, 200)
+    ref, sabs, _ = oracle.gemm(_fp8(np.outer(u, p_), code), _fp8(np.outer(q_, v), code), code)
+    assert np.array_equal(ref, np.dot(p_, q_) * np.outer(u, v).astype(np.float64))
+    ones, _, _ = oracle.gemm(_fp8(np.ones((3, 77)), code), _fp8(np.ones((77, 5)), code), code)
+    assert np.all(ones == 77)
+
+
+@pytest.mark.parametrize("code", [E4M3, E5M2])
+def test_fp8_gemm_against_torch_float64(code):
+    r = _rng(91)
+    A = _fp8(r.uniform(-3, 3, (40, 96)), code)
+    B = _fp8(r.uniform(-3, 3, (96, 56)), code)
+    Ad = torch.from_numpy(oracle.decode(A, code))
+    Bd = torch.from_numpy(oracle.decode(B, code))
+    ref, sabs, _ = oracle.gemm(A, B, code)
+    want = (Ad @ Bd).numpy()
+    wabs = (Ad.abs() @ Bd.abs()).numpy()
+    assert np.all(np.abs(ref - want) <= 1e-12 * wabs + 1e-300)
+    rows, cols = r.integers(0, 40, 50), r.integers(0, 56, 50)
+    sr, ss = oracle.gemm_sampled(A, B, code, rows, cols)
+    assert np.array_equal(sr, ref[rows, cols]) and np.array_equal(ss, sabs[rows, cols])
+
+
+def test_fp8_brute_force_exact_arithmetic():
+    r = _rng(92)
+    for code in (E4M3, E5M2):
+        A = _fp8(r.uniform(-8, 8, (3, 7)), code)
+        B = _fp8(r.uniform(-8, 8, (7, 4)), code)
+        Ad, Bd = oracle.decode(A, code), oracle.decode(B, code)
+        ref, _, _ = oracle.gemm(A, B, code)
+        for i in range(3):
+            for j in range(4):
+                ex = sum(Fraction(Ad[i, k]) * Fraction(Bd[k, j]) for k in range(7))
+                assert Fraction(ref[i, j]) == ex  # few terms: exact in double
