@@ -1,7 +1,9 @@
 // gemm_sm103.cuh -- the persistent, warp-specialised tcgen05 GEMM kernel.
 //
-// C = A * B, A (M x K) and B (K x N) row-major 16-bit floats, fp32
-// accumulation in tensor memory, C (M x N) row-major fp16/bf16/fp32.
+// C = A * B, A (M x K) and B (K x N) 16-bit floats in any of the four
+// row/column-major layouts, or 8-bit floats (E4M3 / E5M2) with both operands
+// K-major; fp32 accumulation in tensor memory, C (M x N) row-major
+// fp16/bf16/fp32.
 //
 // This is the tile-level GEMM of the TileLang skeleton ("TileScale 与
 // TileLang比较", section 核心抽象与编程模型对比): per output tile, clear an
@@ -15,7 +17,8 @@
 //     memory, double buffered so the epilogue of one tile overlaps the
 //     main loop of the next;
 //   * T.gemm                                        -> tcgen05.mma kind::f16
-//     issued by a single thread, BK / 16 instructions per slice;
+//     (kind::f8f6f4 for 8-bit inputs) issued by a single thread, four
+//     instructions per 128-byte slice;
 //   * T.copy(C_r, C)                                -> tcgen05.ld by an
 //     epilogue warpgroup, fp32 -> output conversion, global stores;
 //   * warp(group) specialisation by rank (TileScale README, T.Scale
@@ -49,6 +52,12 @@ constexpr int kMaxStages = 16;
 
 enum OutKind { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2 };
 
+// K-elements per ring slice: one 128-byte swizzle row of the operand, 64
+// 16-bit or 128 8-bit elements.  The shared-memory tiles have the same
+// bytes either way; only the MMA kind and the TMA K coordinate differ.
+template <bool kF8>
+__host__ __device__ constexpr int slice_k() { return kF8 ? 128 : kBK; }
+
 // Operand layouts (the tsgemm_layout_t values): bit 1 set = A stored K x M
 // (column-major A, M contiguous); bit 0 set = B stored N x K (column-major
 // B, K contiguous -- the transpose_B form).  C is always M x N row-major.
@@ -69,7 +78,7 @@ struct GemmParams {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n;
     int32_t splits;       // S: K parts of each split tile
-    int32_t kblocks;      // ceil(K / kBK)
+    int32_t kblocks;      // ceil(K / K-elements per slice)
     int32_t group_m;      // raster group height in tiles
     int32_t stages;
     int32_t debug_flags;
@@ -319,42 +328,52 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
 // a_dst, B columns [col, col + kBCols) at b_dst, in the layout's operand
 // order.  kRemote: the completion goes to a barrier of the peer CTA (the
 // pair's leader), which needs the cta_group::2 form of the copy.
-template <int kLayout, int kBCols, bool kRemote>
+template <int kLayout, int kBCols, bool kRemote, bool kF8 = false>
 __device__ __forceinline__ void load_slice(uint32_t a_dst, uint32_t b_dst, const CUtensorMap* tmA,
                                            const CUtensorMap* tmB, uint32_t bar, int kb, int32_t row,
                                            int32_t col) {
+    static_assert(!kF8 || (a_kmajor(kLayout) && b_kmajor(kLayout)), "8-bit operands are K-major");
     auto ld = [&](uint32_t dst, const CUtensorMap* m, int32_t c0, int32_t c1) {
         if constexpr (kRemote)
             tma_load_2d_pair(dst, m, bar, c0, c1);
         else
             tma_load_2d(dst, m, bar, c0, c1);
     };
+    constexpr int kSK = slice_k<kF8>();
     if constexpr (a_kmajor(kLayout)) {
-        ld(a_dst, tmA, kb * kBK, row);  // one 64 (K) x 128 (M) box
+        ld(a_dst, tmA, kb * kSK, row);  // one 128-byte (K) x 128 (M) box
     } else {
         ld(a_dst, tmA, row, kb * kBK);  // two 64 (M) x 64 (K) boxes
         ld(a_dst + 8192u, tmA, row + 64, kb * kBK);
     }
     if constexpr (b_kmajor(kLayout)) {
-        ld(b_dst, tmB, kb * kBK, col);  // one 64 (K) x kBCols (N) box
+        ld(b_dst, tmB, kb * kSK, col);  // one 128-byte (K) x kBCols (N) box
     } else {
 #pragma unroll
         for (int j = 0; j < kBCols / 64; ++j) ld(b_dst + j * 8192u, tmB, col + j * 64, kb * kBK);
     }
 }
 
-// The four 16-deep MMAs of one K-slice held at a_addr / b_addr.
-template <int kLayout, int kCtaGroup>
+// The four MMAs of one K-slice held at a_addr / b_addr: 16-deep kind::f16
+// steps, or 32-deep kind::f8f6f4 steps for 8-bit operands (32 bytes of a
+// K-major row either way, so the descriptor steps are the same).
+template <int kLayout, int kCtaGroup, bool kF8 = false>
 __device__ __forceinline__ void mma_slice(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc,
                                           uint32_t accumulate) {
     constexpr bool ak = a_kmajor(kLayout), bk = b_kmajor(kLayout);
     const uint64_t ad = smem_desc_sw128(a_addr, op_lbo(ak), 1024u);
     const uint64_t bd = smem_desc_sw128(b_addr, op_lbo(bk), 1024u);
     constexpr uint64_t as = op_kstep(ak), bs = op_kstep(bk);
-    umma_f16<kCtaGroup>(d_tmem, ad, bd, idesc, accumulate);
-    umma_f16<kCtaGroup>(d_tmem, ad + as, bd + bs, idesc, 1u);
-    umma_f16<kCtaGroup>(d_tmem, ad + 2 * as, bd + 2 * bs, idesc, 1u);
-    umma_f16<kCtaGroup>(d_tmem, ad + 3 * as, bd + 3 * bs, idesc, 1u);
+    auto mma = [&](uint64_t a, uint64_t b, uint32_t acc) {
+        if constexpr (kF8)
+            umma_f8<kCtaGroup>(d_tmem, a, b, idesc, acc);
+        else
+            umma_f16<kCtaGroup>(d_tmem, a, b, idesc, acc);
+    };
+    mma(ad, bd, accumulate);
+    mma(ad + as, bd + bs, 1u);
+    mma(ad + 2 * as, bd + 2 * bs, 1u);
+    mma(ad + 3 * as, bd + 3 * bs, 1u);
 }
 
 template <int BN>
@@ -376,7 +395,7 @@ __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
            8u * (2 * stages + 6) /* barriers */ + 16u /* tmem holder, flags */;
 }
 
-template <int BN, int kOut, int kLayout>
+template <int BN, int kOut, int kLayout, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_sm103_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -449,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const uint32_t a_dst = base + stage * TS::kStageBytes;
                         mbar_arrive_expect_tx(full_bar(stage), TS::kStageBytes);
-                        load_slice<kLayout, BN, false>(a_dst, a_dst + TS::kABytes, &tmA, &tmB, full_bar(stage), kb,
+                        load_slice<kLayout, BN, false, kF8>(a_dst, a_dst + TS::kABytes, &tmA, &tmB, full_bar(stage), kb,
                                                        un.tm * kBM, un.tn * BN);
                         outstanding |= 1u << stage;
                         out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
@@ -486,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // (TMA-written operands are visible to the MMA once the
                     // full barrier completes; no tcgen05 fence is needed.)
                     const uint32_t a_addr = base + stage * TS::kStageBytes;
-                    mma_slice<kLayout, 1>(d_tmem, a_addr, a_addr + TS::kABytes, p.idesc, kb > un.kb0 ? 1u : 0u);
+                    mma_slice<kLayout, 1, kF8>(d_tmem, a_addr, a_addr + TS::kABytes, p.idesc, kb > un.kb0 ? 1u : 0u);
                     umma_commit(empty_bar(stage));  // slot free once these MMAs have read it
                     if (++stage == S) {
                         stage = 0;

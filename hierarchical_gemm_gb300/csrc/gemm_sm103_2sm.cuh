@@ -42,7 +42,7 @@ __host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
     return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 6) + 16u;
 }
 
-template <int BN, int kOut, int kLayout>
+template <int BN, int kOut, int kLayout, bool kF8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_sm103_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -127,10 +127,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int32_t bcol = un.tn * BN + static_cast<int32_t>(rank) * PS::kBCols;
                         if (leader) {
                             mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
-                            load_slice<kLayout, PS::kBCols, false>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                            load_slice<kLayout, PS::kBCols, false, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
                                                                    full_bar(stage), kb, arow, bcol);
                         } else {
-                            load_slice<kLayout, PS::kBCols, true>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                            load_slice<kLayout, PS::kBCols, true, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
                                                                   mapa_shared(full_bar(stage), 0u), kb, arow, bcol);
                         }
                         outstanding |= 1u << stage;
@@ -171,7 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // full barrier completes; no tcgen05 fence is needed.)
                     {
                         const uint32_t a_addr = base + stage * PS::kStageBytes;
-                        mma_slice<kLayout, 2>(d_tmem, a_addr, a_addr + PS::kABytes, p.idesc,
+                        mma_slice<kLayout, 2, kF8>(d_tmem, a_addr, a_addr + PS::kABytes, p.idesc,
                                               kb > un.kb0 ? 1u : 0u);
                         umma_commit_pair(empty_bar(stage), 0x3);  // slot free in both CTAs
                     }

@@ -6,16 +6,16 @@
 namespace tsg {
 
 // Kernel entry for a tile width (64/128/192/256), output kind (0 fp16,
-// 1 bf16, 2 fp32) and operand layout (tsgemm_layout_t); null for an
-// unsupported combination.
-const void* kernel_1sm(int block_n, int out_kind, int layout);
+// 1 bf16, 2 fp32), operand layout (tsgemm_layout_t) and input width (in8:
+// 8-bit float inputs, RCR layout only); null for an unsupported combination.
+const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8);
 
 // Dynamic shared memory the kernel above uses with `stages` ring slots.
 int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages);
 
 // The CTA-pair kernel (256 x block_n tiles, block_n 128 or 256), launched
 // with 2 x 1 clusters; null for an unsupported combination.
-const void* kernel_2sm(int block_n, int out_kind, int layout);
+const void* kernel_2sm(int block_n, int out_kind, int layout, bool in8);
 
 // Dynamic shared memory per CTA of the pair kernel with `stages` slots.
 int64_t kernel_2sm_smem_bytes(int block_n, int out_kind, int stages);
@@ -29,5 +29,7 @@ const void* kernel_2sm_layout0(int block_n, int out_kind);
 const void* kernel_2sm_layout1(int block_n, int out_kind);
 const void* kernel_2sm_layout2(int block_n, int out_kind);
 const void* kernel_2sm_layout3(int block_n, int out_kind);
+const void* kernel_1sm_f8(int block_n, int out_kind);
+const void* kernel_2sm_f8(int block_n, int out_kind);
 
 }  // namespace tsg

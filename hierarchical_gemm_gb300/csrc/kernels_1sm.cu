@@ -8,7 +8,8 @@
 
 namespace tsg {
 
-const void* kernel_1sm(int block_n, int out_kind, int layout) {
+const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8) {
+    if (in8) return layout == 1 ? kernel_1sm_f8(block_n, out_kind) : nullptr;
     switch (layout) {
         case 0: return kernel_1sm_layout0(block_n, out_kind);
         case 1: return kernel_1sm_layout1(block_n, out_kind);

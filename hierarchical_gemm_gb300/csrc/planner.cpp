@@ -2,8 +2,10 @@
 // K split, pipeline depth and grid for the persistent kernel.
 //
 // The choice minimises a simple per-SM time model, in SM clock cycles:
-//   * a K-slice (BK = 64) of a 128 x BN tile costs max(MMA, operand load):
-//     MMA   = 128 * BN * 64 / 4096 cycles (4096 bf16 MACs per SM per cycle),
+//   * a K-slice (128 bytes of K: 64 16-bit or 128 8-bit elements) of a
+//     128 x BN tile costs max(MMA, operand load):
+//     MMA   = 128 * BN * 64 / 4096 cycles (4096 bf16 MACs per SM per cycle,
+//             twice as many 8-bit MACs, so the same cycles per slice),
 //     load  = (A slice + B slice bytes) / kL2BytesPerCycle;
 //   * a CTA runs ceil(units / grid) units back to back (wave quantisation);
 //   * a split tile adds S - 1 hand-overs of an fp32 running sum;
@@ -16,6 +18,12 @@
 #include <cmath>
 
 namespace tsg {
+
+bool is_8bit(int dtype) { return dtype == TSGEMM_E4M3 || dtype == TSGEMM_E5M2; }
+
+int64_t in_bytes(int dtype_in) { return is_8bit(dtype_in) ? 1 : 2; }
+
+int slice_k(int dtype_in) { return is_8bit(dtype_in) ? 128 : 64; }
 
 namespace {
 
@@ -33,6 +41,8 @@ constexpr int kDefaultTimeoutMs = 1000;
 bool dtype_pair_ok(int din, int dout) {
     if (din == TSGEMM_F16) return dout == TSGEMM_F16 || dout == TSGEMM_F32;
     if (din == TSGEMM_BF16) return dout == TSGEMM_BF16 || dout == TSGEMM_F32;
+    if (din == TSGEMM_E4M3 || din == TSGEMM_E5M2)
+        return dout == TSGEMM_F16 || dout == TSGEMM_BF16 || dout == TSGEMM_F32;
     return false;
 }
 
@@ -49,14 +59,14 @@ struct Estimate {
 // tile, each SM computing 128 rows and loading half of the B slice.  The
 // last `split_tiles` tiles of the schedule are split into `splits` K parts
 // (all of them, or only the tail wave's, or none).
-Estimate estimate(int64_t M, int64_t N, int64_t K, int dout, int bm, int bn, int splits,
+Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int splits,
                   int64_t split_tiles, int num_sms) {
     const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
     const int64_t full = tiles - split_tiles;
     const int64_t units = full + split_tiles * splits;
     const int64_t slots = bm == 256 ? std::max(1, num_sms / 2) : num_sms;
     const int64_t grid = std::min<int64_t>(units, slots);
-    const int64_t kblocks = ceil_div(K, kBK);
+    const int64_t kblocks = ceil_div(K, slice_k(din));
     const double kb_split = std::ceil(static_cast<double>(kblocks) / splits);
     const double mma = kBM * bn * static_cast<double>(kBK) / kMacsPerCycle;
     const double b_bytes = (bm == 256 ? bn / 2 : bn) * kBK * 2.0;
@@ -67,7 +77,8 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int dout, int bm, int bn, int
     const double split_rounds = static_cast<double>(ceil_div(split_tiles * splits, grid));
     double compute = whole_rounds * (kblocks * per_kb + kUnitOverhead) +
                      split_rounds * (kb_split * per_kb + kUnitOverhead);
-    double bytes = 2.0 * (M * K + K * N) + static_cast<double>(out_bytes(dout)) * M * N;
+    double bytes = static_cast<double>(in_bytes(din)) * (M * K + K * N) +
+                   static_cast<double>(out_bytes(dout)) * M * N;
     if (splits > 1 && split_tiles > 0) {
         // parts 1..S-1 write an fp32 partial of their tile half; part 0
         // reads the S - 1 partials and adds them
@@ -98,17 +109,20 @@ int max_stages_for(int block_m, int block_n, int dtype_out) {
 tsgemm_status_t validate_problem(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
                                  int layout) {
     if (M < 1 || N < 1 || K < 1) return TSGEMM_ERR_INVALID_ARG;
-    if (dtype_in < TSGEMM_F16 || dtype_in > TSGEMM_F32) return TSGEMM_ERR_INVALID_ARG;
-    if (dtype_out < TSGEMM_F16 || dtype_out > TSGEMM_F32) return TSGEMM_ERR_INVALID_ARG;
+    if (dtype_in < TSGEMM_F16 || dtype_in > TSGEMM_E5M2) return TSGEMM_ERR_INVALID_ARG;
+    if (dtype_out < TSGEMM_F16 || dtype_out > TSGEMM_E5M2) return TSGEMM_ERR_INVALID_ARG;
     if (layout < TSGEMM_LAYOUT_RRR || layout > TSGEMM_LAYOUT_CCR) return TSGEMM_ERR_INVALID_ARG;
     if (!dtype_pair_ok(dtype_in, dtype_out)) return TSGEMM_ERR_UNSUPPORTED;
+    // 8-bit operands are read K-major only: A stored M x K, B stored N x K.
+    if (is_8bit(dtype_in) && layout != TSGEMM_LAYOUT_RCR) return TSGEMM_ERR_UNSUPPORTED;
     // Tensor-map coordinates and the kernel's tile indices are 32-bit.
     const int64_t lim = (int64_t{1} << 31) - 1;
     if (M > lim || N > lim || K > lim) return TSGEMM_ERR_UNSUPPORTED;
     // Stored row strides of A, B and C must be multiples of 16 bytes (TMA).
     const int64_t a_row = (layout & 2) ? M : K;  // A stored K x M, or M x K
     const int64_t b_row = (layout & 1) ? K : N;  // B stored N x K, or K x N
-    if ((a_row * 2) % 16 != 0 || (b_row * 2) % 16 != 0 || (N * out_bytes(dtype_out)) % 16 != 0)
+    const int64_t eb = in_bytes(dtype_in);
+    if ((a_row * eb) % 16 != 0 || (b_row * eb) % 16 != 0 || (N * out_bytes(dtype_out)) % 16 != 0)
         return TSGEMM_ERR_ALIGNMENT;
     return TSGEMM_OK;
 }
@@ -133,7 +147,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     if (f.units != 0 || f.workspace_bytes != 0) return TSGEMM_ERR_INVALID_ARG;  // derived fields
     if (f.split_tiles < 0 || (f.split_tiles > 0 && f.splits < 2)) return TSGEMM_ERR_INVALID_ARG;
 
-    const int64_t kblocks = ceil_div(K, kBK);
+    const int64_t kblocks = ceil_div(K, slice_k(dtype_in));
     if (f.splits > kblocks || f.splits > 4096) return TSGEMM_ERR_UNSUPPORTED;
 
     // Candidate tile widths: never wider than N rounded up to 64.
@@ -170,7 +184,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                 }
                 for (int64_t st : options) {
                     if (st < 0 || st > tiles) continue;
-                    const Estimate e = estimate(M, N, K, dtype_out, bm, bn, s, st, num_sms);
+                    const Estimate e = estimate(M, N, K, dtype_in, dtype_out, bm, bn, s, st, num_sms);
                     // strict improvement required: ties keep the earlier candidate
                     if (best_bn == 0 || e.cycles < best * 0.999) {
                         best = e.cycles;

@@ -11,6 +11,15 @@ namespace tsg {
 // Shared-memory budget of one CTA on sm_103a (227 KiB opt-in maximum).
 constexpr int64_t kSmemPerCtaMax = 232448;
 
+// 8-bit float input formats (E4M3, E5M2).
+bool is_8bit(int dtype);
+
+// Bytes per input element (1 or 2).
+int64_t in_bytes(int dtype_in);
+
+// K-elements per 128-byte ring slice: 64 (16-bit inputs) or 128 (8-bit).
+int slice_k(int dtype_in);
+
 // Validate a problem description without touching a GPU.
 tsgemm_status_t validate_problem(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
                                  int layout);

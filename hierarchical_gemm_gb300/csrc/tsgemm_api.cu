@@ -38,16 +38,17 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// tcgen05 instruction descriptor, kind::f16:
+// tcgen05 instruction descriptor, kind::f16 and kind::f8f6f4:
 //   bits  4-5  accumulator format (1 = fp32)
-//   bits  7-9  A format (0 = fp16, 1 = bf16)
+//   bits  7-9  A format (kind::f16: 0 = fp16, 1 = bf16;
+//              kind::f8f6f4: 0 = E4M3, 1 = E5M2)
 //   bits 10-12 B format
 //   bit  15    A major (0 = K-major: A stored M x K; 1 = MN-major: stored K x M)
 //   bit  16    B major (0 = K-major: B stored N x K; 1 = MN-major: stored K x N)
 //   bits 17-22 N >> 3
 //   bits 24-28 M >> 4
 uint32_t make_idesc(int dtype_in, int m, int n, int layout) {
-    const uint32_t fmt = dtype_in == TSGEMM_BF16 ? 1u : 0u;
+    const uint32_t fmt = (dtype_in == TSGEMM_BF16 || dtype_in == TSGEMM_E5M2) ? 1u : 0u;
     const uint32_t a_mn = tsg::a_kmajor(layout) ? 0u : 1u;
     const uint32_t b_mn = tsg::b_kmajor(layout) ? 0u : 1u;
     return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) |
@@ -58,7 +59,7 @@ int out_kind(int dtype_out) {
     return dtype_out == TSGEMM_F16 ? tsg::kOutF16 : (dtype_out == TSGEMM_BF16 ? tsg::kOutBF16 : tsg::kOutF32);
 }
 
-int64_t elem_bytes(int dt) { return dt == TSGEMM_F32 ? 4 : 2; }
+int64_t elem_bytes(int dt) { return dt == TSGEMM_F32 ? 4 : (tsg::is_8bit(dt) ? 1 : 2); }
 
 }  // namespace
 
@@ -138,8 +139,9 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     if (st != TSGEMM_OK) return st;
 
     const bool pair = cfg.block_m == 256;
-    const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out), layout)
-                            : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out), layout);
+    const bool in8 = tsg::is_8bit(dtype_in);
+    const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out), layout, in8)
+                            : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out), layout, in8);
     const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages)
                               : tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages);
     if (!kern || need != tsg::smem_bytes_for(cfg.block_m, cfg.block_n, dtype_out, cfg.stages) ||
@@ -221,7 +223,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.tiles_m = static_cast<int32_t>((M + cfg.block_m - 1) / cfg.block_m);
     gp.tiles_n = static_cast<int32_t>((N + cfg.block_n - 1) / cfg.block_n);
     gp.splits = cfg.splits;
-    gp.kblocks = static_cast<int32_t>((K + 63) / 64);
+    gp.kblocks = static_cast<int32_t>((K + tsg::slice_k(dtype_in) - 1) / tsg::slice_k(dtype_in));
     gp.group_m = cfg.group_m;
     gp.stages = cfg.stages;
     gp.debug_flags = cfg.debug_flags;
@@ -268,27 +270,32 @@ static bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
 static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* B) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return TSGEMM_ERR_CUDA;
-    const CUtensorMapDataType dt =
-        p->dtype_in == TSGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const bool in8 = tsg::is_8bit(p->dtype_in);
+    const CUtensorMapDataType dt = in8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : (p->dtype_in == TSGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    const int64_t eb = in8 ? 1 : 2;
     const cuuint32_t estr[2] = {1, 1};
     auto tile_map = [&](CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, cuuint32_t box_inner,
                         cuuint32_t box_outer) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * eb)};
         const cuuint32_t box[2] = {box_inner, box_outer};
         return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    // Every box is 64 elements (128 bytes, one swizzle row) along the
-    // contiguous dimension.
-    //   A stored M x K: 64 (K) x 128 (M) boxes;  A stored K x M: 64 (M) x 64 (K)
-    //   B stored K x N: 64 (N) x 64 (K) boxes;   B stored N x K: 64 (K) x the
-    //   CTA's columns (N) -- block_n, or block_n / 2 for a CTA pair
+    // Every box is 128 bytes (one swizzle row) along the contiguous
+    // dimension: 64 16-bit or 128 8-bit elements.
+    //   A stored M x K: 128 B (K) x 128 (M) boxes;  A stored K x M: 64 (M) x 64 (K)
+    //   B stored K x N: 64 (N) x 64 (K) boxes;      B stored N x K: 128 B (K) x
+    //   the CTA's columns (N) -- block_n, or block_n / 2 for a CTA pair
+    // (8-bit operands are always stored K-major, the first form of each).
+    const cuuint32_t kbox = static_cast<cuuint32_t>(128 / eb);
     const bool ak = tsg::a_kmajor(p->layout), bk = tsg::b_kmajor(p->layout);
     const cuuint32_t b_cols = static_cast<cuuint32_t>(p->cfg.block_m == 256 ? p->cfg.block_n / 2 : p->cfg.block_n);
-    const bool ok_a = ak ? tile_map(&p->tmA, A, p->K, p->M, 64, 128) : tile_map(&p->tmA, A, p->M, p->K, 64, 64);
-    const bool ok_b = bk ? tile_map(&p->tmB, B, p->K, p->N, 64, b_cols) : tile_map(&p->tmB, B, p->N, p->K, 64, 64);
+    const bool ok_a = ak ? tile_map(&p->tmA, A, p->K, p->M, kbox, 128) : tile_map(&p->tmA, A, p->M, p->K, 64, 64);
+    const bool ok_b = bk ? tile_map(&p->tmB, B, p->K, p->N, kbox, b_cols) : tile_map(&p->tmB, B, p->N, p->K, 64, 64);
     return ok_a && ok_b ? TSGEMM_OK : TSGEMM_ERR_CUDA;
 }
 
@@ -323,7 +330,8 @@ tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, voi
         return TSGEMM_ERR_CUDA;
     }
     if (dev != plan->device) return TSGEMM_ERR_INVALID_ARG;
-    const int64_t a_bytes = plan->M * plan->K * 2, b_bytes = plan->K * plan->N * 2;
+    const int64_t a_bytes = plan->M * plan->K * elem_bytes(plan->dtype_in);
+    const int64_t b_bytes = plan->K * plan->N * elem_bytes(plan->dtype_in);
     const int64_t c_bytes = plan->M * plan->N * elem_bytes(plan->dtype_out);
     if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)) return TSGEMM_ERR_INVALID_ARG;
 

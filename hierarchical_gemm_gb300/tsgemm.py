@@ -11,6 +11,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libtsgemm.so")
 
 F16, BF16, F32 = 0, 1, 2
+E4M3, E5M2 = 3, 4  # 8-bit float inputs (OCP FP8), RCR layout only
 # operand storage: A M x K or K x M (column-major), B K x N or N x K
 LAYOUT_RRR, LAYOUT_RCR, LAYOUT_CRR, LAYOUT_CCR = 0, 1, 2, 3
 _LAYOUT_NAMES = {"rrr": LAYOUT_RRR, "rcr": LAYOUT_RCR, "crr": LAYOUT_CRR, "ccr": LAYOUT_CCR}
@@ -28,7 +29,8 @@ DEBUG_SKIP_FIRST_LOAD = 1
 
 _DTYPE_NAMES = {"f16": F16, "fp16": F16, "float16": F16, "half": F16,
                 "bf16": BF16, "bfloat16": BF16,
-                "f32": F32, "fp32": F32, "float32": F32, "float": F32}
+                "f32": F32, "fp32": F32, "float32": F32, "float": F32,
+                "e4m3": E4M3, "float8_e4m3fn": E4M3, "e5m2": E5M2, "float8_e5m2": E5M2}
 
 # Every entry point include/tsgemm.h declares.
 EXPORTS = ("tsgemm_plan", "tsgemm_plan_ex", "tsgemm_run", "tsgemm_destroy",
@@ -199,27 +201,41 @@ _TORCH_OUT = {F16: "float16", BF16: "bfloat16", F32: "float32"}
 _plans = {}
 
 
+def _storage(X):
+    """(column-major?, tensor whose data pointer is the stored matrix) for a
+    2-D CUDA tensor that is row-major contiguous or the transpose of one."""
+    if X.is_contiguous():
+        return False, X
+    if X.t().is_contiguous():
+        return True, X.t()
+    raise ValueError("operands must be row-major contiguous or transposes of contiguous tensors")
+
+
 def gemm(A, B, out_dtype=None, C=None, stream=None):
-    """C = A @ B for row-major CUDA tensors A (M x K) and B (K x N) of dtype
-    float16 or bfloat16; plans are cached per shape and dtype."""
+    """C = A @ B for CUDA tensors A (M x K) and B (K x N) of dtype float16,
+    bfloat16, float8_e4m3fn or float8_e5m2.  Each operand may be row-major
+    contiguous or a transposed view of a contiguous tensor (for example
+    W.t() of a weight W stored N x K); the layout follows from the strides.
+    Plans are cached per shape, dtype and layout."""
     import torch
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError("expected A (M x K) and B (K x N)")
     if A.dtype != B.dtype:
         raise ValueError("A and B must have the same dtype")
-    if not (A.is_contiguous() and B.is_contiguous()):
-        raise ValueError("A and B must be row-major contiguous")
+    a_col, A_store = _storage(A)
+    b_col, B_store = _storage(B)
+    layout = (LAYOUT_CRR if a_col else 0) | (LAYOUT_RCR if b_col else 0)
     din = dtype_code(A.dtype)
     dout = dtype_code(out_dtype) if out_dtype is not None else (F32 if C is None else dtype_code(C.dtype))
     M, K = A.shape
     N = B.shape[1]
-    key = (A.device.index, M, N, K, din, dout)
+    key = (A.device.index, M, N, K, din, dout, layout)
     plan = _plans.get(key)
     if plan is None:
-        plan = _plans[key] = Plan(M, N, K, din, dout)
+        plan = _plans[key] = Plan(M, N, K, din, dout, layout=layout)
     if C is None:
         C = torch.empty((M, N), dtype=getattr(torch, _TORCH_OUT[dout]), device=A.device)
-    return plan.run(A, B, C, stream)
+    return plan.run(A_store, B_store, C, stream)
 
 
 def run_splitk_noalloc(A, B, C, splits=0, status=None, stream=None):

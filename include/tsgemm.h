@@ -15,9 +15,15 @@
  * beyond the fp32 summation order.
  *
  * Supported (dtype_in, dtype_out): (F16, F32), (F16, F16), (BF16, BF16),
- * (BF16, F32).  Everything else returns TSGEMM_ERR_UNSUPPORTED.
+ * (BF16, F32), and the 8-bit float inputs (E4M3 or E5M2, both operands the
+ * same format) with an F16, BF16 or F32 output: a low-precision GEMM on the
+ * same skeleton, of the Dequant-GEMM family TileLang targets ("TileScale 与
+ * TileLang比较", sections 设计目标、定位与适用场景 and 生态互操作、性能、
+ * 局限与路线图).  8-bit inputs take the RCR layout only (A stored M x K, B stored N x K, the
+ * K-major form both tensor-core operands are read in).  Everything else
+ * returns TSGEMM_ERR_UNSUPPORTED.
  *
- * Numerics.  Products of the 16-bit inputs are exact; sums are fp32 in an
+ * Numerics.  Products of the 16-bit or 8-bit inputs are exact; sums are fp32 in an
  * order fixed by the plan (tensor-core order inside a K-slice, K-slices in
  * increasing k, split-K partials added in split order 0..S-1), so results
  * are reproducible run to run.  fp32 -> bf16/fp16 output conversion rounds
@@ -26,8 +32,9 @@
  * Memory.  A, B and C are device pointers owned by the caller, on the device
  * that was current when the plan was made, 16-byte aligned, with C not
  * overlapping A or B.  Stored row strides must be multiples of 16 bytes: A's
- * (K * 2, or M * 2 when A is stored K x M), B's (N * 2, or K * 2 when B is
- * stored N x K) and C's (N * sizeof(out)); otherwise TSGEMM_ERR_ALIGNMENT.
+ * (K * e, or M * e when A is stored K x M), B's (N * e, or K * e when B is
+ * stored N x K), e the input element size (2, or 1 for 8-bit inputs), and
+ * C's (N * sizeof(out)); otherwise TSGEMM_ERR_ALIGNMENT.
  *
  * Errors.  Every call returns a tsgemm_status_t.  Argument, alignment and
  * device errors are detected on the host before anything is launched.  A
@@ -56,7 +63,9 @@ typedef struct tsgemm_plan_s* tsgemm_plan_t;
 typedef enum {
     TSGEMM_F16 = 0,  /* IEEE binary16 */
     TSGEMM_BF16 = 1, /* bfloat16 */
-    TSGEMM_F32 = 2   /* IEEE binary32 (outputs only) */
+    TSGEMM_F32 = 2,  /* IEEE binary32 (outputs only) */
+    TSGEMM_E4M3 = 3, /* OCP 8-bit float E4M3 (bias 7, no infinities, max 448); inputs only */
+    TSGEMM_E5M2 = 4  /* OCP 8-bit float E5M2 (bias 15, IEEE-style inf/NaN, max 57344); inputs only */
 } tsgemm_dtype_t;
 
 /* Operand storage.  C is always M x N row-major.  The transposed-B forms are

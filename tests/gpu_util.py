@@ -1,13 +1,17 @@
-"""Helpers shared by the GPU tests: move 16-bit input bits to the device, run
-a plan through the C ABI and bring the output back as raw bits."""
+"""Helpers shared by the GPU tests: move 16-bit or 8-bit input bits to the
+device, run a plan through the C ABI and bring the output back as raw bits."""
 import numpy as np
 import torch
 
-TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+            "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 def to_dev(bits, din, device="cuda"):
-    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+    if din in ("e4m3", "e5m2"):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.uint8)).to(device)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
     return t.view(TORCH_DT[din])
 
 

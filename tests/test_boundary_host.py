@@ -188,3 +188,44 @@ def test_alignment_rules_per_layout(ts, layout, shape, code):
         with pytest.raises(ts.TsgemmError) as e:
             ts.choose_config(M, N, K, "bf16", "bf16", 152, layout=layout)
         assert e.value.status == ts.ERR_ALIGNMENT
+
+
+# ------------------------------------------------------- 8-bit inputs --
+
+@pytest.mark.parametrize("din", ["e4m3", "e5m2"])
+def test_fp8_takes_the_k_major_layout_only(ts, din):
+    for dout in ("f16", "bf16", "f32"):
+        cfg = ts.choose_config(512, 512, 1024, din, dout, 152, layout="rcr")
+        assert cfg["block_n"] in (64, 128, 192, 256)
+    for layout in ("rrr", "crr", "ccr"):
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(512, 512, 1024, din, "bf16", 152, layout=layout)
+        assert e.value.status == ts.ERR_UNSUPPORTED
+    for dout in ("e4m3", "e5m2"):  # 8-bit formats are inputs only
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(512, 512, 1024, din, dout, 152, layout="rcr")
+        assert e.value.status == ts.ERR_UNSUPPORTED
+
+
+def test_fp8_alignment_is_in_bytes(ts):
+    ts.choose_config(64, 64, 16, "e4m3", "f32", 152, layout="rcr")  # rows of 16 bytes
+    for shape in [(64, 64, 8), (64, 64, 24)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(*shape, "e4m3", "f32", 152, layout="rcr")
+        assert e.value.status == ts.ERR_ALIGNMENT
+
+
+def test_fp8_slices_are_128_deep(ts):
+    # K = 256 is two 128-element slices: at most two K parts
+    ts.choose_config(128, 128, 256, "e4m3", "f32", 152, layout="rcr", splits=2)
+    with pytest.raises(ts.TsgemmError) as e:
+        ts.choose_config(128, 128, 256, "e4m3", "f32", 152, layout="rcr", splits=3)
+    assert e.value.status == ts.ERR_UNSUPPORTED
+    # the 16-bit path at the same K has four 64-element slices
+    ts.choose_config(128, 128, 256, "bf16", "f32", 152, layout="rcr", splits=4)
+
+
+def test_fp8_dtype_names(ts):
+    assert ts.dtype_code("e4m3") == ts.E4M3 == 3
+    assert ts.dtype_code(torch.float8_e4m3fn) == ts.E4M3
+    assert ts.dtype_code(torch.float8_e5m2) == ts.E5M2 == 4
