@@ -11,7 +11,9 @@ Prints one JSON line.  `value` is TFLOP/s (2*M*N*K per step) over all ranks;
 `e2e` is the same metric through the same C ABI call with pinned host
 buffers, the host->device copies of A and B and the device->host copy of C
 inside the timed region; `roofline` relates the kernel to the measured bf16
-tensor peak; `cpu_baseline` is the fp64 oracle timed on the host cores.
+tensor peak (for 8-bit inputs: twice that, the nominal fp8 : bf16 ratio);
+`cpu_baseline` is the fp64 oracle timed on the host cores.  --workload picks
+another seeded workload (the five benchmark configurations, or the FP8 ones).
 
 With --impl reference the fp64 CPU oracle itself is timed on the same
 metric (a bounded sample of rows of the product per step).
@@ -45,6 +47,23 @@ KERNEL_SOURCES = ["hierarchical_gemm_gb300/csrc/gemm_sm103.cuh",
                   "hierarchical_gemm_gb300/csrc/ptx.cuh",
                   "hierarchical_gemm_gb300/csrc/kernels_1sm.cu",
                   "hierarchical_gemm_gb300/csrc/kernels_2sm.cu"]
+# nominal dense fp8 : bf16 tensor throughput on GB300 (4.5 : 2.25 PFLOP/s)
+FP8_TO_BF16 = 2.0
+
+
+def to_device_bits(bits, din, device=None, pin=False):
+    """A torch tensor of the input format holding the numpy bit patterns."""
+    import numpy as np
+    import torch
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn,
+           "e5m2": torch.float8_e5m2}[din]
+    raw = np.ascontiguousarray(bits)
+    t = torch.from_numpy(raw.view(np.uint8) if raw.dtype == np.uint8 else raw.view(np.int16))
+    if pin:
+        t = t.pin_memory()
+    elif device is not None:
+        t = t.to(device)
+    return t.view(tdt)
 
 
 def parse_args(argv=None):
@@ -251,7 +270,7 @@ def run_reference(args):
     import oracle
     import synth
     w = synth.workload(args.workload)
-    A, B = synth.inputs(args.workload)
+    A, B = synth.inputs(args.workload)  # logical A (M x K), B (K x N)
     # size one step at ~ (cpu_seconds / steps), at least 8 rows
     per_step = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
     _, rows, _, _ = oracle_rows_tflops(A, B, w["dtype_in"], per_step)
@@ -302,15 +321,17 @@ def run_ours(args):
     w = synth.workload(args.workload)
     M, N, K = w["M"], w["N"], w["K"]
     din, dout = w["dtype_in"], w["dtype_out"]
+    layout = w["layout"]
     off = rank_seed_offset(rank)
     A_np = synth.matrix(M, K, w["dist_a"], w["seed_a"] + off, din)
     B_np = synth.matrix(K, N, w["dist_b"], w["seed_b"] + off, din)
+    A_st, B_st = synth.stored(A_np, B_np, layout)  # as the library is handed them
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    A = torch.from_numpy(A_np.view(np.int16)).to(dev).view(tdt[din])
-    B = torch.from_numpy(B_np.view(np.int16)).to(dev).view(tdt[din])
+    A = to_device_bits(A_st, din, dev)
+    B = to_device_bits(B_st, din, dev)
     C = torch.empty((M, N), dtype=tdt[dout], device=dev)
     force = {k: int(v) for k, v in (kv.split("=") for kv in args.plan.split(",") if kv)}
-    plan = tsgemm.Plan(M, N, K, din, dout, **force)
+    plan = tsgemm.Plan(M, N, K, din, dout, layout=layout, **force)
     cfg = plan.config
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -376,13 +397,13 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = args.e2e_steps or min(args.steps, 50)
-        A_pin = torch.from_numpy(A_np.view(np.int16)).view(tdt[din]).pin_memory()
-        B_pin = torch.from_numpy(B_np.view(np.int16)).view(tdt[din]).pin_memory()
+        A_pin = to_device_bits(A_st, din, pin=True)
+        B_pin = to_device_bits(B_st, din, pin=True)
         C_pin = torch.empty((M, N), dtype=tdt[dout]).pin_memory()
         A_d = [torch.empty_like(A) for _ in range(2)]
         B_d = [torch.empty_like(B) for _ in range(2)]
         C_d = [torch.empty_like(C) for _ in range(2)]
-        plans = [tsgemm.Plan(M, N, K, din, dout, **force) for _ in range(2)]
+        plans = [tsgemm.Plan(M, N, K, din, dout, layout=layout, **force) for _ in range(2)]
         s_up, s_gemm, s_down = (torch.cuda.Stream(dev) for _ in range(3))
         ev = lambda: torch.cuda.Event()  # noqa: E731
         up_done, gemm_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -436,13 +457,20 @@ def run_ours(args):
 
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    peak_desc = peak_kind + " bf16 burst (cuBLAS-class torch.matmul)"
+    eight_bit = din in ("e4m3", "e5m2")
+    if eight_bit:
+        peak *= FP8_TO_BF16
+        peak_desc += " x %.0f (nominal fp8 : bf16 dense ratio)" % FP8_TO_BF16
     achieved = flops / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": stored_traffic(w["name"]),
-                "peak_kind": peak_kind + " bf16 burst (cuBLAS-class torch.matmul)",
-                "kernel": "gemm_sm103_%s<BN=%d>" % ("2sm" if cfg["block_m"] == 256 else "1sm", cfg["block_n"]),
+                "peak_kind": peak_desc,
+                "kernel": "gemm_sm103_%s<BN=%d%s>" % ("2sm" if cfg["block_m"] == 256 else "1sm", cfg["block_n"],
+                                                     ", 8-bit" if eight_bit else ""),
                 "algorithmic_flops_per_launch": flops,
-                "algorithmic_bytes_per_launch": 2 * (M * K + K * N) + (4 if dout == "f32" else 2) * M * N}
+                "algorithmic_bytes_per_launch": synth.workloads.in_nbytes(din) * (M * K + K * N)
+                + synth.workloads.out_nbytes(dout) * M * N}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -456,8 +484,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if din == "bf16" else "f16", "data": "synthetic",
-        "config": {"workload": w["name"], "M": M, "N": N, "K": K, "dtype_in": din,
+        "dtype": din, "data": "synthetic",
+        "config": {"workload": w["name"], "M": M, "N": N, "K": K, "dtype_in": din, "layout": layout,
                    "dtype_out": dout, "accumulate": "f32", "l2": "flushed between steps (256 MB write)",
                    "plan": {k: cfg[k] for k in ("block_m", "block_n", "splits", "stages", "group_m", "grid")},
                    "parallelism": "independent replica per GPU" if world > 1 else "1 GPU"},

@@ -125,4 +125,4 @@ def matrix(rows, cols, dist, seed, dtype, out=None):
     return out
 
 
-from .workloads import WORKLOADS, workload, inputs  # noqa: E402,F401
+from .workloads import WORKLOADS, EXTRA_WORKLOADS, workload, inputs, stored  # noqa: E402,F401

@@ -1,8 +1,11 @@
-"""The five seeded GEMM workloads: shapes, formats, distributions and seeds.
+"""The seeded GEMM workloads: shapes, formats, distributions and seeds.
 
-Seeds: A uses 0x7E5A0000 + index, B uses 0x7E5A0000 + index + 0x100, where
-index is the workload's position in this table (0-based).  A is generated
-before B; both are row-major.
+WORKLOADS holds the five benchmark configurations; EXTRA_WORKLOADS the ones
+of the wider rows built on the same kernels (8-bit inputs).  Seeds: A uses
+0x7E5A0000 + index, B uses 0x7E5A0000 + index + 0x100.  A (M x K) is
+generated before B (K x N), both as logical row-major matrices; `layout`
+says how the library is handed them (for "rcr", B is stored transposed,
+N x K), which changes no value.
 """
 import numpy as np
 
@@ -34,8 +37,23 @@ WORKLOADS = {
 }
 
 
+# FP8 (E4M3) inputs, bf16 output, operands stored K-major (RCR): the
+# 4096^3 and 16384 x 16384 x 8192 shapes of the table above.
+EXTRA_WORKLOADS = {
+    "gemm_4096_e4m3_rcr": dict(
+        index=5, M=4096, N=4096, K=4096, dtype_in="e4m3", dtype_out="bf16",
+        dist_a=("normal", 1.0), dist_b=("normal", 1.0),
+        exact=False, cluster=None, layout="rcr"),
+    "gemm_16384x16384x8192_e4m3_rcr": dict(
+        index=6, M=16384, N=16384, K=8192, dtype_in="e4m3", dtype_out="bf16",
+        dist_a=("uniform", -1.0, 1.0), dist_b=("uniform", -1.0, 1.0),
+        exact=False, cluster=(2, 1), layout="rcr"),
+}
+
+
 def workload(name):
-    w = dict(WORKLOADS[name])
+    w = dict(WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name])
+    w.setdefault("layout", "rrr")
     w["name"] = name
     w["seed_a"] = _SEED_BASE + w["index"]
     w["seed_b"] = _SEED_BASE + w["index"] + 0x100
@@ -44,7 +62,9 @@ def workload(name):
 
 
 def inputs(name, out_a=None, out_b=None):
-    """(A_bits, B_bits) numpy uint16 arrays for a named workload."""
+    """(A_bits, B_bits) numpy arrays (uint16 for 16-bit inputs, uint8 for
+    8-bit) of the logical row-major A (M x K) and B (K x N) of a named
+    workload."""
     from . import matrix
     w = workload(name)
     A = matrix(w["M"], w["K"], w["dist_a"], w["seed_a"], w["dtype_in"], out=out_a)
@@ -54,6 +74,20 @@ def inputs(name, out_a=None, out_b=None):
 
 def out_nbytes(dtype_out):
     return 4 if dtype_out == "f32" else 2
+
+
+def in_nbytes(dtype_in):
+    return 1 if dtype_in in ("e4m3", "e5m2") else 2
+
+
+def stored(A, B, layout):
+    """The operands as the library is handed them for `layout`: A as is or
+    transposed (K x M), B as is or transposed (N x K), both contiguous."""
+    import numpy as np
+    lay = {"rrr": 0, "rcr": 1, "crr": 2, "ccr": 3}[layout]
+    A_s = np.ascontiguousarray(A.T) if lay & 2 else A
+    B_s = np.ascontiguousarray(B.T) if lay & 1 else B
+    return A_s, B_s
 
 
 def out_numpy_dtype(dtype_out):
