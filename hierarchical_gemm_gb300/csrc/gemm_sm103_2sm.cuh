@@ -19,6 +19,15 @@
 //     leader (remote mbarrier arrive) when the accumulator is free again.
 // Everything else -- the persistent schedule over work units, the split-K
 // workspace reduction, the bounded waits -- is the one-SM kernel's.
+//
+// With kPairs = 2 the cluster holds two such pairs side by side along N
+// (4 x 1 CTAs: ranks 0-1 and 2-3), computing the tiles (tm, 2j) and
+// (tm, 2j + 1) of the same A rows.  The CTAs of the two pairs that hold the
+// same 128 A rows each load half of them and TMA-multicast it to both, so
+// each SM fetches 8 KiB of A per K-slice instead of 16 (the cluster network
+// of the TileScale hierarchy sharing operand tiles through distributed
+// shared memory).  A slot of a CTA is then written by both pairs, so its
+// empty barrier waits for both pairs' MMA commits.
 #pragma once
 
 #include "gemm_sm103.cuh"
@@ -42,11 +51,43 @@ __host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
     return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 6) + 16u;
 }
 
-template <int BN, int kOut, int kLayout, bool kF8 = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// The loads of one K-slice by a CTA of a two-pair cluster: its own B
+// columns, and half `pair` (64 rows) of the 128 A rows that the CTAs of
+// rank `half` in both pairs need, multicast to both.  Every byte completes
+// on the barrier `fb` of the destination's pair leader.
+template <int kLayout, int kBCols, bool kF8>
+__device__ __forceinline__ void load_slice_mc(uint32_t a_dst, uint32_t b_dst, const CUtensorMap* tmA,
+                                              const CUtensorMap* tmB, uint32_t fb, bool leader, uint32_t half,
+                                              uint32_t pair, int kb, int32_t row, int32_t col) {
+    static_assert(!kF8 || (a_kmajor(kLayout) && b_kmajor(kLayout)), "8-bit operands are K-major");
+    constexpr int kSK = slice_k<kF8>();
+    const uint16_t mask = static_cast<uint16_t>((1u << half) | (1u << (half + 2u)));
+    const uint32_t a_part = a_dst + pair * 8192u;  // rows [64 pair, 64 pair + 64) of the A tile
+    const int32_t arow = row + 64 * static_cast<int32_t>(pair);
+    if constexpr (a_kmajor(kLayout))
+        tma_load_2d_pair_mc(a_part, tmA, fb, mask, kb * kSK, arow);  // 128 bytes (K) x 64 (M)
+    else
+        tma_load_2d_pair_mc(a_part, tmA, fb, mask, arow, kb * kSK);  // 64 (M) x 64 (K)
+    auto ld = [&](uint32_t dst, int32_t c0, int32_t c1) {
+        if (leader)
+            tma_load_2d(dst, tmB, fb, c0, c1);
+        else
+            tma_load_2d_pair(dst, tmB, fb, c0, c1);
+    };
+    if constexpr (b_kmajor(kLayout)) {
+        ld(b_dst, kb * kSK, col);  // one 128-byte (K) x kBCols (N) box
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBCols / 64; ++j) ld(b_dst + j * 8192u, col + j * 64, kb * kSK);
+    }
+}
+
+template <int BN, int kOut, int kLayout, bool kF8 = false, int kPairs = 1>
+__global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_sm103_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     using PS = PairShape<BN>;
+    static_assert(kPairs == 1 || kPairs == 2, "one or two CTA pairs per cluster");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -68,13 +109,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();  // 0: leader, 1: peer
-    const bool leader = rank == 0;
+    const uint32_t rank = cluster_ctarank();  // 2 * pair + half
+    const uint32_t half = rank & 1u;          // 0: the pair's leader, 1: its peer
+    const uint32_t pair = rank >> 1;          // which pair of the cluster
+    const uint32_t lead_rank = rank & ~1u;
+    const bool leader = half == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);   // the leader's producer arrives once
-            mbar_init(empty_bar(s), 1);  // one multicast commit
+            mbar_init(empty_bar(s), kPairs);  // one multicast commit from each pair's leader
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);                    // one multicast commit
@@ -92,14 +136,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_alloc<2>(smem_u32(tmem_holder), PS::kTmemCols);
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // barriers of both CTAs initialised before either uses them
+    cluster_sync();  // barriers of every CTA initialised before any uses them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-    ctl.peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+    for (uint32_t r = 0; r < 2u * kPairs; ++r)
+        if (r != rank) ctl.peer_abort[ctl.npeers++] = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), r);
 
-    const int64_t cluster_id = blockIdx.x >> 1;
-    const int64_t nclusters = gridDim.x >> 1;
+    const int64_t cluster_id = blockIdx.x / (2 * kPairs);
+    const int64_t nclusters = gridDim.x / (2 * kPairs);
 
     if (warp == 0) {
         // ------------------------------------------- TMA producer (both) --
@@ -123,15 +168,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         skip = false;
                     } else {
                         const uint32_t a_dst = base + stage * PS::kStageBytes;
-                        const int32_t arow = un.tm * (2 * kBM) + static_cast<int32_t>(rank) * kBM;
-                        const int32_t bcol = un.tn * BN + static_cast<int32_t>(rank) * PS::kBCols;
-                        if (leader) {
-                            mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
-                            load_slice<kLayout, PS::kBCols, false, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
-                                                                   full_bar(stage), kb, arow, bcol);
+                        const int32_t arow = un.tm * (2 * kBM) + static_cast<int32_t>(half) * kBM;
+                        const int32_t tn = un.tn * kPairs + static_cast<int32_t>(pair);
+                        const int32_t bcol = tn * BN + static_cast<int32_t>(half) * PS::kBCols;
+                        if constexpr (kPairs == 1) {
+                            if (leader) {
+                                mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
+                                load_slice<kLayout, PS::kBCols, false, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                            full_bar(stage), kb, arow, bcol);
+                            } else {
+                                load_slice<kLayout, PS::kBCols, true, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                           mapa_shared(full_bar(stage), 0u), kb,
+                                                                           arow, bcol);
+                            }
                         } else {
-                            load_slice<kLayout, PS::kBCols, true, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
-                                                                  mapa_shared(full_bar(stage), 0u), kb, arow, bcol);
+                            // the pair leader's barrier counts the bytes landing in
+                            // both CTAs of the pair, from either pair's loads
+                            const uint32_t fb = leader ? full_bar(stage) : mapa_shared(full_bar(stage), lead_rank);
+                            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
+                            load_slice_mc<kLayout, PS::kBCols, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB, fb,
+                                                                    leader, half, pair, kb, arow, bcol);
                         }
                         outstanding |= 1u << stage;
                         out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
@@ -173,7 +229,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint32_t a_addr = base + stage * PS::kStageBytes;
                         mma_slice<kLayout, 2, kF8>(d_tmem, a_addr, a_addr + PS::kABytes, p.idesc,
                                               kb > un.kb0 ? 1u : 0u);
-                        umma_commit_pair(empty_bar(stage), 0x3);  // slot free in both CTAs
+                        // slot free in every CTA whose slot these MMAs read or whose
+                        // loads wrote into it
+                        umma_commit_pair(empty_bar(stage), static_cast<uint16_t>((1u << (2 * kPairs)) - 1u));
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -181,13 +239,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(tfull_bar(acc), 0x3);
+                umma_commit_pair(tfull_bar(acc), static_cast<uint16_t>(0x3u << lead_rank));
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
-            umma_commit_pair(drain_bar, 0x1);
+            umma_commit_pair(drain_bar, static_cast<uint16_t>(1u << lead_rank));
             wait_bounded(drain_bar, 0u, ctl, false);
         }
         __syncwarp();
@@ -221,24 +279,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (leader)
                     mbar_arrive(tempty_bar(a));
                 else
-                    mbar_arrive_cluster(tempty_bar(a), 0u);
+                    mbar_arrive_cluster(tempty_bar(a), lead_rank);
             }
         };
         for (int64_t u = cluster_id; u < p.units; u += nclusters) {
-            const Unit un = decode_unit(p, u);
-            const int tm = un.tm, tn = un.tn;
+            Unit un = decode_unit(p, u);
+            un.tn = un.tn * kPairs + static_cast<int>(pair);  // this pair's tile column
+            const int tm = un.tm;
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, ctl) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             __syncwarp();
             tc_fence_after();
-            const int row0 = tm * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32;
+            const int row0 = tm * (2 * kBM) + static_cast<int>(half) * kBM + q * 32;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PS::kAccCols;
             // workspace tile and counter of this CTA's 128-row half
-            const int64_t half = un.slot * 2 + rank;
+            const int64_t wh = (un.slot * kPairs + pair) * 2 + half;
             const int a_now = acc;
-            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, half, c_begin, etid, last_flag,
+            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, wh, c_begin, etid, last_flag,
                                       ctl, epi_sync, [&]() { release_acc(a_now); }))
                 break;
             if (++acc == 2) {
@@ -250,8 +309,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ exit --
-    // Neither CTA leaves while the other may still read its shared memory
-    // or signal its barriers; tensor memory of the pair is freed together.
+    // No CTA leaves while another may still read or write its shared memory
+    // or signal its barriers; tensor memory of a pair is freed together.
     // The barriers here are the non-aligned forms, which count threads one
     // by one, so warps whose lane 0 ran a role loop alone may arrive in any
     // convergence state.

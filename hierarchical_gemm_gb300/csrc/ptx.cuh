@@ -122,8 +122,20 @@ struct WaitCtl {
     volatile int* abort;   // shared memory
     int* status;           // global status word of the plan
     uint64_t timeout_ns;
-    uint32_t peer_abort = 0;  // shared::cluster address of the peer CTA's flag (pairs), or 0
+    // shared::cluster addresses of the abort flags of the other CTAs of the
+    // cluster (at most 3), which a CTA that gives up sets too
+    uint32_t peer_abort[3] = {0u, 0u, 0u};
+    int npeers = 0;
 };
+
+// Record a timeout: this CTA's and its cluster peers' abort flags, and the
+// plan's status word.
+__device__ __forceinline__ void record_timeout(const WaitCtl& ctl) {
+    *ctl.abort = 1;
+    for (int i = 0; i < ctl.npeers; ++i) st_shared_cluster_u32(ctl.peer_abort[i], 1u);
+    atomicExch(ctl.status, 5 /* TSGEMM_ERR_TIMEOUT */);
+    __threadfence();
+}
 
 // Wait for phase `parity` of `bar`, for at most ctl.timeout_ns.  Returns
 // false when the limit expired (after recording the timeout) or, if
@@ -140,10 +152,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
         if (probe()) return true;
         if (respect_abort && *ctl.abort) return false;
         if (globaltimer() - t0 > ctl.timeout_ns) {
-            *ctl.abort = 1;
-            if (ctl.peer_abort) st_shared_cluster_u32(ctl.peer_abort, 1u);
-            atomicExch(ctl.status, 5 /* TSGEMM_ERR_TIMEOUT */);
-            __threadfence();
+            record_timeout(ctl);
             return false;
         }
     }
@@ -175,10 +184,7 @@ __device__ __forceinline__ bool wait_flag_bounded(const int* p, int value, const
         if (ld_acquire_gpu(p) == value) return true;
         if (*ctl.abort) return false;
         if (globaltimer() - t0 > ctl.timeout_ns) {
-            *ctl.abort = 1;
-            if (ctl.peer_abort) st_shared_cluster_u32(ctl.peer_abort, 1u);
-            atomicExch(ctl.status, 5 /* TSGEMM_ERR_TIMEOUT */);
-            __threadfence();
+            record_timeout(ctl);
             return false;
         }
     }
@@ -210,6 +216,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
         "bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(m), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Multicast form of tma_load_2d_pair: the box lands at `dst` in every CTA
+// of `cta_mask` (bit i = cluster rank i).  The bytes that land in a CTA
+// complete on the barrier at the offset of `bar_cluster` in the even CTA of
+// that destination's pair (the address passed is the issuing pair's even
+// CTA's barrier).
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster,
+                                                    uint16_t cta_mask, int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes.multicast::cluster [%0], [%1, {%4, %5}], [%2], %3;" ::"r"(dst),
+        "l"(m), "r"(bar_cluster), "h"(cta_mask), "r"(c0), "r"(c1)
         : "memory");
 }
 

@@ -104,9 +104,13 @@ typedef struct {
                                 split_tiles * (splits - 1) * block_m * block_n * 4 bytes */
     int32_t timeout_ms;   /* limit of every device-side wait */
     int32_t debug_flags;  /* tests only: TSGEMM_DEBUG_* */
-    int64_t split_tiles;  /* tiles split into `splits` K parts: the last ones of
-                             the schedule (all tiles, or the last partial wave).
-                             Forced with splits > 1; 0 then means every tile. */
+    int64_t split_tiles;  /* work units split into `splits` K parts: the last
+                             ones of the schedule (all, or the last partial
+                             wave). Forced with splits > 1; 0 then means all. */
+    int32_t cluster_n;    /* CTA pairs per cluster along N (block_m 256 only):
+                             1, or 2 = two pairs compute adjacent 256 x 256
+                             tiles of the same A rows and share those A tiles
+                             by TMA multicast (a work unit is then 2 tiles) */
 } tsgemm_config_t;
 
 /* Tests only: the first CTA (or CTA pair) skips the first operand load of

@@ -229,3 +229,20 @@ def test_fp8_dtype_names(ts):
     assert ts.dtype_code("e4m3") == ts.E4M3 == 3
     assert ts.dtype_code(torch.float8_e4m3fn) == ts.E4M3
     assert ts.dtype_code(torch.float8_e5m2) == ts.E5M2 == 4
+
+
+# ------------------------------------------- two CTA pairs per cluster --
+
+def test_cluster_n_rules(ts):
+    cfg = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, cluster_n=2)
+    assert cfg["cluster_n"] == 2 and cfg["block_m"] == 256 and cfg["block_n"] == 256
+    assert cfg["grid"] % 4 == 0 and cfg["grid"] <= 152
+    # a unit is two tiles: 16 tile rows x 8 column pairs
+    assert cfg["units"] == 16 * 8 + cfg["split_tiles"] * (cfg["splits"] - 1)
+    assert cfg["workspace_bytes"] == cfg["split_tiles"] * (cfg["splits"] - 1) * 256 * 512 * 4
+    for force in [dict(cluster_n=2, block_m=128), dict(cluster_n=2, block_n=128), dict(cluster_n=3)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, **force)
+        assert e.value.status == ts.ERR_UNSUPPORTED, force
+    # unforced plans on one SM tile keep one pair (or no pair) per cluster
+    assert ts.choose_config(128, 28672, 8192, "bf16", "bf16", 152)["cluster_n"] == 1
