@@ -207,16 +207,22 @@ struct CStager {
 // at `tbase`; this thread holds row `row_local`, and its warp's 32 rows
 // start at row `row0` of C).
 //   * A whole tile is converted and stored to C.
-//   * A part s > 0 of a tile split along K writes its fp32 partial and
-//     counts itself in; part 0 waits for the others, adds them to its own
-//     accumulator in split order and stores C.  The sum is p_0 + p_1 + ... +
-//     p_{S-1}, the same bits on every run.  Only part 0 waits, and for
-//     higher-numbered units, so the S parts of a tile must run on S
-//     different CTAs (or pairs): the planner keeps S within the grid.
+//   * The S parts of a tile split along K share the reduction: 32-column
+//     chunk j of the tile belongs to part j mod S.  Every part writes the
+//     fp32 partial of the chunks it does not own to the workspace and counts
+//     itself in; once all S have, each part adds, for every chunk it owns,
+//     the S partials in split order (0 + p_0 + p_1 + ... + p_{S-1}, its own
+//     from tensor memory) and stores C.  The bits do not depend on which
+//     part owns a chunk or on timing.  The last part to finish reading
+//     resets the tile's counter.  All S parts wait for each other, so they
+//     must run at the same time on S different CTAs (or pairs): the planner
+//     keeps S within the grid, and since the schedule is static and every
+//     CTA walks its units in order, parts that straddle two rounds still
+//     meet.
 // `h` indexes the workspace tile and counter of this 128-row half;
-// `epi_sync` is the epilogue warpgroup's bounded barrier and `release` hands
-// the accumulator back to the MMA issuer.  Returns false if the CTA is
-// aborting.
+// `epi_sync` is the epilogue's bounded barrier (both warpgroups) and
+// `release` hands the accumulator back to the MMA issuer.  Returns false if
+// the CTA is aborting.
 template <int BN, int kOut, class Sync, class Release>
 __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
                                            const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
@@ -235,63 +241,83 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
         }
         return true;
     }
-    // A tile split along K: part 0 (k = 0) owns it.  Parts 1..S-1 write
-    // their fp32 partials to the workspace and count themselves in; the
-    // owner waits for S - 1 of them and stores C = p_0 + p_1 + ... + p_{S-1},
-    // added in split order.  Each partial of a 128 x BN half tile is stored
-    // in the order the epilogue warps hold it, so every warp access is 512
-    // contiguous bytes: [BN/32 column chunks][4 lane quarters][8 float4][32
-    // lanes].
+    // Each partial chunk of a 128 x BN half tile is stored in the order the
+    // epilogue warps hold it, so every warp access is 512 contiguous bytes:
+    // [part][BN/32 chunks][4 lane quarters][8 float4][32 lanes].
+    const int S = un.nsplit, me = un.split;
     const int q = row_local >> 5, lane = row_local & 31;
-    constexpr int kChunkFloats = 4 * 8 * 128;  // one 32-column chunk of the half tile
-    auto part = [&](int s) -> float* {         // partial of part s >= 1, this thread
-        return p.ws + (h * (un.nsplit - 1) + (s - 1)) * (kBM * BN) + q * (8 * 128) + lane * 4;
+    constexpr int kChunks = BN / 32;
+    constexpr int kChunkFloats = 4 * 8 * 128;
+    auto part = [&](int s, int chunk) -> float* {
+        return p.ws + ((h * S + s) * kChunks + chunk) * kChunkFloats + q * (8 * 128) + lane * 4;
     };
-    if (un.split > 0) {
-        float* mine = part(un.split);
+    auto owned = [&](int c) { return (c >> 5) % S == me; };
+    // 1. the chunks this part does not own go to the workspace
+    int mine = 0;  // chunks of this warpgroup's half that this part owns
 #pragma unroll 1
-        for (int c = c_begin; c < c_end; c += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c, r);
-            tmem_ld_wait();
-            if (c + 32 >= c_end) release();
-            float* rc = mine + (c >> 5) * kChunkFloats;
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-                st_global_v4(rc + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+    for (int c = c_begin; c < c_end; c += 32) {
+        if (owned(c)) {
+            ++mine;
+            continue;
         }
-        __threadfence();  // the partial is visible before it is counted
-        if (!epi_sync()) return false;
-        if (etid == 0) red_release_gpu_add(p.counters + h, 1);
-        return true;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c, r);
+        tmem_ld_wait();
+        float* dst = part(me, c >> 5);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            st_global_v4(dst + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
     }
-    if (etid == 0) *flag = wait_flag_bounded(p.counters + h, un.nsplit - 1, ctl) ? 1 : 0;
+    if (mine == 0) release();
+    __threadfence();  // the partials are visible before they are counted
+    if (!epi_sync()) return false;
+    if (etid == 0) {
+        red_release_gpu_add(p.counters + h, 1);
+        *flag = wait_count_bounded(p.counters + h, S, ctl) ? 1 : 0;
+    }
     if (!epi_sync()) return false;
     if (!*flag) return false;
     __threadfence();
-    // Items (chunk, part s = 1..S-1) in order; two items' loads are in
-    // flight ahead of the one being added.
-    const int nparts = un.nsplit - 1;
-    const int nitems = ((c_end - c_begin) >> 5) * nparts;
+    // 2. the owned chunks: items (owned chunk, part s != me) in order, two
+    // items' loads in flight ahead of the one being added; this part's own
+    // term is read from tensor memory at its place in the order
+    const int nothers = S - 1;
+    const int nitems = mine * nothers;
+    auto item = [&](int i, int& c, int& s) {
+        const int k = i / nothers, j = i - k * nothers;
+        // the k-th owned chunk of [c_begin, c_end): chunks are owned every S
+        const int first = ((c_begin >> 5) + ((me - (c_begin >> 5)) % S + S) % S);
+        c = (first + k * S) << 5;
+        s = j < me ? j : j + 1;
+    };
     auto fetch = [&](int i, float4 (&dst)[8]) {
         if (i < nitems) {
-            const int c = c_begin + (i / nparts) * 32, s = i % nparts + 1;
-            const float* rc = part(s) + (c >> 5) * kChunkFloats;
+            int c, s;
+            item(i, c, s);
+            const float* src = part(s, c >> 5);
 #pragma unroll
-            for (int v = 0; v < 8; ++v) dst[v] = ld_global_cg_f4(rc + v * 128);
+            for (int v = 0; v < 8; ++v) dst[v] = ld_global_cg_f4(src + v * 128);
         }
     };
     float acc[32];
-    auto consume = [&](int i, const float4 (&src)[8]) {
-        const int c = c_begin + (i / nparts) * 32, s = i % nparts + 1;
-        if (s == 1) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c, r);
-            tmem_ld_wait();
-            if (c + 32 >= c_end) release();
-            // the sum starts from a cleared (+0) accumulator
+    auto add_own = [&](int c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c, r);
+        tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(0.0f, __uint_as_float(r[j]));
+        for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(acc[j], __uint_as_float(r[j]));
+    };
+    int done_chunks = 0;
+    auto consume = [&](int i, const float4 (&src)[8]) {
+        int c, s;
+        item(i, c, s);
+        if (s == (me == 0 ? 1 : 0)) {  // the chunk's first term: the sum starts from +0
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+            if (me == 0) add_own(c);
+        }
+        if (s == me + 1) {  // this part's term comes right before p_{me+1}
+            if (me != 0) add_own(c);
         }
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -300,7 +326,9 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
             acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], src[v].z);
             acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], src[v].w);
         }
-        if (s == nparts) {
+        if (s == S - 1 || (me == S - 1 && s == S - 2)) {  // the chunk's last stored term
+            if (me == S - 1) add_own(c);
+            if (++done_chunks == mine) release();  // every accumulator read of this thread is done
             uint32_t r[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
@@ -319,9 +347,12 @@ __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMa
             fetch(i + 3, pb);
         }
     }
-    if (etid == 0) p.counters[h] = 0;  // ready for the next launch
+    // 3. count this part out; the last of the S resets the counter for the
+    // next launch (2 S counts in all)
+    if (!epi_sync()) return false;
+    if (etid == 0 && atom_acq_rel_gpu_add(p.counters + h, 1) == 2 * S - 1) p.counters[h] = 0;
     // no thread may still be reading `flag` when the next unit rewrites it
-    return epi_sync();
+    return true;
 }
 
 // TMA loads of K-slice kb into a ring slot: A rows [row, row + 128) at

@@ -8,7 +8,8 @@
 //             twice as many 8-bit MACs, so the same cycles per slice),
 //     load  = (A slice + B slice bytes) / kL2BytesPerCycle;
 //   * a CTA runs ceil(units / grid) units back to back (wave quantisation);
-//   * a split tile adds S - 1 hand-overs of an fp32 running sum;
+//   * a split tile adds the reduction: every part writes (S - 1) / S of its
+//     fp32 partial and reads as much of the others';
 //   * the whole job can go no faster than its HBM traffic allows.
 // The model only ranks candidates; the tile widths it picks are the
 // measured-best ones on the shapes this library is tuned for.
@@ -33,7 +34,7 @@ constexpr int64_t kEpiWarps = 8;  // epilogue warps, each staging two 32 x 32 ou
 constexpr double kMacsPerCycle = 4096.0;
 constexpr double kL2BytesPerCycle = 72.0;     // operand feed per SM (measured ballpark)
 constexpr double kHbmBytesPerCycle = 3500.0;  // whole GPU (model)
-constexpr double kReduceBytesPerCycle = 32.0; // split-K partial reads per SM (measured ballpark)
+constexpr double kReduceBytesPerCycle = 14.0; // split-K partial writes + reads per SM (measured)
 constexpr double kUnitOverhead = 600.0;       // pipeline fill / drain per unit (model)
 constexpr int kMaxSplits = 32;
 constexpr int kDefaultTimeoutMs = 1000;
@@ -49,6 +50,19 @@ bool dtype_pair_ok(int din, int dout) {
 int64_t out_bytes(int dout) { return dout == TSGEMM_F32 ? 4 : 2; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// True when the S parts of some split unit fall into two consecutive rounds
+// of the static schedule (units u run in round u / slots).  That is
+// correct, but the parts in the earlier round then wait for a whole
+// mainloop of the later one, so the planner does not choose it.
+bool parts_straddle(int64_t full, int64_t split_tiles, int splits, int64_t slots) {
+    if (splits <= 1) return false;
+    for (int64_t t = 0; t < split_tiles; ++t) {
+        const int64_t first = full + t * splits;
+        if (first / slots != (first + splits - 1) / slots) return true;
+    }
+    return false;
+}
 
 struct Estimate {
     double cycles;
@@ -82,9 +96,11 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, in
     double bytes = static_cast<double>(in_bytes(din)) * (M * K + K * N) +
                    static_cast<double>(out_bytes(dout)) * M * N;
     if (splits > 1 && split_tiles > 0) {
-        // parts 1..S-1 write an fp32 partial of their tile half; part 0
-        // reads the S - 1 partials and adds them
-        compute += splits * static_cast<double>(kBM) * bn * 4.0 / kReduceBytesPerCycle;
+        // each part writes the (S - 1) / S of its fp32 partial it does not
+        // own and reads the others' partials of the chunks it owns
+        // (in every round of split units)
+        compute += split_rounds * 2.0 * (splits - 1) / splits * static_cast<double>(kBM) * bn * 4.0 /
+                   kReduceBytesPerCycle;
         const double ws = 2.0 * 4.0 * (splits - 1) * static_cast<double>(split_tiles) * bm * bn * cn;
         bytes += ws;
     }
@@ -193,6 +209,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                 }
                 for (int64_t st : options) {
                     if (st < 0 || st > tiles) continue;
+                    if (!f.splits && parts_straddle(tiles - st, st, s, slots)) continue;
                     const Estimate e = estimate(M, N, K, dtype_in, dtype_out, bm, bn, cn, s, st, num_sms);
                     // strict improvement required: ties keep the earlier candidate
                     if (best_bn == 0 || e.cycles < best * 0.999) {
@@ -230,8 +247,9 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     // part 0 of a split tile waits for parts 1..S-1, which must run on other
     // CTAs (pairs) at the same time: S may not exceed the grid's slots
     if (c.split_tiles > 0 && best_s > c.grid / ctas_per_slot) return TSGEMM_ERR_UNSUPPORTED;
-    // S - 1 fp32 partials per split unit (cn tiles)
-    c.workspace_bytes = c.split_tiles * (best_s - 1) * best_bm * static_cast<int64_t>(best_bn) * best_cn * 4;
+    // S fp32 partial slots per split unit (cn tiles); each part fills the
+    // chunks it does not own
+    c.workspace_bytes = c.split_tiles * best_s * best_bm * static_cast<int64_t>(best_bn) * best_cn * 4;
     c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
     c.debug_flags = f.debug_flags;
     *out = c;

@@ -173,15 +173,22 @@ __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Wait until the global flag *p equals `value` (it is set by another CTA),
-// for at most ctl.timeout_ns; false when the limit expired or the CTA is
-// aborting.
-__device__ __forceinline__ bool wait_flag_bounded(const int* p, int value, const WaitCtl& ctl) {
-    if (ld_acquire_gpu(p) == value) return true;
+// *p += v at GPU scope, acquire + release; returns the previous value.
+__device__ __forceinline__ int atom_acq_rel_gpu_add(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Wait until the global counter *p reaches at least `value` (other CTAs
+// count it up), for at most ctl.timeout_ns; false when the limit expired or
+// the CTA is aborting.
+__device__ __forceinline__ bool wait_count_bounded(const int* p, int value, const WaitCtl& ctl) {
+    if (ld_acquire_gpu(p) >= value) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         __nanosleep(32);
-        if (ld_acquire_gpu(p) == value) return true;
+        if (ld_acquire_gpu(p) >= value) return true;
         if (*ctl.abort) return false;
         if (globaltimer() - t0 > ctl.timeout_ns) {
             record_timeout(ctl);

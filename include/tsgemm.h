@@ -101,7 +101,8 @@ typedef struct {
     int32_t grid;         /* CTAs launched (persistent) */
     int64_t units;        /* work units = whole tiles + split_tiles * splits */
     int64_t workspace_bytes; /* split-K partials owned by the plan:
-                                split_tiles * (splits - 1) * block_m * block_n * 4 bytes */
+                                split_tiles * splits * block_m * block_n *
+                                cluster_n * 4 bytes */
     int32_t timeout_ms;   /* limit of every device-side wait */
     int32_t debug_flags;  /* tests only: TSGEMM_DEBUG_* */
     int64_t split_tiles;  /* work units split into `splits` K parts: the last
@@ -194,9 +195,9 @@ TSGEMM_API const char* tsgemm_status_string(tsgemm_status_t s);
  * on `stream` before the launch).
  *
  * Limits: at most TSGEMM_NOALLOC_MAX_TILES output tiles and at most
- * TSGEMM_NOALLOC_WS_BYTES of fp32 partials (split tiles * (S - 1) * 128 *
- * block_n * 4 bytes); larger problems return TSGEMM_ERR_SCRATCH_LIMIT before
- * anything is enqueued.
+ * TSGEMM_NOALLOC_WS_BYTES of fp32 partials (split tiles * S * 128 * block_n *
+ * 4 bytes); larger problems return TSGEMM_ERR_SCRATCH_LIMIT before anything
+ * is enqueued.
  *
  * Every call uses the same scratch array, which keeps the previous call's
  * contents; each call clears the tile counters it needs on `stream` before

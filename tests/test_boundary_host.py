@@ -104,7 +104,7 @@ def test_planner_invariants(ts, shape, sms):
     assert 1 <= c["splits"] <= _ceil(K, 64)
     per = bm // 128  # CTAs per unit
     assert c["grid"] % per == 0 and 1 <= c["grid"] <= per * min(sms // per, c["units"])
-    assert c["workspace_bytes"] == st * (c["splits"] - 1) * bm * bn * 4
+    assert c["workspace_bytes"] == st * c["splits"] * bm * bn * 4
     stage = 128 * 64 * 2 + (bn // per) * 64 * 2
     staging = 8 * 2 * 32 * 32 * (4 if dout == "f32" else 2)  # 8 epilogue warps x 2 blocks
     smem = 1024 + c["stages"] * stage + staging + 8 * (2 * c["stages"] + 6) + 16
@@ -239,7 +239,7 @@ def test_cluster_n_rules(ts):
     assert cfg["grid"] % 4 == 0 and cfg["grid"] <= 152
     # a unit is two tiles: 16 tile rows x 8 column pairs
     assert cfg["units"] == 16 * 8 + cfg["split_tiles"] * (cfg["splits"] - 1)
-    assert cfg["workspace_bytes"] == cfg["split_tiles"] * (cfg["splits"] - 1) * 256 * 512 * 4
+    assert cfg["workspace_bytes"] == cfg["split_tiles"] * cfg["splits"] * 256 * 512 * 4
     for force in [dict(cluster_n=2, block_m=128), dict(cluster_n=2, block_n=128), dict(cluster_n=3)]:
         with pytest.raises(ts.TsgemmError) as e:
             ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, **force)
