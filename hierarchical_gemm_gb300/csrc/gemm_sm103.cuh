@@ -30,8 +30,10 @@
 //   * the K split with a reduction (TileScale README, "Example of GEMM",
 //     warpgroups split along K and reduce): a work unit may cover a K range
 //     of a tile (all tiles, or only those of the last, partial wave);
-//     partial tiles go to an fp32 workspace and the CTA that finishes a
-//     tile last adds the partials in split order 0..S-1.
+//     partial tiles go to an fp32 workspace and are added in split order;
+//   * stream-K: the K slices of the schedule's last tiles are spread evenly
+//     over all CTAs, so every CTA ends at the same time; a tile cut between
+//     CTAs is finished by the CTA that holds its first K slices.
 //
 // Every wait is bounded in time (see WaitCtl); a CTA that gives up records a
 // timeout in the status word, lets its in-flight copies and MMAs finish,
@@ -83,7 +85,9 @@ struct GemmParams {
     int32_t stages;
     int32_t debug_flags;
     int64_t full_tiles;   // tiles [0, full_tiles) of the schedule are not split
-    int64_t units;        // full_tiles + (tiles - full_tiles) * S
+    int64_t units;        // full_tiles + (tiles - full_tiles) * S (split mode)
+    int64_t sk_tiles;     // stream-K mode: the last sk_tiles tiles (0: split mode)
+    int64_t sk_work;      // sk_tiles * kblocks K slices, spread over the slots
     uint32_t idesc;       // tcgen05 instruction descriptor
     uint32_t pad_;
     void* C;
@@ -93,21 +97,36 @@ struct GemmParams {
     uint64_t timeout_ns;
 };
 
-// One work unit: a whole tile, or one of the S K-parts of a split tile.
+// One work unit: a whole tile, one of the S K-parts of a split tile, or a
+// stream-K segment of a tile.
 struct Unit {
     int tm, tn;      // tile row and column
-    int split;       // K part of this unit
-    int nsplit;      // 1: the whole tile
+    int split;       // K part of this unit (split mode)
+    int nsplit;      // 1: the whole tile; stream-K owner: 1 + contributors
     int kb0, kb1;    // K-slices [kb0, kb1)
-    int64_t slot;    // index of the tile among the split tiles (nsplit > 1)
+    int64_t slot;    // index of the tile among the split (or stream-K) tiles
+    int sk;          // 0: not stream-K; 1: a later K range of a tile, whose
+                     // partial another CTA adds; 2: the tile's first K range,
+                     // whose CTA adds the others' partials and stores C
 };
 
-// Work unit u of the static schedule.  The first full_tiles units are whole
-// tiles; after them come the split tiles, their S parts adjacent so that
-// they run at the same time (the split tiles are the schedule's last, so
-// splitting fills the last, partial wave of tiles).  Linear tiles are
-// rastered in groups of `group_m` tile rows so that concurrently running
-// CTAs share A and B panels in L2.
+// Tile row and column of linear tile `tile`: tiles are rastered in groups
+// of `group_m` tile rows so that concurrently running CTAs share A and B
+// panels in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int64_t tile, int& tm, int& tn) {
+    const int64_t span = static_cast<int64_t>(p.group_m) * p.tiles_n;
+    const int64_t group = tile / span;
+    const int first_m = static_cast<int>(group * p.group_m);
+    const int gm = min(p.tiles_m - first_m, p.group_m);
+    const int64_t rr = tile - group * span;
+    tm = first_m + static_cast<int>(rr % gm);
+    tn = static_cast<int>(rr / gm);
+}
+
+// Work unit u of the static schedule (split mode).  The first full_tiles
+// units are whole tiles; after them come the split tiles, their S parts
+// adjacent so that they run at the same time (the split tiles are the
+// schedule's last, so splitting fills the last, partial wave of tiles).
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int64_t u) {
     Unit r;
     int64_t tile;
@@ -124,16 +143,67 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int64_t u) {
         r.nsplit = p.splits;
         r.slot = t;
     }
-    const int64_t span = static_cast<int64_t>(p.group_m) * p.tiles_n;
-    const int64_t group = tile / span;
-    const int first_m = static_cast<int>(group * p.group_m);
-    const int gm = min(p.tiles_m - first_m, p.group_m);
-    const int64_t rr = tile - group * span;
-    r.tm = first_m + static_cast<int>(rr % gm);
-    r.tn = static_cast<int>(rr / gm);
+    tile_coords(p, tile, r.tm, r.tn);
     r.kb0 = static_cast<int>(static_cast<int64_t>(r.split) * p.kblocks / r.nsplit);
     r.kb1 = static_cast<int>(static_cast<int64_t>(r.split + 1) * p.kblocks / r.nsplit);
+    r.sk = 0;
     return r;
+}
+
+// Stream-K mode: the sk_work K slices of the last sk_tiles tiles (tile by
+// tile, k ascending) are cut into G equal ranges; slot g takes slices
+// [g W / G, (g + 1) W / G).  sk_slot_of(x) is the slot whose range holds
+// slice x.
+__device__ __forceinline__ int64_t sk_begin(const GemmParams& p, int64_t g, int64_t G) { return g * p.sk_work / G; }
+__device__ __forceinline__ int64_t sk_slot_of(const GemmParams& p, int64_t x, int64_t G) {
+    return ((x + 1) * G - 1) / p.sk_work;
+}
+
+// The j-th work unit of slot g of the G slots (CTAs, or CTA clusters);
+// false past the slot's last.  Split mode: units g, g + G, g + 2G, ...
+// Stream-K mode: the slot's whole tiles (g, g + G, ... below full_tiles),
+// then the segments of its stream-K range, one per tile it touches.  A
+// range that starts inside a tile contributes that tile's later K slices
+// (sk = 1); one that ends inside a tile holds its first K slices (sk = 2)
+// and is the slot's last unit.
+__device__ __forceinline__ bool unit_at(const GemmParams& p, int64_t g, int64_t G, int64_t j, Unit& r) {
+    if (p.sk_tiles == 0) {
+        const int64_t u = g + j * G;
+        if (u >= p.units) return false;
+        r = decode_unit(p, u);
+        return true;
+    }
+    r.split = 0;
+    r.nsplit = 1;
+    r.slot = -1;
+    r.sk = 0;
+    const int64_t ndp = g < p.full_tiles ? (p.full_tiles - 1 - g) / G + 1 : 0;
+    if (j < ndp) {
+        tile_coords(p, g + j * G, r.tm, r.tn);
+        r.kb0 = 0;
+        r.kb1 = p.kblocks;
+        return true;
+    }
+    const int64_t kb = p.kblocks;
+    const int64_t a = sk_begin(p, g, G), b = sk_begin(p, g + 1, G);
+    const int64_t jj = j - ndp;
+    const int64_t start = jj == 0 ? a : (a / kb + jj) * kb;
+    if (start >= b) return false;
+    const int64_t t = start / kb;
+    const int64_t end = min(b, (t + 1) * kb);
+    tile_coords(p, p.full_tiles + t, r.tm, r.tn);
+    r.kb0 = static_cast<int>(start - t * kb);
+    r.kb1 = static_cast<int>(end - t * kb);
+    if (r.kb0 > 0) {
+        r.sk = 1;
+        r.slot = t;
+        r.nsplit = 2;
+    } else if (r.kb1 < kb) {
+        r.sk = 2;
+        r.slot = t;
+        r.nsplit = 1 + static_cast<int>(sk_slot_of(p, (t + 1) * kb - 1, G) - g);
+    }
+    return true;
 }
 
 // Shared-memory staging of the output: each epilogue warp owns two buffers
@@ -219,17 +289,139 @@ struct CStager {
 //     keeps S within the grid, and since the schedule is static and every
 //     CTA walks its units in order, parts that straddle two rounds still
 //     meet.
-// `h` indexes the workspace tile and counter of this 128-row half;
+//   * Stream-K: a segment holding a later K range of a tile (sk = 1) writes
+//     its partial to its slot's workspace and counts itself in.  The
+//     segment holding the tile's first K range (sk = 2) waits for the
+//     nsplit - 1 others, adds their partials after its own in K order and
+//     stores C; it is its CTA's last unit, so the operand ring is idle and,
+//     when the partials fit, they are bulk-copied into it and read from
+//     shared memory.
+// `h` indexes the counter (and, in split mode, the workspace tile) of this
+// 128-row half; `aux` holds the stream-K workspace slots and the ring;
 // `epi_sync` is the epilogue's bounded barrier (both warpgroups) and
 // `release` hands the accumulator back to the MMA issuer.  Returns false if
 // the CTA is aborting.
+struct EpiAux {
+    int64_t wsi;          // stream-K: this slot's workspace index (128 x BN fp32 each)
+    int64_t wstride;      // stream-K: workspace index step from one slot to the next
+    uint32_t ring;        // shared-memory operand ring
+    uint32_t ring_bytes;
+    uint32_t red_bar;     // barrier of the bulk copies into the ring
+};
+
+template <int BN, int kOut, class Sync, class Release>
+__device__ __forceinline__ bool drain_sk_owner(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
+                                               const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
+                                               const EpiAux& aux, int c_begin, int etid, volatile int* flag,
+                                               const WaitCtl& ctl, Sync&& epi_sync, Release&& release) {
+    const int col0 = un.tn * BN;
+    const int c_end = c_begin + BN / 2;
+    const int m = un.nsplit - 1;  // contributors, in K order: slots g + 1 .. g + m
+    const int q = row_local >> 5, lane = row_local & 31;
+    constexpr int kChunkFloats = 4 * 8 * 128;
+    constexpr uint32_t kHalfBytes = kBM * BN * 4;
+    auto src = [&](int s, int c) -> const float* {  // partial of contributor s (1..m), chunk of column c
+        return p.ws + (aux.wsi + s * aux.wstride) * (kBM * BN) + (c >> 5) * kChunkFloats;
+    };
+    if (etid == 0) *flag = wait_count_bounded(p.counters + h, m, ctl) ? 1 : 0;
+    if (!epi_sync()) return false;
+    if (!*flag) return false;
+    __threadfence();
+    const bool staged = static_cast<uint32_t>(m) * kHalfBytes <= aux.ring_bytes;
+    if (staged) {
+        // contributor s's partial lands at ring + (s - 1) * kHalfBytes, in
+        // the workspace's order; every thread reads its own 512 bytes of a
+        // chunk as 8 conflict-free 16-byte loads
+        if (etid == 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(aux.red_bar, static_cast<uint32_t>(m) * kHalfBytes);
+            for (int s = 1; s <= m; ++s)
+                for (int c = 0; c < BN; c += 32)
+                    bulk_load(aux.ring + (s - 1) * kHalfBytes + (c >> 5) * kChunkFloats * 4, src(s, c),
+                              kChunkFloats * 4, aux.red_bar);
+        }
+        int good = 1;
+        if (lane == 0) good = wait_bounded(aux.red_bar, 0u, ctl) ? 1 : 0;
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+            // let the copies land before the CTA can exit
+            if (lane == 0) wait_bounded(aux.red_bar, 0u, ctl, false);
+            __syncwarp();
+            return false;
+        }
+    }
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 32) {
+        float acc[32];
+        {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c, r);
+            tmem_ld_wait();
+            if (c + 32 >= c_end) release();
+            // the sum starts from a cleared (+0) accumulator
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(0.0f, __uint_as_float(r[j]));
+        }
+#pragma unroll 1
+        for (int s = 1; s <= m; ++s) {
+            float4 v4[8];
+            if (staged) {
+                const uint32_t a = aux.ring + (s - 1) * kHalfBytes + (c >> 5) * kChunkFloats * 4 + q * 4096 + lane * 16;
+#pragma unroll
+                for (int v = 0; v < 8; ++v) v4[v] = ld_shared_f4(a + v * 512);
+            } else {
+                const float* g = src(s, c) + q * (8 * 128) + lane * 4;
+#pragma unroll
+                for (int v = 0; v < 8; ++v) v4[v] = ld_global_cg_f4(g + v * 128);
+            }
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                acc[4 * v] = __fadd_rn(acc[4 * v], v4[v].x);
+                acc[4 * v + 1] = __fadd_rn(acc[4 * v + 1], v4[v].y);
+                acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], v4[v].z);
+                acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], v4[v].w);
+            }
+        }
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
+        out.put(p, tmC, row0, col0 + c, r);
+    }
+    if (!epi_sync()) return false;
+    if (etid == 0) p.counters[h] = 0;  // ready for the next launch
+    return true;
+}
+
 template <int BN, int kOut, class Sync, class Release>
 __device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
                                            const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
-                                           int c_begin, int etid, volatile int* flag, const WaitCtl& ctl,
-                                           Sync&& epi_sync, Release&& release) {
+                                           const EpiAux& aux, int c_begin, int etid, volatile int* flag,
+                                           const WaitCtl& ctl, Sync&& epi_sync, Release&& release) {
     const int col0 = un.tn * BN;
     const int c_end = c_begin + BN / 2;  // this warpgroup's half of the columns
+    if (un.sk == 2)
+        return drain_sk_owner<BN, kOut>(p, tmC, out, un, tbase, row0, row_local, h, aux, c_begin, etid, flag, ctl,
+                                        epi_sync, release);
+    if (un.sk == 1) {
+        // a later K range of a stream-K tile: its partial, for the owner
+        const int q = row_local >> 5, lane = row_local & 31;
+        float* mine = p.ws + aux.wsi * (kBM * BN) + q * (8 * 128) + lane * 4;
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c, r);
+            tmem_ld_wait();
+            if (c + 32 >= c_end) release();
+            float* dst = mine + (c >> 5) * (4 * 8 * 128);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                st_global_v4(dst + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        }
+        __threadfence();  // the partial is visible before it is counted
+        if (!epi_sync()) return false;
+        if (etid == 0) red_release_gpu_add(p.counters + h, 1);
+        return true;
+    }
     if (un.nsplit == 1) {
 #pragma unroll 1
         for (int c = c_begin; c < c_end; c += 32) {
@@ -423,7 +615,7 @@ struct TileShape {
 template <int BN, int kOut>
 __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
     return 1024u /* alignment slack */ + stages * TileShape<BN>::kStageBytes + epi_smem_bytes<kOut>() +
-           8u * (2 * stages + 6) /* barriers */ + 16u /* tmem holder, flags */;
+           8u * (2 * stages + 7) /* barriers */ + 16u /* tmem holder, flags */;
 }
 
 template <int BN, int kOut, int kLayout, bool kF8 = false>
@@ -445,7 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     const uint32_t epi_bar = bars + 8u * (2 * S + 5);
-    uint8_t* misc = base_ptr + S * TS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 6);
+    const uint32_t red_bar = bars + 8u * (2 * S + 6);
+    uint8_t* misc = base_ptr + S * TS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 7);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
@@ -464,6 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(epi_bar, kEpiWarps);
+        mbar_init(red_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -487,8 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t outstanding = 0, out_parity = 0;  // loads issued, per slot
             bool skip = (p.debug_flags & 1) && blockIdx.x == 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                const Unit un = decode_unit(p, u);
+            for (int64_t j = 0; ok; ++j) {
+                Unit un;
+                if (!unit_at(p, blockIdx.x, gridDim.x, j, un)) break;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, ctl)) {
                         ok = false;
@@ -523,8 +718,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                const Unit un = decode_unit(p, u);
+            for (int64_t j = 0; ok; ++j) {
+                Unit un;
+                if (!unit_at(p, blockIdx.x, gridDim.x, j, un)) break;
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, ctl)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * TS::kAccCols;
@@ -580,9 +776,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             epi_phase ^= 1u;
             return good != 0;
         };
-        for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const Unit un = decode_unit(p, u);
-            const int tm = un.tm, tn = un.tn;
+        const EpiAux aux{static_cast<int64_t>(blockIdx.x), 1, base, static_cast<uint32_t>(S) * TS::kStageBytes,
+                         red_bar};
+        for (int64_t j = 0;; ++j) {
+            Unit un;
+            if (!unit_at(p, blockIdx.x, gridDim.x, j, un)) break;
+            const int tm = un.tm;
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, ctl) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -595,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(tempty_bar(acc));
             };
-            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, c_begin, etid,
+            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, aux, c_begin, etid,
                                       last_flag, ctl, epi_sync, release))
                 break;
             if (++acc == 2) {

@@ -48,7 +48,7 @@ struct PairShape {
 
 template <int BN, int kOut>
 __host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
-    return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 6) + 16u;
+    return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 7) + 16u;
 }
 
 // The loads of one K-slice by a CTA of a two-pair cluster: its own B
@@ -102,7 +102,8 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     const uint32_t epi_bar = bars + 8u * (2 * S + 5);
-    uint8_t* misc = base_ptr + S * PS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 6);
+    const uint32_t red_bar = bars + 8u * (2 * S + 6);
+    uint8_t* misc = base_ptr + S * PS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 7);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
@@ -126,6 +127,7 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
         }
         mbar_init(drain_bar, 1);
         mbar_init(epi_bar, kEpiWarps);
+        mbar_init(red_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -157,8 +159,9 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
             // unannounced, so the MMA issuer's bounded wait runs out
             bool skip = (p.debug_flags & 1) && cluster_id == 0 && leader;
             bool ok = true;
-            for (int64_t u = cluster_id; ok && u < p.units; u += nclusters) {
-                const Unit un = decode_unit(p, u);
+            for (int64_t j = 0; ok; ++j) {
+                Unit un;
+                if (!unit_at(p, cluster_id, nclusters, j, un)) break;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, ctl)) {
                         ok = false;
@@ -213,8 +216,9 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int64_t u = cluster_id; ok && u < p.units; u += nclusters) {
-                const Unit un = decode_unit(p, u);
+            for (int64_t j = 0; ok; ++j) {
+                Unit un;
+                if (!unit_at(p, cluster_id, nclusters, j, un)) break;
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, ctl)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * PS::kAccCols;
@@ -282,8 +286,11 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
                     mbar_arrive_cluster(tempty_bar(a), lead_rank);
             }
         };
-        for (int64_t u = cluster_id; u < p.units; u += nclusters) {
-            Unit un = decode_unit(p, u);
+        const EpiAux aux{(cluster_id * kPairs + pair) * 2 + half, 2 * kPairs, base,
+                         static_cast<uint32_t>(S) * PS::kStageBytes, red_bar};
+        for (int64_t j = 0;; ++j) {
+            Unit un;
+            if (!unit_at(p, cluster_id, nclusters, j, un)) break;
             un.tn = un.tn * kPairs + static_cast<int>(pair);  // this pair's tile column
             const int tm = un.tm;
             int ok = 1;
@@ -297,7 +304,7 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
             // workspace tile and counter of this CTA's 128-row half
             const int64_t wh = (un.slot * kPairs + pair) * 2 + half;
             const int a_now = acc;
-            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, wh, c_begin, etid, last_flag,
+            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, wh, aux, c_begin, etid, last_flag,
                                       ctl, epi_sync, [&]() { release_acc(a_now); }))
                 break;
             if (++acc == 2) {

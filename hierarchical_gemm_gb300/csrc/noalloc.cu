@@ -147,6 +147,7 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     tsgemm_config_t force{};
     force.splits = splits;
     force.block_m = 128;  // the one-SM kernel
+    force.stream_k_tiles = -1;  // split mode only
     tsgemm_config_t cfg{};
     st = tsg::choose_config(M, N, K, dtype_in, dtype_out, TSGEMM_LAYOUT_RRR, ds->num_sms, &force, &cfg);
     if (st != TSGEMM_OK) return st;

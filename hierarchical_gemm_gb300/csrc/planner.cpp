@@ -36,6 +36,9 @@ constexpr double kL2BytesPerCycle = 72.0;     // operand feed per SM (measured b
 constexpr double kHbmBytesPerCycle = 3500.0;  // whole GPU (model)
 constexpr double kReduceBytesPerCycle = 14.0; // split-K partial writes + reads per SM (measured)
 constexpr double kUnitOverhead = 600.0;       // pipeline fill / drain per unit (model)
+constexpr bool kAutoStreamK = true;          // the planner proposes stream-K itself
+constexpr double kFixupCycles = 11000.0;      // stream-K: segment hand-overs and the final add (measured)
+constexpr double kStagedBytesPerCycle = 64.0; // stream-K: partials bulk-copied into the idle ring
 constexpr int kMaxSplits = 32;
 constexpr int kDefaultTimeoutMs = 1000;
 
@@ -108,6 +111,40 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, in
     return {std::max(compute, hbm) + 0.05 * compute, compute};
 }
 
+// Stream-K: the last `sk` tiles' K slices spread evenly over the slots,
+// after ceil((tiles - sk) / slots) rounds of whole tiles.  A tile cut
+// between slots costs its later parts a partial write (mostly hidden
+// behind their next mainloop) and its first part's CTA, at the very end, a
+// copy of the partials into the idle ring and the final add.
+Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int cn, int64_t sk,
+                     int num_sms) {
+    const int64_t tiles = ceil_div(M, bm) * ceil_div(ceil_div(N, bn), cn);
+    const int64_t slots = std::max(1, num_sms / ((bm / kBM) * cn));
+    const int64_t kblocks = ceil_div(K, slice_k(din));
+    const double mma = kBM * bn * static_cast<double>(kBK) / kMacsPerCycle;
+    const double b_bytes = (bm == 256 ? bn / 2 : bn) * kBK * 2.0;
+    const double load = (kBM * kBK * 2.0 / cn + b_bytes) / kL2BytesPerCycle;
+    const double per_kb = std::max(mma, load);
+    const double dp_rounds = static_cast<double>(ceil_div(tiles - sk, slots));
+    const double sk_slices = std::ceil(static_cast<double>(sk) * kblocks / slots);
+    // contributors per owner; their partials fit the idle ring when each
+    // is no larger than the ring's share, else they are read from global
+    // memory at the split-K rate
+    const double owners_parts = std::ceil(kblocks / std::max(1.0, sk_slices));
+    const double half_bytes = kBM * bn * 4.0;
+    const double ring_bytes = static_cast<double>(max_stages_for(bm, bn, dout)) *
+                              (kBM * kBK * 2.0 + (bm == 256 ? bn / 2 : bn) * kBK * 2.0);
+    const double fetch = owners_parts * half_bytes <= ring_bytes ? owners_parts * half_bytes / kStagedBytesPerCycle
+                                                                 : owners_parts * half_bytes / kReduceBytesPerCycle;
+    double compute = dp_rounds * (kblocks * per_kb + kUnitOverhead) + sk_slices * per_kb + 2 * kUnitOverhead +
+                     kFixupCycles + fetch;
+    double bytes = static_cast<double>(in_bytes(din)) * (M * K + K * N) +
+                   static_cast<double>(out_bytes(dout)) * M * N +
+                   2.0 * 4.0 * static_cast<double>(slots) * bm * bn * cn;
+    const double hbm = bytes / kHbmBytesPerCycle;
+    return {std::max(compute, hbm) + 0.05 * compute, compute};
+}
+
 }  // namespace
 
 int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages) {
@@ -115,7 +152,7 @@ int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages) {
     const int64_t stage = static_cast<int64_t>(kBM) * kBK * 2 + b_cols * kBK * 2;
     // output staging: 8 epilogue warps x 2 buffers of one 32 x 32 block
     const int64_t staging = kEpiWarps * 2 * 32 * 32 * out_bytes(dtype_out);
-    return 1024 + stages * stage + staging + 8 * (2 * stages + 6) + 16;
+    return 1024 + stages * stage + staging + 8 * (2 * stages + 7) + 16;
 }
 
 int max_stages_for(int block_m, int block_n, int dtype_out) {
@@ -167,6 +204,8 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     if (f.cluster_n < 0 || f.cluster_n > 2) return TSGEMM_ERR_UNSUPPORTED;
     if (f.cluster_n == 2 && (f.block_m == 128 || (f.block_n != 0 && f.block_n != 256) || num_sms < 4))
         return TSGEMM_ERR_UNSUPPORTED;
+    if (f.stream_k_tiles < -1) return TSGEMM_ERR_INVALID_ARG;
+    if (f.stream_k_tiles > 0 && (f.splits > 1 || f.split_tiles > 0)) return TSGEMM_ERR_INVALID_ARG;
 
     const int64_t kblocks = ceil_div(K, slice_k(dtype_in));
     if (f.splits > kblocks || f.splits > 4096) return TSGEMM_ERR_UNSUPPORTED;
@@ -174,7 +213,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     // Candidate tile widths: never wider than N rounded up to 64.
     const int64_t n_pad = ceil_div(N, 64) * 64;
     int best_bm = 0, best_bn = 0, best_cn = 1, best_s = 0;
-    int64_t best_st = 0;
+    int64_t best_st = 0, best_sk = 0;
     double best = 0;
     const int bms[2] = {256, 128};  // pairs first: ties go to the pair
     const int bns[4] = {256, 192, 128, 64};
@@ -195,7 +234,34 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                                       : static_cast<int>(std::min<int64_t>(
                                             std::min<int64_t>(kMaxSplits, slots), std::max<int64_t>(1, kblocks / 4)));
             const int smin = f.splits ? f.splits : 1;
+            // stream-K: the tail wave, or the tail and one full wave before it
+            // (so that whole-tile rounds stay whole), or a forced count
+            if (f.stream_k_tiles != -1 && smin == 1 && !f.split_tiles) {
+                int64_t sk_opts[2] = {-1, -1};
+                if (f.stream_k_tiles > 0) {
+                    sk_opts[0] = f.stream_k_tiles;
+                } else if (kAutoStreamK && (tiles % slots != 0 || tiles < slots)) {
+                    sk_opts[0] = tiles % slots;
+                    if (tiles > slots) sk_opts[1] = tiles % slots + slots;
+                }
+                for (int64_t sk : sk_opts) {
+                    // every slot needs at least one K slice, so that the
+                    // slots sharing a tile are consecutive
+                    if (sk <= 0 || sk > tiles || sk * kblocks < slots) continue;
+                    const Estimate e = estimate_sk(M, N, K, dtype_in, dtype_out, bm, bn, cn, sk, num_sms);
+                    if (best_bn == 0 || e.cycles < best * 0.999) {
+                        best = e.cycles;
+                        best_bm = bm;
+                        best_bn = bn;
+                        best_cn = cn;
+                        best_s = 1;
+                        best_st = 0;
+                        best_sk = sk;
+                    }
+                }
+            }
             for (int s = smin; s <= smax; ++s) {
+                if (f.stream_k_tiles > 0) break;
                 // which tiles are split: none (s = 1), a forced count, every
                 // tile, or only the tiles of the last, partial wave
                 int64_t options[2] = {0, -1};
@@ -219,6 +285,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                         best_cn = cn;
                         best_s = s;
                         best_st = st;
+                        best_sk = 0;
                     }
                 }
             }
@@ -238,11 +305,30 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     c.cluster_n = best_cn;
     const int64_t tiles = ceil_div(M, best_bm) * ceil_div(ceil_div(N, best_bn), best_cn);
     c.split_tiles = best_s > 1 ? best_st : 0;
+    c.stream_k_tiles = best_sk;
     c.units = (tiles - c.split_tiles) + c.split_tiles * best_s;
     // a pair kernel launches two CTAs per unit slot, a two-pair cluster four
     const int64_t ctas_per_slot = (best_bm / kBM) * best_cn;
     int64_t slots = (f.grid ? f.grid : num_sms) / ctas_per_slot;
     if (slots < 1) return TSGEMM_ERR_UNSUPPORTED;
+    if (best_sk > 0) {
+        // every slot takes part in the stream-K ranges; units = whole tiles
+        // + stream-K segments (one per tile a slot's range touches)
+        const int64_t w = best_sk * kblocks;
+        int64_t segs = 0;
+        for (int64_t g = 0; g < slots; ++g) {
+            const int64_t a = g * w / slots, b = (g + 1) * w / slots;
+            if (b > a) segs += (b - 1) / kblocks - a / kblocks + 1;
+        }
+        c.units = tiles - best_sk + segs;
+        c.grid = static_cast<int32_t>(slots * ctas_per_slot);
+        // one fp32 partial slot per CTA half of each slot
+        c.workspace_bytes = slots * best_bm * static_cast<int64_t>(best_bn) * best_cn * 4;
+        c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
+        c.debug_flags = f.debug_flags;
+        *out = c;
+        return TSGEMM_OK;
+    }
     c.grid = static_cast<int32_t>(std::min<int64_t>(c.units, slots) * ctas_per_slot);
     // part 0 of a split tile waits for parts 1..S-1, which must run on other
     // CTAs (pairs) at the same time: S may not exceed the grid's slots

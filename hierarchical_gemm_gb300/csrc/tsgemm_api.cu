@@ -189,9 +189,10 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     p->device = dev;
     p->kernel = kern;
     p->smem = smem;
-    // split-K counters: one per 128-row half of each tile of a split unit
-    // (pairs reduce halves)
-    p->num_tiles = cfg.split_tiles * (cfg.block_m / 128) * cfg.cluster_n;
+    // split-K (stream-K) counters: one per 128-row half of each tile of a
+    // split (stream-K) unit (pairs reduce halves)
+    p->num_tiles = (cfg.stream_k_tiles > 0 ? cfg.stream_k_tiles : cfg.split_tiles) * (cfg.block_m / 128) *
+                   cfg.cluster_n;
 
     if (cudaMalloc(&p->status_d, sizeof(int)) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -203,7 +204,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
         plan_free(p);
         return TSGEMM_ERR_CUDA;
     }
-    if (cfg.splits > 1) {
+    if (cfg.splits > 1 || cfg.stream_k_tiles > 0) {
         if (cudaMalloc(&p->ws, static_cast<size_t>(cfg.workspace_bytes)) != cudaSuccess ||
             cudaMalloc(&p->counters, static_cast<size_t>(p->num_tiles) * sizeof(int)) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -231,7 +232,9 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.stages = cfg.stages;
     gp.debug_flags = cfg.debug_flags;
     gp.units = cfg.units;
-    gp.full_tiles = ((M + cfg.block_m - 1) / cfg.block_m) * gp.tiles_n - cfg.split_tiles;
+    gp.full_tiles = ((M + cfg.block_m - 1) / cfg.block_m) * gp.tiles_n - cfg.split_tiles - cfg.stream_k_tiles;
+    gp.sk_tiles = cfg.stream_k_tiles;
+    gp.sk_work = cfg.stream_k_tiles * gp.kblocks;
     gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n, layout);
     gp.C = nullptr;
     gp.ws = p->ws;

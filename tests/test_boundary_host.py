@@ -99,15 +99,22 @@ def test_planner_invariants(ts, shape, sms):
     tiles = _ceil(M, bm) * _ceil(N, bn)
     assert (bm, bn) in [(128, 64), (128, 128), (128, 192), (128, 256), (256, 128), (256, 256)]
     st = c["split_tiles"]
-    assert 0 <= st <= tiles and (st == 0) == (c["splits"] == 1)
-    assert c["units"] == (tiles - st) + st * c["splits"]
-    assert 1 <= c["splits"] <= _ceil(K, 64)
+    sk = c["stream_k_tiles"]
     per = bm // 128  # CTAs per unit
-    assert c["grid"] % per == 0 and 1 <= c["grid"] <= per * min(sms // per, c["units"])
-    assert c["workspace_bytes"] == st * c["splits"] * bm * bn * 4
+    assert 0 <= st <= tiles and (st == 0) == (c["splits"] == 1)
+    assert 1 <= c["splits"] <= _ceil(K, 64)
+    if sk:
+        # stream-K: every slot takes a share of the last sk tiles' K slices
+        assert c["splits"] == 1 and st == 0 and 0 < sk <= tiles
+        assert c["units"] >= tiles and c["grid"] == per * (sms // per)
+        assert c["workspace_bytes"] == (sms // per) * bm * bn * 4
+    else:
+        assert c["units"] == (tiles - st) + st * c["splits"]
+        assert c["grid"] % per == 0 and 1 <= c["grid"] <= per * min(sms // per, c["units"])
+        assert c["workspace_bytes"] == st * c["splits"] * bm * bn * 4
     stage = 128 * 64 * 2 + (bn // per) * 64 * 2
     staging = 8 * 2 * 32 * 32 * (4 if dout == "f32" else 2)  # 8 epilogue warps x 2 blocks
-    smem = 1024 + c["stages"] * stage + staging + 8 * (2 * c["stages"] + 6) + 16
+    smem = 1024 + c["stages"] * stage + staging + 8 * (2 * c["stages"] + 7) + 16
     assert smem <= 232448
     # the ring is as deep as the shared memory allows
     assert smem + stage > 232448 or c["stages"] == 16
@@ -234,7 +241,7 @@ def test_fp8_dtype_names(ts):
 # ------------------------------------------- two CTA pairs per cluster --
 
 def test_cluster_n_rules(ts):
-    cfg = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, cluster_n=2)
+    cfg = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, cluster_n=2, stream_k_tiles=-1)
     assert cfg["cluster_n"] == 2 and cfg["block_m"] == 256 and cfg["block_n"] == 256
     assert cfg["grid"] % 4 == 0 and cfg["grid"] <= 152
     # a unit is two tiles: 16 tile rows x 8 column pairs
@@ -246,3 +253,75 @@ def test_cluster_n_rules(ts):
         assert e.value.status == ts.ERR_UNSUPPORTED, force
     # unforced plans on one SM tile keep one pair (or no pair) per cluster
     assert ts.choose_config(128, 28672, 8192, "bf16", "bf16", 152)["cluster_n"] == 1
+
+
+# ---------------------------------------------------------- stream-K --
+
+def _sk_segments(w, slots, kb):
+    segs = 0
+    for g in range(slots):
+        a, b = g * w // slots, (g + 1) * w // slots
+        if b > a:
+            segs += (b - 1) // kb - a // kb + 1
+    return segs
+
+
+def test_stream_k_plan(ts):
+    c = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, block_m=256, block_n=256, stream_k_tiles=104)
+    assert c["stream_k_tiles"] == 104 and c["splits"] == 1 and c["split_tiles"] == 0
+    assert c["grid"] == 152 and c["workspace_bytes"] == 76 * 256 * 256 * 4
+    assert c["units"] == (256 - 104) + _sk_segments(104 * 64, 76, 64)
+    c = ts.choose_config(1000, 1288, 328, "bf16", "f32", 152, block_m=128, block_n=128, stream_k_tiles=30)
+    assert c["grid"] == 152 and c["workspace_bytes"] == 152 * 128 * 128 * 4
+    assert c["units"] == (8 * 11 - 30) + _sk_segments(30 * 6, 152, 6)
+    for force, code in [(dict(stream_k_tiles=-2), 1), (dict(stream_k_tiles=10, splits=2), 1),
+                        (dict(stream_k_tiles=10, splits=2, split_tiles=3), 1)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, **force)
+        assert e.value.status == code, force
+    # -1: no stream-K even where the planner would otherwise consider it
+    assert ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, stream_k_tiles=-1)["stream_k_tiles"] == 0
+
+
+def test_stream_k_needs_a_slice_per_slot(ts):
+    # 5 tiles x 6 K slices < 152 slots: some slots would get no slice
+    with pytest.raises(ts.TsgemmError) as e:
+        ts.choose_config(1000, 1288, 328, "bf16", "f32", 152, block_m=128, block_n=128, stream_k_tiles=5)
+    assert e.value.status == ts.ERR_UNSUPPORTED
+
+
+def _sk_walk(tiles_sk, kb, G):
+    """The kernel's stream-K decomposition, restated: every K slice of every
+    stream-K tile is covered once, contributors are their slot's first
+    segment, and each owner's contributors are the next m slots."""
+    W = tiles_sk * kb
+    cover = [[0] * kb for _ in range(tiles_sk)]
+    owners, contrib = {}, {}
+    for g in range(G):
+        a, b = g * W // G, (g + 1) * W // G
+        j = 0
+        while True:
+            start = a if j == 0 else (a // kb + j) * kb
+            if start >= b:
+                break
+            t = start // kb
+            end = min(b, (t + 1) * kb)
+            for k in range(start - t * kb, end - t * kb):
+                cover[t][k] += 1
+            if start > t * kb:
+                assert j == 0
+                contrib.setdefault(t, []).append(g)
+            elif end < (t + 1) * kb:
+                owners[t] = (g, ((t + 1) * kb * G - 1) // W - g)
+                assert end == b  # the owner segment is the slot's last
+            j += 1
+    assert all(c == 1 for row in cover for c in row)
+    assert set(contrib) == set(owners)
+    for t, (g, m) in owners.items():
+        assert contrib[t] == list(range(g + 1, g + m + 1))
+
+
+@pytest.mark.parametrize("args", [(16, 64, 76), (104, 16, 76), (64, 32, 152), (30, 6, 152), (20, 16, 36),
+                                  (30, 40, 76), (104, 64, 76), (16, 1024, 76), (68, 128, 76)])
+def test_stream_k_decomposition(args):
+    _sk_walk(*args)
