@@ -206,20 +206,23 @@ __device__ __forceinline__ bool unit_at(const GemmParams& p, int64_t g, int64_t 
     return true;
 }
 
-// Shared-memory staging of the output: each epilogue warp owns two buffers
-// of one 32 x 32 block (rows = its 32 accumulator lanes, 32 columns), filled
-// from registers and written to C by a TMA tensor store, so that global
-// writes are whole lines and rows or columns past the edge of C are clipped
-// by the copy engine.  The block is laid out in the tensor map's swizzle
-// (128-byte for fp32 rows, 64-byte for 16-bit rows); buffers are 1024-byte
-// aligned, as the swizzle patterns require.
+// Output path.  16-bit outputs are staged in shared memory: each epilogue
+// warp owns two buffers of one 32 x 32 block (rows = its 32 accumulator
+// lanes, 32 columns), filled from registers and written to C by a TMA
+// tensor store, so that global writes are whole lines and rows or columns
+// past the edge of C are clipped by the copy engine.  The block is laid out
+// in the tensor map's 64-byte swizzle; buffers are 1024-byte aligned, as
+// the swizzle requires.  fp32 outputs go straight from registers to C (each
+// thread writes its row's 128 contiguous bytes): their staging would take
+// 64 KiB, two slots of the operand ring, and the deeper ring is worth more
+// (measured on the 1024 x 1024 x 65536 shape).
 template <int kOut>
 __host__ __device__ constexpr uint32_t epi_buf_bytes() {
-    return 32u * 32u * (kOut == kOutF32 ? 4u : 2u);  // one 32 x 32 output block
+    return kOut == kOutF32 ? 0u : 32u * 32u * 2u;  // one 32 x 32 16-bit block
 }
 template <int kOut>
 __host__ __device__ constexpr uint32_t epi_smem_bytes() {
-    return kEpiWarps * 2u * epi_buf_bytes<kOut>();  // 32 KiB (16-bit), 64 KiB (fp32)
+    return kEpiWarps * 2u * epi_buf_bytes<kOut>();  // 32 KiB (16-bit), none (fp32)
 }
 
 template <int kOut>
@@ -232,18 +235,20 @@ struct CStager {
     // store the warp's 32 x 32 block at (row0, col0) of C.
     __device__ __forceinline__ void put(const GemmParams& p, const CUtensorMap* tmC, int row0, int col0,
                                         const uint32_t (&r)[32]) {
-        const uint32_t buf = buf0 + which * epi_buf_bytes<kOut>();
-        if (lane == 0) bulk_wait_group_read<1>();  // the store that used `buf` last has read it
-        __syncwarp();
         if constexpr (kOut == kOutF32) {
-            // 128-byte rows in the TMA 128-byte swizzle: 16-byte chunk j of
-            // row l sits at chunk position j ^ (l mod 8), so the 8 lanes of
-            // each store phase hit distinct banks
+            // straight to C: this lane's row, 8 16-byte vectors; N is a
+            // multiple of 4, so a vector is wholly inside C or outside
+            const int row = row0 + lane;
+            if (row < p.M) {
+                float* dst = static_cast<float*>(p.C) + static_cast<int64_t>(row) * p.N + col0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
-                             r[4 * j + 3]);
+                for (int j = 0; j < 8; ++j)
+                    if (col0 + 4 * j < p.N) st_global_v4(dst + 4 * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
         } else {
+            const uint32_t buf = buf0 + which * epi_buf_bytes<kOut>();
+            if (lane == 0) bulk_wait_group_read<1>();  // the store that used `buf` last has read it
+            __syncwarp();
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -256,14 +261,14 @@ struct CStager {
             for (int j = 0; j < 4; ++j)
                 st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
                              w[4 * j + 3]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, buf, col0, row0);
+                bulk_commit_group();  // (an empty group when the block is wholly outside C)
+            }
+            which ^= 1u;
         }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-            if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, buf, col0, row0);
-            bulk_commit_group();  // (an empty group when the block is wholly outside C)
-        }
-        which ^= 1u;
     }
 
     // All of this warp's stores have completed.

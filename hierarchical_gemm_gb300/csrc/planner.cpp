@@ -150,8 +150,9 @@ Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm,
 int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages) {
     const int64_t b_cols = block_m == 256 ? block_n / 2 : block_n;
     const int64_t stage = static_cast<int64_t>(kBM) * kBK * 2 + b_cols * kBK * 2;
-    // output staging: 8 epilogue warps x 2 buffers of one 32 x 32 block
-    const int64_t staging = kEpiWarps * 2 * 32 * 32 * out_bytes(dtype_out);
+    // output staging: 8 epilogue warps x 2 buffers of one 32 x 32 16-bit
+    // block (fp32 outputs are stored from registers)
+    const int64_t staging = dtype_out == TSGEMM_F32 ? 0 : kEpiWarps * 2 * 32 * 32 * out_bytes(dtype_out);
     return 1024 + stages * stage + staging + 8 * (2 * stages + 7) + 16;
 }
 

@@ -308,7 +308,9 @@ static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* 
 }
 
 // C: inner dimension N, outer M; box 32 x 32 (the block one epilogue warp
-// stores at a time), in the swizzle the kernel writes its staging buffer in.
+// stores at a time), in the swizzle the kernel writes its staging buffer in
+// (16-bit outputs; fp32 outputs are stored from registers and the map goes
+// unused).
 static tsgemm_status_t encode_c(tsgemm_plan_s* p, void* C) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return TSGEMM_ERR_CUDA;
