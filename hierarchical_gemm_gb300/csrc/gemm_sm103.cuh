@@ -616,14 +616,79 @@ struct TileShape {
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
+// The cluster-split form's exchange area: one 128-row x 32-column fp32
+// chunk per epilogue warpgroup, and its full / empty barriers.
+constexpr uint32_t kCsBufBytes = 2u * kBM * 32u * 4u;
+constexpr uint32_t kCsBytes = kCsBufBytes + 4u * 8u;
+
 // Bytes of dynamic shared memory the kernel needs for `stages` slots.
-template <int BN, int kOut>
+template <int BN, int kOut, bool kCS = false>
 __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
     return 1024u /* alignment slack */ + stages * TileShape<BN>::kStageBytes + epi_smem_bytes<kOut>() +
-           8u * (2 * stages + 7) /* barriers */ + 16u /* tmem holder, flags */;
+           (kCS ? kCsBytes : 0u) + 8u * (2 * stages + 7) /* barriers */ + 16u /* tmem holder, flags */;
 }
 
-template <int BN, int kOut, int kLayout, bool kF8 = false>
+// Cluster split (a 2 x 1 cluster of one-SM CTAs per tile): CTA 1 computes
+// the tile's second half of K and hands its accumulator, chunk by chunk, to
+// CTA 0 through distributed shared memory; CTA 0 adds it after its own
+// (the K order) and stores C.  Per epilogue warp and 32-column chunk: the
+// sender waits until the receiver's buffer is free, writes its 32 rows into
+// it with st.shared::cluster and arrives (release, cluster scope) on the
+// receiver's full barrier; the receiver waits for it (acquire), adds, and
+// arrives on the sender's empty barrier.  Every lane arrives, so each
+// lane's own writes (reads) are ordered before its arrival.  `buf` is this
+// warp's 4 KiB of its warpgroup's buffer in CTA 0; `phase` counts chunks.
+template <int BN, int kOut, class Release>
+__device__ __forceinline__ bool drain_cs(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
+                                         const Unit& un, uint32_t tbase, int row0, int lane, int c_begin,
+                                         uint32_t rank, uint32_t buf, uint32_t full_bar, uint32_t empty_bar,
+                                         uint32_t& phase, const WaitCtl& ctl, Release&& release) {
+    const int col0 = un.tn * BN;
+    const int c_end = c_begin + BN / 2;
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 32) {
+        uint32_t r[32];
+        if (rank != 0) {
+            if (!wait_bounded<true>(empty_bar, phase ^ 1u, ctl)) return false;  // the receiver read the last chunk
+            tmem_ld_32x32b_x32(tbase + c, r);
+            tmem_ld_wait();
+            if (c + 32 >= c_end) release();
+            const uint32_t dst = mapa_shared(buf + lane * 16u, 0u);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                st_shared_cluster_v4(dst + v * 512u, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+            mbar_arrive_cluster(full_bar, 0u);
+        } else {
+            if (!wait_bounded<true>(full_bar, phase, ctl)) return false;
+            tmem_ld_32x32b_x32(tbase + c, r);
+            tmem_ld_wait();
+            if (c + 32 >= c_end) release();
+            float acc[32];
+            // the sum starts from a cleared (+0) accumulator: 0 + own + partner
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(0.0f, __uint_as_float(r[j]));
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const float4 x = ld_shared_f4(buf + lane * 16u + v * 512u);
+                acc[4 * v] = __fadd_rn(acc[4 * v], x.x);
+                acc[4 * v + 1] = __fadd_rn(acc[4 * v + 1], x.y);
+                acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], x.z);
+                acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], x.w);
+            }
+            mbar_arrive_cluster(empty_bar, 1u);  // the buffer may be refilled
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
+            out.put(p, tmC, row0, col0 + c, r);
+        }
+        phase ^= 1u;
+    }
+    return true;
+}
+
+// kCS: launched as 2 x 1 clusters (a runtime launch attribute), the two
+// CTAs splitting each tile's K range and exchanging through distributed
+// shared memory (drain_cs).
+template <int BN, int kOut, int kLayout, bool kF8 = false, bool kCS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_sm103_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -635,7 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = p.stages;
 
     const uint32_t epi_smem = base + S * TS::kStageBytes;  // output staging
-    const uint32_t bars = epi_smem + epi_smem_bytes<kOut>();
+    const uint32_t cs_buf = epi_smem + epi_smem_bytes<kOut>();  // cluster-split exchange
+    const uint32_t cs_bars = cs_buf + kCsBufBytes;
+    const uint32_t bars = cs_buf + (kCS ? kCsBytes : 0u);
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
@@ -643,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
     const uint32_t epi_bar = bars + 8u * (2 * S + 5);
     const uint32_t red_bar = bars + 8u * (2 * S + 6);
-    uint8_t* misc = base_ptr + S * TS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 7);
+    uint8_t* misc = base_ptr + (bars - base) + 8u * (2 * S + 7);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
@@ -663,6 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(drain_bar, 1);
         mbar_init(epi_bar, kEpiWarps);
         mbar_init(red_bar, 1);
+        if constexpr (kCS) {
+            for (int w = 0; w < 4; ++w) mbar_init(cs_bars + 8u * w, 128);  // every lane of a warpgroup
+        }
         *abort_flag = 0;
         *last_flag = 0;
         fence_barrier_init();
@@ -673,9 +743,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_alloc<1>(smem_u32(tmem_holder), TS::kTmemCols);
     tc_fence_before();
     __syncthreads();
+    if constexpr (kCS) cluster_sync();  // both CTAs' barriers initialised before either uses them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    // work slot and, for the cluster split, this CTA's half of every tile's K
+    const uint32_t cs_rank = kCS ? cluster_ctarank() : 0u;
+    if constexpr (kCS) ctl.peer_abort[ctl.npeers++] = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), cs_rank ^ 1u);
+    const int64_t slot = kCS ? blockIdx.x >> 1 : blockIdx.x;
+    const int64_t nslots = kCS ? gridDim.x >> 1 : gridDim.x;
+    auto next_unit = [&](int64_t j, Unit& un) -> bool {
+        if (!unit_at(p, slot, nslots, j, un)) return false;
+        if constexpr (kCS) {
+            un.kb0 = static_cast<int>(cs_rank * p.kblocks / 2);
+            un.kb1 = static_cast<int>((cs_rank + 1) * p.kblocks / 2);
+        }
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
@@ -688,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t j = 0; ok; ++j) {
                 Unit un;
-                if (!unit_at(p, blockIdx.x, gridDim.x, j, un)) break;
+                if (!next_unit(j, un)) break;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, ctl)) {
                         ok = false;
@@ -725,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t j = 0; ok; ++j) {
                 Unit un;
-                if (!unit_at(p, blockIdx.x, gridDim.x, j, un)) break;
+                if (!next_unit(j, un)) break;
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, ctl)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * TS::kAccCols;
@@ -783,9 +867,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         const EpiAux aux{static_cast<int64_t>(blockIdx.x), 1, base, static_cast<uint32_t>(S) * TS::kStageBytes,
                          red_bar};
+        const int wg = e >> 2;
+        const uint32_t cs_mine = cs_buf + static_cast<uint32_t>(wg) * (kCsBufBytes / 2) + static_cast<uint32_t>(q) * 4096u;
+        uint32_t cs_phase = 0;
         for (int64_t j = 0;; ++j) {
             Unit un;
-            if (!unit_at(p, blockIdx.x, gridDim.x, j, un)) break;
+            if (!next_unit(j, un)) break;
             const int tm = un.tm;
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, ctl) ? 1 : 0;
@@ -799,9 +886,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(tempty_bar(acc));
             };
-            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, aux, c_begin, etid,
-                                      last_flag, ctl, epi_sync, release))
-                break;
+            if constexpr (kCS) {
+                if (!drain_cs<BN, kOut>(p, &tmC, out, un, tbase, row0, lane, c_begin, cs_rank, cs_mine,
+                                        cs_bars + 8u * wg, cs_bars + 8u * (2 + wg), cs_phase, ctl, release))
+                    break;
+            } else {
+                if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, aux, c_begin, etid,
+                                          last_flag, ctl, epi_sync, release))
+                    break;
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -815,6 +908,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane 0 ran a role loop alone may arrive in any convergence state.
     tc_fence_before();
     cta_barrier_any();
+    // (cluster split: neither CTA leaves while the other may still write
+    // into or read its shared memory)
+    if constexpr (kCS) cluster_barrier_any();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

@@ -6,12 +6,14 @@
 namespace tsg {
 
 // Kernel entry for a tile width (64/128/192/256), output kind (0 fp16,
-// 1 bf16, 2 fp32), operand layout (tsgemm_layout_t) and input width (in8:
-// 8-bit float inputs, RCR layout only); null for an unsupported combination.
-const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8);
+// 1 bf16, 2 fp32), operand layout (tsgemm_layout_t), input width (in8:
+// 8-bit float inputs, RCR layout only) and cluster split (cs = 2: launched
+// as 2 x 1 clusters splitting each tile's K; RRR, 16-bit inputs); null for
+// an unsupported combination.
+const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8, int cs);
 
 // Dynamic shared memory the kernel above uses with `stages` ring slots.
-int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages);
+int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages, int cs);
 
 // The CTA-pair kernel (256 x block_n tiles, block_n 128 or 256), launched
 // with clusters of `pairs` CTA pairs along N (1, or 2 for block_n 256: the
@@ -32,6 +34,7 @@ const void* kernel_2sm_layout1(int block_n, int out_kind, int pairs);
 const void* kernel_2sm_layout2(int block_n, int out_kind, int pairs);
 const void* kernel_2sm_layout3(int block_n, int out_kind, int pairs);
 const void* kernel_1sm_f8(int block_n, int out_kind);
+const void* kernel_1sm_cs(int block_n, int out_kind);
 const void* kernel_2sm_f8(int block_n, int out_kind, int pairs);
 
 }  // namespace tsg

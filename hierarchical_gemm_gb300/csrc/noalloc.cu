@@ -174,8 +174,8 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     }
 
     const int out_kind = dtype_out == TSGEMM_F16 ? tsg::kOutF16 : (dtype_out == TSGEMM_BF16 ? tsg::kOutBF16 : tsg::kOutF32);
-    const void* kern = tsg::kernel_1sm(cfg.block_n, out_kind, TSGEMM_LAYOUT_RRR, false);
-    const int64_t need = tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind, cfg.stages);
+    const void* kern = tsg::kernel_1sm(cfg.block_n, out_kind, TSGEMM_LAYOUT_RRR, false, 1);
+    const int64_t need = tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind, cfg.stages, 1);
     if (!kern || need > tsg::kSmemPerCtaMax) return TSGEMM_ERR_UNSUPPORTED;
     const int64_t smem = need > tsg::kSmemPerCtaMax / 2 + 1024 ? need : tsg::kSmemPerCtaMax / 2 + 1024;
     bool& attr = ds->attr_set[cfg.block_n / 64 - 1][out_kind];

@@ -147,18 +147,21 @@ Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm,
 
 }  // namespace
 
-int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages) {
+int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages, int cluster_split) {
     const int64_t b_cols = block_m == 256 ? block_n / 2 : block_n;
     const int64_t stage = static_cast<int64_t>(kBM) * kBK * 2 + b_cols * kBK * 2;
     // output staging: 8 epilogue warps x 2 buffers of one 32 x 32 16-bit
     // block (fp32 outputs are stored from registers)
     const int64_t staging = dtype_out == TSGEMM_F32 ? 0 : kEpiWarps * 2 * 32 * 32 * out_bytes(dtype_out);
-    return 1024 + stages * stage + staging + 8 * (2 * stages + 7) + 16;
+    // cluster split: a 128 x 32 fp32 exchange chunk per epilogue warpgroup
+    // and four barriers
+    const int64_t exchange = cluster_split == 2 ? 2 * 128 * 32 * 4 + 4 * 8 : 0;
+    return 1024 + stages * stage + staging + exchange + 8 * (2 * stages + 7) + 16;
 }
 
-int max_stages_for(int block_m, int block_n, int dtype_out) {
+int max_stages_for(int block_m, int block_n, int dtype_out, int cluster_split) {
     int s = 1;
-    while (s < 16 && smem_bytes_for(block_m, block_n, dtype_out, s + 1) <= kSmemPerCtaMax) ++s;
+    while (s < 16 && smem_bytes_for(block_m, block_n, dtype_out, s + 1, cluster_split) <= kSmemPerCtaMax) ++s;
     return s;
 }
 
@@ -180,6 +183,39 @@ tsgemm_status_t validate_problem(int64_t M, int64_t N, int64_t K, int dtype_in, 
     const int64_t eb = in_bytes(dtype_in);
     if ((a_row * eb) % 16 != 0 || (b_row * eb) % 16 != 0 || (N * out_bytes(dtype_out)) % 16 != 0)
         return TSGEMM_ERR_ALIGNMENT;
+    return TSGEMM_OK;
+}
+
+// The DSMEM cluster-split plan (forced by cluster_split = 2): one-SM tiles
+// of the widest width up to N, every tile's K range split between the two
+// CTAs of a 2 x 1 cluster, one tile per cluster at a time.
+static tsgemm_status_t choose_cluster_split(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
+                                            int num_sms, const tsgemm_config_t& f, int64_t kblocks,
+                                            tsgemm_config_t* out) {
+    (void)K;
+    (void)dtype_in;
+    const int64_t n_pad = ceil_div(N, 64) * 64;
+    int bn = f.block_n;
+    if (!bn) bn = n_pad >= 256 ? 256 : (n_pad >= 192 ? 192 : (n_pad >= 128 ? 128 : 64));
+    tsgemm_config_t c{};
+    c.block_m = 128;
+    c.block_n = bn;
+    c.splits = 1;
+    const int smax_fit = max_stages_for(128, bn, dtype_out, 2);
+    if (f.stages > smax_fit || (f.stages != 0 && f.stages < 2)) return TSGEMM_ERR_UNSUPPORTED;
+    c.stages = f.stages ? f.stages : smax_fit;
+    c.group_m = f.group_m ? f.group_m : 8;
+    c.cluster_n = 1;
+    c.cluster_split = 2;
+    const int64_t tiles = ceil_div(M, 128) * ceil_div(N, bn);
+    c.units = tiles;
+    const int64_t slots = (f.grid ? f.grid : num_sms) / 2;
+    if (slots < 1) return TSGEMM_ERR_UNSUPPORTED;
+    c.grid = static_cast<int32_t>(std::min<int64_t>(tiles, slots) * 2);
+    c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
+    c.debug_flags = f.debug_flags;
+    (void)kblocks;
+    *out = c;
     return TSGEMM_OK;
 }
 
@@ -206,10 +242,22 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     if (f.cluster_n == 2 && (f.block_m == 128 || (f.block_n != 0 && f.block_n != 256) || num_sms < 4))
         return TSGEMM_ERR_UNSUPPORTED;
     if (f.stream_k_tiles < -1) return TSGEMM_ERR_INVALID_ARG;
+    if (f.cluster_split < 0 || f.cluster_split > 2) return TSGEMM_ERR_UNSUPPORTED;
+    if (f.cluster_split == 2) {
+        // the DSMEM K split: one-SM tiles, each split in two between the
+        // CTAs of a 2 x 1 cluster; RRR layout and 16-bit inputs
+        if (f.block_m == 256 || f.splits > 1 || f.split_tiles > 0 || f.stream_k_tiles > 0 || f.cluster_n == 2)
+            return TSGEMM_ERR_INVALID_ARG;
+        if (layout != TSGEMM_LAYOUT_RRR || is_8bit(dtype_in) || num_sms < 2) return TSGEMM_ERR_UNSUPPORTED;
+    }
     if (f.stream_k_tiles > 0 && (f.splits > 1 || f.split_tiles > 0)) return TSGEMM_ERR_INVALID_ARG;
 
     const int64_t kblocks = ceil_div(K, slice_k(dtype_in));
     if (f.splits > kblocks || f.splits > 4096) return TSGEMM_ERR_UNSUPPORTED;
+    if (f.cluster_split == 2) {
+        if (kblocks < 2) return TSGEMM_ERR_UNSUPPORTED;
+        return choose_cluster_split(M, N, K, dtype_in, dtype_out, num_sms, f, kblocks, out);
+    }
 
     // Candidate tile widths: never wider than N rounded up to 64.
     const int64_t n_pad = ceil_div(N, 64) * 64;
@@ -304,6 +352,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     c.stages = f.stages ? f.stages : smax_fit;
     c.group_m = f.group_m ? f.group_m : 8;
     c.cluster_n = best_cn;
+    c.cluster_split = 1;
     const int64_t tiles = ceil_div(M, best_bm) * ceil_div(ceil_div(N, best_bn), best_cn);
     c.split_tiles = best_s > 1 ? best_st : 0;
     c.stream_k_tiles = best_sk;

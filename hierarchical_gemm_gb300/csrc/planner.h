@@ -31,12 +31,12 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                               tsgemm_config_t* out);
 
 // Dynamic shared memory per CTA of the kernel for this tile shape (block_m
-// 128: one SM per tile; 256: a CTA pair per tile), output type and ring
-// depth.
-int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages);
+// 128: one SM per tile; 256: a CTA pair per tile), output type, ring depth
+// and cluster split (2: the exchange area of the DSMEM K split).
+int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages, int cluster_split = 1);
 
 // Deepest ring that fits the shared-memory budget for this tile shape and
 // output type.
-int max_stages_for(int block_m, int block_n, int dtype_out);
+int max_stages_for(int block_m, int block_n, int dtype_out, int cluster_split = 1);
 
 }  // namespace tsg

@@ -140,11 +140,12 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
 
     const bool pair = cfg.block_m == 256;
     const bool in8 = tsg::is_8bit(dtype_in);
+    const int cs = cfg.cluster_split == 2 ? 2 : 1;
     const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out), layout, in8, cfg.cluster_n)
-                            : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out), layout, in8);
+                            : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out), layout, in8, cs);
     const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages)
-                              : tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages);
-    if (!kern || need != tsg::smem_bytes_for(cfg.block_m, cfg.block_n, dtype_out, cfg.stages) ||
+                              : tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages, cs);
+    if (!kern || need != tsg::smem_bytes_for(cfg.block_m, cfg.block_n, dtype_out, cfg.stages, cs) ||
         need > tsg::kSmemPerCtaMax)
         return TSGEMM_ERR_UNSUPPORTED;
     // Ask for more than half the SM's shared memory even when the ring is
@@ -157,14 +158,24 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;
     }
-    if (pair) {
+    if (pair || cs == 2) {
         // Persistent clusters: launch no more than can be resident at once
         // (a cluster's CTAs must share a GPC).
-        const int per_cluster = 2 * cfg.cluster_n;
+        const int per_cluster = pair ? 2 * cfg.cluster_n : 2;
         cudaLaunchConfig_t lc{};
         lc.gridDim = dim3(static_cast<unsigned>(cfg.grid), 1, 1);
         lc.blockDim = dim3(tsg::kThreads, 1, 1);
         lc.dynamicSmemBytes = static_cast<size_t>(smem);
+        // the cluster-split kernel takes its 2 x 1 cluster shape at launch
+        cudaLaunchAttribute cattr{};
+        cattr.id = cudaLaunchAttributeClusterDimension;
+        cattr.val.clusterDim.x = 2;
+        cattr.val.clusterDim.y = 1;
+        cattr.val.clusterDim.z = 1;
+        if (!pair) {
+            lc.attrs = &cattr;
+            lc.numAttrs = 1;
+        }
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) != cudaSuccess || clusters < 1) {
             (void)cudaGetLastError();
@@ -373,6 +384,15 @@ tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, voi
     lc.stream = static_cast<cudaStream_t>(stream);
     lc.attrs = nullptr;
     lc.numAttrs = 0;
+    cudaLaunchAttribute cattr{};
+    if (plan->cfg.cluster_split == 2) {
+        cattr.id = cudaLaunchAttributeClusterDimension;
+        cattr.val.clusterDim.x = 2;
+        cattr.val.clusterDim.y = 1;
+        cattr.val.clusterDim.z = 1;
+        lc.attrs = &cattr;
+        lc.numAttrs = 1;
+    }
     void* args[4] = {&plan->tmA, &plan->tmB, &plan->tmC, &plan->params};
     if (cudaLaunchKernelExC(&lc, plan->kernel, args) != cudaSuccess) {
         (void)cudaGetLastError();

@@ -121,6 +121,13 @@ typedef struct {
                                none, 0 the planner's choice. The workspace is
                                then one block_m x block_n x cluster_n fp32
                                partial per slot. */
+    int32_t cluster_split;  /* 2: the DSMEM split of K (block_m 128, RRR
+                               layout, 16-bit inputs): the two CTAs of a 2 x 1
+                               cluster compute the two halves of every tile's
+                               K range and CTA 1 hands its fp32 accumulator to
+                               CTA 0 through distributed shared memory, chunk
+                               by chunk; no workspace.  Forced only; the
+                               planner reports 1 otherwise. */
 } tsgemm_config_t;
 
 /* Tests only: the first CTA (or CTA pair) skips the first operand load of

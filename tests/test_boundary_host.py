@@ -325,3 +325,26 @@ def _sk_walk(tiles_sk, kb, G):
                                   (30, 40, 76), (104, 64, 76), (16, 1024, 76), (68, 128, 76)])
 def test_stream_k_decomposition(args):
     _sk_walk(*args)
+
+
+# ------------------------------------------------ DSMEM cluster split --
+
+def test_cluster_split_rules(ts):
+    c = ts.choose_config(1024, 2048, 8192, "bf16", "bf16", 152, cluster_split=2)
+    assert c["cluster_split"] == 2 and c["block_m"] == 128 and c["splits"] == 1
+    assert c["units"] == 8 * 8 and c["grid"] == 128 and c["workspace_bytes"] == 0
+    stage = 128 * 64 * 2 + c["block_n"] * 64 * 2
+    smem = 1024 + c["stages"] * stage + 8 * 2 * 32 * 32 * 2 + (2 * 128 * 32 * 4 + 32) + 8 * (2 * c["stages"] + 7) + 16
+    assert smem <= 232448 < smem + stage
+    # the planner never proposes it by itself
+    assert ts.choose_config(1024, 2048, 8192, "bf16", "bf16", 152)["cluster_split"] == 1
+    for force, code in [(dict(cluster_split=2, block_m=256), 1), (dict(cluster_split=2, splits=2), 1),
+                        (dict(cluster_split=2, stream_k_tiles=4), 1), (dict(cluster_split=3), 2)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(1024, 2048, 8192, "bf16", "bf16", 152, **force)
+        assert e.value.status == code, force
+    for args, code in [((1024, 2048, 8192, "bf16", "bf16", 152, "rcr"), 2), ((1024, 2048, 64, "bf16", "bf16", 152, "rrr"), 2),
+                       ((1024, 2048, 8192, "e4m3", "bf16", 152, "rcr"), 2)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(*args[:6], layout=args[6], cluster_split=2)
+        assert e.value.status == code, args
