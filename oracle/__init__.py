@@ -64,6 +64,9 @@ def lib():
         L.oracle_gemm8.argtypes = [i64, i64, i64, vp, vp, i32, vp, vp, i32]
         L.oracle_gemm8_sampled.argtypes = [i64, i64, i64, vp, vp, i32, i64, vp,
                                            vp, vp, vp]
+        L.oracle_attention.restype = i32
+        L.oracle_attention.argtypes = [i64, i64, i64, i64, i64, i64, vp, vp, vp, i32,
+                                       ctypes.c_double, i32, vp, vp]
         _lib = L
     return _lib
 
@@ -220,3 +223,58 @@ def accept(C, ref, sabs, dtype_out, exact=False):
             "worst_index": tuple(int(v) for v in np.unravel_index(worst, ratio.shape))
             if ratio.size else ()}
     return nbad == 0, info
+
+
+# ------------------------------------------------------------- attention --
+
+def attention(Q_bits, K_bits, V_bits, dtype_in, scale, causal=False):
+    """O = softmax(scale * Q K^T) V per (batch, head), and per element
+    bound = sum_t w_t |V[t]|, both float64 of shape (B, H, Sq, Dv).
+
+    Q_bits (B, H, Sq, D), K_bits (B, H, Sk, D), V_bits (B, H, Sk, Dv): 16-bit
+    bit patterns.  Causal: row i sees keys t <= i + Sk - Sq; a row that sees
+    none is zero.  (oracle_attention.c, after the FlashMLA example of the
+    TileScale README.)"""
+    code = dtype_code(dtype_in)
+    Q_bits, pq = _c(Q_bits, np.uint16)
+    K_bits, pk = _c(K_bits, np.uint16)
+    V_bits, pv = _c(V_bits, np.uint16)
+    B, H, Sq, D = Q_bits.shape
+    Sk, Dv = K_bits.shape[2], V_bits.shape[3]
+    assert K_bits.shape == (B, H, Sk, D) and V_bits.shape == (B, H, Sk, Dv)
+    O = np.empty((B, H, Sq, Dv), dtype=np.float64)
+    bound = np.empty((B, H, Sq, Dv), dtype=np.float64)
+    if lib().oracle_attention(B, H, Sq, Sk, D, Dv, pq, pk, pv, code, float(scale), int(bool(causal)),
+                              O.ctypes.data, bound.ctypes.data) != 0:
+        raise MemoryError("oracle_attention could not allocate its scratch")
+    return O, bound
+
+
+# Acceptance rule for an attention output (derived from the arithmetic of
+# the kernel's online softmax): the weights are computed in fp32 and
+# rounded once to the 16-bit input format before they multiply V, a
+# relative error of at most 2^-9 (bf16) per weight, which moves an output
+# element by at most 2^-9 * sum_t w_t |V[t]|; fp32 accumulation, the
+# approximate base-2 exponential and the fp32 division add far less.  The
+# bound allows twice that, plus half an ulp of the 16-bit output format.
+ATTN_RTOL = 2.0 ** -8
+ATTN_ATOL = 1e-6
+
+
+def accept_attention(O, ref, bound, dtype_out):
+    code = dtype_code(dtype_out)
+    got = output_values(O, code)
+    tol = ATTN_RTOL * bound + ATTN_ATOL
+    if code != F32:
+        tol = tol + half_ulp(np.maximum(np.abs(ref), np.abs(got)), code)
+    err = np.abs(got - ref)
+    bad = ~(err <= tol)
+    info = {"max_err": float(np.nanmax(err)) if err.size else 0.0,
+            "max_err_over_bound": float(np.nanmax(err / tol)) if err.size else 0.0,
+            "bad": int(bad.sum())}
+    if bad.any():
+        idx = np.unravel_index(int(np.argmax(np.where(bad, err / tol, -1))), err.shape)
+        info["first_bad"] = [int(x) for x in idx]
+        info["got"] = float(got[idx])
+        info["want"] = float(ref[idx])
+    return not bad.any(), info

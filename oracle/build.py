@@ -1,26 +1,26 @@
-"""Compile the oracle's C source into oracle/_build/liboracle.so with gcc.
+"""Compile the oracle's C sources into oracle/_build/liboracle.so with gcc.
 
 Test infrastructure: building the checker is not using it.  The library is
-rebuilt when the source is newer than the shared object.
+rebuilt when a source is newer than the shared object.
 """
 import os
 import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "oracle_gemm.c")
+SRCS = [os.path.join(HERE, "oracle_gemm.c"), os.path.join(HERE, "oracle_attention.c")]
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liboracle.so")
 
 
 def build(force: bool = False) -> str:
     if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+            and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in SRCS)):
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB + ".%d.tmp" % os.getpid()
     cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-o", tmp, SRC, "-lpthread", "-lm"]
+           "-fPIC", "-shared", "-o", tmp] + SRCS + ["-lpthread", "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB
