@@ -1,0 +1,541 @@
+// attention_sm103.cu -- the attention block (softmax(scale Q K^T) V) on
+// tcgen05, and its C ABI (tsattn.h).
+//
+// It is the per-device block of the FlashMLA example of the TileScale
+// README (section "Example of FlashMLA"), laid out for sm_103a:
+//   * a CTA owns 128 query rows of one (batch, head): Q is loaded once by
+//     TMA into shared memory (128-byte swizzle);
+//   * key / value blocks of 128 rows stream through a two-slot ring;
+//   * S_j = Q K_j^T is computed by tcgen05.mma into one of two tensor-memory
+//     score buffers (acc_s of the example), so that the scores of block j+1
+//     are computed while block j's softmax runs;
+//   * one warpgroup, a thread per query row, reads its row of S_j, keeps the
+//     running maximum (scores_max) and row sum (logsum) in base-2 units,
+//     writes P_j = 2^(t - m) rounded to the 16-bit input format into shared
+//     memory (acc_s_cast) and, when its maximum has grown, rescales its row
+//     of the output accumulator (scores_scale);
+//   * O += P_j V_j is computed by tcgen05.mma into a tensor-memory
+//     accumulator (acc_o); at the end each thread divides its row by the
+//     row sum and stores it.
+// The rescale is lazy: a row keeps its old maximum until the new one exceeds
+// it by 2^8, so the output accumulator is read and rewritten only when a
+// row's scores jump; the weights then stay below 2^8, well inside the
+// 16-bit formats, and the final division uses the same maximum as every
+// weight, so the result is the same softmax.
+//
+// Warp roles: warp 0 lane 0 issues the TMA loads, warp 1 lane 0 the MMAs,
+// warps 2-5 run the softmax and the epilogue.  Every wait is bounded in time
+// (WaitCtl); a CTA that gives up records a timeout, lets its copies and MMAs
+// finish, frees tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "ptx.cuh"
+#include "tsattn.h"
+
+namespace tsg {
+namespace attn {
+
+constexpr int kBQ = 128;                // query rows per CTA (TMEM lanes)
+constexpr int kBKV = 128;               // keys per block
+constexpr int kD = 128;                 // head dimension
+constexpr int kThreads = 192;           // producer warp, MMA warp, softmax warpgroup
+constexpr uint32_t kAtom = 128u * 128u; // 128 rows x 128 bytes: one swizzle atom column
+constexpr uint32_t kTile = 2u * kAtom;  // 128 rows x 128 16-bit elements
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kKVOff = kTile;      // ring slot: K block, then V block
+constexpr uint32_t kSlotBytes = 2u * kTile;
+constexpr int kSlots = 2;
+constexpr uint32_t kPOff = kKVOff + kSlots * kSlotBytes;  // two P buffers
+constexpr uint32_t kBarOff = kPOff + 2u * kTile;
+constexpr int kNumBars = 14;
+constexpr uint32_t kMiscOff = kBarOff + 8u * kNumBars;
+constexpr uint32_t kSmemBytes = 1024u + kMiscOff + 16u;
+constexpr uint32_t kTmemCols = 512;     // S buffers at columns 0 and 128, O at 256
+constexpr uint32_t kOCol = 256;
+constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct AttnParams {
+    int32_t B, H, Sq, Sk;
+    int32_t nq;           // query blocks per (batch, head)
+    int32_t causal;
+    float scale_log2;     // scale * log2(e): scores to base-2 exponent units
+    int32_t debug_flags;
+    void* O;
+    int* status;
+    uint64_t timeout_ns;
+};
+
+// Key / value blocks query block qb has to visit.
+__device__ __forceinline__ int kv_blocks(const AttnParams& p, int qb) {
+    const int nk = (p.Sk + kBKV - 1) / kBKV;
+    if (!p.causal) return nk;
+    const int last_q = min(qb * kBQ + kBQ - 1, p.Sq - 1);
+    const int last_k = last_q + p.Sk - p.Sq;  // the last key that block's last row sees
+    if (last_k < 0) return 0;
+    return min(nk, last_k / kBKV + 1);
+}
+
+// tcgen05 instruction descriptor, kind::f16, fp32 accumulator, M = N = 128;
+// A K-major; B K-major (K^T: rows of K are the N index) or N-major (V).
+__host__ __device__ constexpr uint32_t idesc(bool f16, bool b_nmajor) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((b_nmajor ? 1u : 0u) << 16) |
+           ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+template <bool kF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_sm103(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t bars = base + kBarOff;
+    const uint32_t q_full = bars;
+    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bars + 8u * (3 + s); };
+    auto s_full = [&](int b) { return bars + 8u * (5 + b); };
+    auto s_free = [&](int b) { return bars + 8u * (7 + b); };
+    auto p_full = [&](int b) { return bars + 8u * (9 + b); };
+    auto p_free = [&](int b) { return bars + 8u * (11 + b); };  // PV on buffer b done
+    const uint32_t drain_bar = bars + 8u * 13;
+    uint8_t* misc = base_ptr + kMiscOff;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / p.nq;
+    const int qb = p.nq - 1 - static_cast<int>(blockIdx.x % p.nq);  // (causal: longest blocks first)
+    const int nkv = kv_blocks(p, qb);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full(b), 1);
+            mbar_init(s_free(b), kBQ);  // every softmax thread
+            mbar_init(p_full(b), kBQ);
+            mbar_init(p_free(b), 1);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    if (warp == 1) tmem_alloc<1>(smem_u32(tmem_holder), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    const uint32_t qs = base + kQOff;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0 && nkv > 0) {
+            uint32_t outstanding = 0, out_par = 0;
+            mbar_arrive_expect_tx(q_full, kTile);
+            tma_load_3d(qs, &tmQ, q_full, 0, qb * kBQ, bh);
+            tma_load_3d(qs + kAtom, &tmQ, q_full, 64, qb * kBQ, bh);
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j & 1;
+                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+                if (!wait_bounded(kv_empty(st), ph ^ 1u, ctl)) break;
+                // tests only: the first CTA leaves its first block unloaded
+                if ((p.debug_flags & 1) && blockIdx.x == 0 && j == 0) continue;
+                const uint32_t ks = base + kKVOff + st * kSlotBytes, vs = ks + kTile;
+                mbar_arrive_expect_tx(kv_full(st), 2u * kTile);
+                tma_load_3d(ks, &tmK, kv_full(st), 0, j * kBKV, bh);
+                tma_load_3d(ks + kAtom, &tmK, kv_full(st), 64, j * kBKV, bh);
+                tma_load_3d(vs, &tmV, kv_full(st), 0, j * kBKV, bh);
+                tma_load_3d(vs + kAtom, &tmV, kv_full(st), 64, j * kBKV, bh);
+                outstanding |= 1u << st;
+                out_par = (out_par & ~(1u << st)) | (ph << st);
+            }
+            // every copy this thread started lands before the CTA exits
+            wait_bounded(q_full, 0u, ctl, false);
+            for (int s = 0; s < kSlots; ++s)
+                if (outstanding & (1u << s)) wait_bounded(kv_full(s), (out_par >> s) & 1u, ctl, false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0 && nkv > 0) {
+            constexpr uint32_t kIdS = idesc(kF16, false), kIdPV = idesc(kF16, true);
+            bool ok = wait_bounded(q_full, 0u, ctl);
+            // O += P_i V_i.  P (128 rows x 128 keys) is K-major like Q; V
+            // (128 keys x 128 columns, columns contiguous) is the N-major B
+            // operand: 64-column boxes 16 KiB apart, 8-key groups 1 KiB
+            // apart, the k-th 16-key step 2 KiB further.
+            auto issue_pv = [&](int i) -> bool {
+                const int pb = i & 1;
+                if (!wait_bounded(p_full(pb), static_cast<uint32_t>(i >> 1) & 1u, ctl)) return false;
+                tc_fence_after();
+                const uint32_t ps = base + kPOff + pb * kTile;
+                const uint32_t vs = base + kKVOff + (i & 1) * kSlotBytes + kTile;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t ad = smem_desc_sw128(ps + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
+                    const uint64_t bd = smem_desc_sw128(vs + k * 2048u, kAtom, 1024u);
+                    umma_f16<1>(tmem + kOCol, ad, bd, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
+                }
+                umma_commit(p_free(pb));          // P buffer read; O holds PV_0..PV_i
+                umma_commit(kv_empty(i & 1));     // K_i and V_i read
+                return true;
+            };
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j & 1, sb = j & 1;
+                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+                if (!wait_bounded(kv_full(st), ph, ctl) || !wait_bounded(s_free(sb), ph ^ 1u, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // S_j = Q K_j^T: both operands K-major, two 64-wide swizzle
+                // columns of D, the k-th 16-deep step 32 bytes along a row
+                const uint32_t ks = base + kKVOff + st * kSlotBytes;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t ad = smem_desc_sw128(qs + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
+                    const uint64_t bd = smem_desc_sw128(ks + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
+                    umma_f16<1>(tmem + sb * 128u, ad, bd, kIdS, k > 0 ? 1u : 0u);
+                }
+                umma_commit(s_full(sb));
+                if (j >= 1 && !issue_pv(j - 1)) ok = false;
+            }
+            if (ok) issue_pv(nkv - 1);
+            // every MMA issued above completes before tensor memory is freed
+            umma_commit(drain_bar);
+            wait_bounded(drain_bar, 0u, ctl, false);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------- softmax and epilogue --
+        const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+        const int r = quarter * 32 + lane;            // query row within the block
+        const int qrow = qb * kBQ + r;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int kv_last = p.causal ? qrow + p.Sk - p.Sq : p.Sk - 1;  // last key this row sees
+        // a bounded wait taken by lane 0 for the whole warp
+        auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+            int good = 1;
+            if (lane == 0) good = wait_bounded(bar, parity, ctl) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, good, 0) != 0;
+        };
+        float m_used = -INFINITY;  // base-2 maximum the weights are taken against
+        float l = 0.0f;            // sum of this row's weights
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            const int sb = j & 1, pb = j & 1;
+            if (!warp_wait(s_full(sb), static_cast<uint32_t>(j >> 1) & 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c);
+                tmem_ld_32x32b_x32(trow + sb * 128u + 32u * c, part);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(s_free(sb));  // the score buffer may be overwritten
+            // scores to base-2 units; keys past Sk or past the causal limit
+            // weigh nothing
+            const int k0 = j * kBKV;
+            const bool whole = k0 + kBKV - 1 <= kv_last && k0 + kBKV <= p.Sk;
+            float mb = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                float x = __uint_as_float(s[c]) * p.scale_log2;
+                if (!whole && (k0 + c > kv_last || k0 + c >= p.Sk)) x = -INFINITY;
+                s[c] = __float_as_uint(x);
+                mb = fmaxf(mb, x);
+            }
+            const float m_new = fmaxf(m_used, mb);
+            const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
+            if (__any_sync(0xffffffffu, need)) {
+                // every lane of the warp moves to its own new maximum
+                const float alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m_new);
+                if (m_new > -INFINITY) m_used = m_new;
+                l *= alpha;
+                if (j >= 1) {
+                    // O holds P_0 V_0 + ... + P_{j-1} V_{j-1}: wait for the last,
+                    // then scale this row
+                    if (!warp_wait(p_free((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 128; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(trow + kOCol + c, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st_32x32b_x32(trow + kOCol + c, o);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            // P_j goes to buffer pb once P V of block j - 2 has read it
+            if (j >= 2 && !warp_wait(p_free(pb), static_cast<uint32_t>((j - 2) >> 1) & 1u)) {
+                ok = false;
+                break;
+            }
+            const uint32_t pbase = base + kPOff + pb * kTile + static_cast<uint32_t>(r) * 128u;
+            float rs = 0.0f;
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 64 * a + 8 * c8 + 2 * e;
+                        const float x0 = __uint_as_float(s[c]), x1 = __uint_as_float(s[c + 1]);
+                        const float p0 = m_used == -INFINITY ? 0.0f : ex2_approx(x0 - m_used);
+                        const float p1 = m_used == -INFINITY ? 0.0f : ex2_approx(x1 - m_used);
+                        rs += p0 + p1;
+                        w[e] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+                    }
+                    // K-major, 128-byte swizzle: 16-byte chunk c8 of row r at
+                    // chunk position c8 ^ (r mod 8)
+                    st_shared_v4(pbase + a * kAtom + ((static_cast<uint32_t>(c8) ^ (r & 7)) << 4), w[0], w[1], w[2],
+                                 w[3]);
+                }
+            }
+            l += rs;
+            fence_proxy_async_shared();  // the P writes are visible to the tensor core
+            tc_fence_before();
+            mbar_arrive(p_full(pb));
+        }
+        // -------------------------------------------------- epilogue --
+        if (ok && nkv > 0 && !warp_wait(p_free((nkv - 1) & 1), static_cast<uint32_t>((nkv - 1) >> 1) & 1u))
+            ok = false;
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            uint16_t* orow = static_cast<uint16_t*>(p.O) + (static_cast<int64_t>(bh) * p.Sq + qrow) * kD;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+                uint32_t o[32];
+                if (nkv > 0) {
+                    tmem_ld_32x32b_x32(trow + kOCol + c, o);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float lo = __uint_as_float(o[2 * i]) * inv, hi = __uint_as_float(o[2 * i + 1]) * inv;
+                    w[i] = kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+                }
+                if (qrow < p.Sq) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        st_global_v4(orow + c + 8 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ exit --
+    tc_fence_before();
+    cta_barrier_any();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc<1>(tmem, kTmemCols);
+    }
+}
+
+// --------------------------------------------------------------- host --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// The library's status word (one per device that loads the library), used
+// when the caller passes no status pointer.
+__device__ int g_attn_status;
+
+struct DeviceState {
+    bool ready = false;
+    int* status = nullptr;
+    bool attr[2] = {false, false};
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+}  // namespace attn
+}  // namespace tsg
+
+extern "C" {
+
+tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int32_t D, tsgemm_dtype_t dtype,
+                                  float scale, int32_t causal, const void* Q, const void* K, const void* V, void* O,
+                                  int* status, void* stream, int32_t debug_flags, int32_t timeout_ms) {
+    using namespace tsg::attn;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || !Q || !K || !V || !O || timeout_ms < 0) return TSGEMM_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return TSGEMM_ERR_INVALID_ARG;
+    if (dtype != TSGEMM_F16 && dtype != TSGEMM_BF16) return TSGEMM_ERR_UNSUPPORTED;
+    if (D != kD) return TSGEMM_ERR_UNSUPPORTED;
+    const int64_t lim = (int64_t{1} << 31) - 1;
+    if (B * H > lim || Sq > lim || Sk > lim || B * H * ((Sq + kBQ - 1) / kBQ) > lim) return TSGEMM_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
+         reinterpret_cast<uintptr_t>(O)) &
+        15u)
+        return TSGEMM_ERR_ALIGNMENT;
+    const int64_t qbytes = B * H * Sq * D * 2, kvbytes = B * H * Sk * D * 2;
+    auto overlaps = [](const void* a, int64_t na, const void* b, int64_t nb) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+        return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
+    };
+    if (overlaps(O, qbytes, Q, qbytes) || overlaps(O, qbytes, K, kvbytes) || overlaps(O, qbytes, V, kvbytes))
+        return TSGEMM_ERR_INVALID_ARG;
+
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return TSGEMM_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= kMaxDevices) return TSGEMM_ERR_UNSUPPORTED;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return TSGEMM_ERR_CUDA;
+    const bool f16 = dtype == TSGEMM_F16;
+    const void* kern = f16 ? reinterpret_cast<const void*>(&attn_fwd_sm103<true>)
+                           : reinterpret_cast<const void*>(&attn_fwd_sm103<false>);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState& ds = g_dev[dev];
+        if (!ds.ready) {
+            void* sym = nullptr;
+            if (cudaGetSymbolAddress(&sym, g_attn_status) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return TSGEMM_ERR_CUDA;
+            }
+            ds.status = static_cast<int*>(sym);
+            ds.ready = true;
+        }
+        if (!ds.attr[f16 ? 1 : 0]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytes)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return TSGEMM_ERR_CUDA;
+            }
+            ds.attr[f16 ? 1 : 0] = true;
+        }
+    }
+    int* st = status ? status : g_dev[dev].status;
+
+    // [B*H][S][D] as a 3-D tensor: a 64 (D) x 128 (rows) box never crosses
+    // into another (batch, head); rows past S read as zeros
+    const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    auto map3 = [&](CUtensorMap* m, const void* ptr, int64_t S) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                                    static_cast<cuuint64_t>(B * H)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S * D) * 2};
+        const cuuint32_t box[3] = {64, 128, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        return enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    alignas(64) CUtensorMap tmQ, tmK, tmV;
+    if (!map3(&tmQ, Q, Sq) || !map3(&tmK, K, Sk) || !map3(&tmV, V, Sk)) return TSGEMM_ERR_CUDA;
+
+    AttnParams prm{};
+    prm.B = static_cast<int32_t>(B);
+    prm.H = static_cast<int32_t>(H);
+    prm.Sq = static_cast<int32_t>(Sq);
+    prm.Sk = static_cast<int32_t>(Sk);
+    prm.nq = static_cast<int32_t>((Sq + kBQ - 1) / kBQ);
+    prm.causal = causal ? 1 : 0;
+    prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    prm.debug_flags = debug_flags;
+    prm.O = O;
+    prm.status = st;
+    prm.timeout_ns = static_cast<uint64_t>(timeout_ms ? timeout_ms : 1000) * 1000000ull;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(st, 0, sizeof(int), s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(B * H * prm.nq), 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = kSmemBytes;
+    lc.stream = s;
+    void* args[4] = {&tmQ, &tmK, &tmV, &prm};
+    if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    return TSGEMM_OK;
+}
+
+tsgemm_status_t tsattn_forward(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int32_t D, tsgemm_dtype_t dtype,
+                               float scale, int32_t causal, const void* Q, const void* K, const void* V, void* O,
+                               int* status, void* stream) {
+    return tsattn_forward_ex(B, H, Sq, Sk, D, dtype, scale, causal, Q, K, V, O, status, stream, 0, 0);
+}
+
+tsgemm_status_t tsattn_status(void) {
+    using namespace tsg::attn;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_attn_status, sizeof(int)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TSGEMM_ERR_CUDA;
+    }
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return TSGEMM_ERR_CUDA;
+        }
+    }
+    return static_cast<tsgemm_status_t>(word);
+}
+
+}  // extern "C"

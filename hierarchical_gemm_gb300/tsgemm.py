@@ -32,10 +32,11 @@ _DTYPE_NAMES = {"f16": F16, "fp16": F16, "float16": F16, "half": F16,
                 "f32": F32, "fp32": F32, "float32": F32, "float": F32,
                 "e4m3": E4M3, "float8_e4m3fn": E4M3, "e5m2": E5M2, "float8_e5m2": E5M2}
 
-# Every entry point include/tsgemm.h declares.
+# Every entry point include/tsgemm.h and include/tsattn.h declare.
 EXPORTS = ("tsgemm_plan", "tsgemm_plan_ex", "tsgemm_run", "tsgemm_destroy",
            "tsgemm_status", "tsgemm_get_config", "tsgemm_choose_config",
-           "tsgemm_status_string", "tsgemm_run_splitk_noalloc")
+           "tsgemm_status_string", "tsgemm_run_splitk_noalloc",
+           "tsattn_forward", "tsattn_forward_ex", "tsattn_status")
 
 
 class Config(ctypes.Structure):
@@ -78,6 +79,13 @@ def _load():
     L.tsgemm_status_string.argtypes = [i32]
     L.tsgemm_run_splitk_noalloc.restype = i32
     L.tsgemm_run_splitk_noalloc.argtypes = [i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp]
+    f32 = ctypes.c_float
+    L.tsattn_forward.restype = i32
+    L.tsattn_forward.argtypes = [i64, i64, i64, i64, i32, i32, f32, i32, vp, vp, vp, vp, vp, vp]
+    L.tsattn_forward_ex.restype = i32
+    L.tsattn_forward_ex.argtypes = [i64, i64, i64, i64, i32, i32, f32, i32, vp, vp, vp, vp, vp, vp, i32, i32]
+    L.tsattn_status.restype = i32
+    L.tsattn_status.argtypes = []
     return L
 
 
@@ -252,3 +260,35 @@ def run_splitk_noalloc(A, B, C, splits=0, status=None, stream=None):
                                          _ptr(C), _ptr(status), _stream_handle(stream)),
            "tsgemm_run_splitk_noalloc")
     return C
+
+
+def attention(Q, K, V, scale=None, causal=False, O=None, status=None, stream=None, debug_flags=0,
+              timeout_ms=0):
+    """O = softmax(scale * Q K^T) V for CUDA tensors Q (B, H, Sq, D), K and V
+    (B, H, Sk, D), contiguous, all float16 or all bfloat16, D = 128 (the
+    attention block of tsattn.h).  scale defaults to D ** -0.5; `causal`
+    lets query row i see keys t <= i + Sk - Sq.  `status`: an optional
+    device int tensor that receives a device-side timeout."""
+    import torch
+    if Q.dim() != 4 or K.dim() != 4 or V.dim() != 4:
+        raise ValueError("expected Q, K, V of shape (B, H, S, D)")
+    B, H, Sq, D = Q.shape
+    Sk = K.shape[2]
+    if K.shape != (B, H, Sk, D) or V.shape != (B, H, Sk, D):
+        raise ValueError("K and V must be (B, H, Sk, D) with Q's B, H and D")
+    if not (Q.dtype == K.dtype == V.dtype) or not all(x.is_contiguous() for x in (Q, K, V)):
+        raise ValueError("Q, K, V must share a dtype and be contiguous")
+    if scale is None:
+        scale = float(D) ** -0.5
+    if O is None:
+        O = torch.empty_like(Q)
+    _check(lib.tsattn_forward_ex(B, H, Sq, Sk, D, dtype_code(Q.dtype), float(scale), int(bool(causal)),
+                                 _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(status), _stream_handle(stream),
+                                 int(debug_flags), int(timeout_ms)),
+           "tsattn_forward")
+    return O
+
+
+def attention_status():
+    """The library's own attention status word (0 = OK); reading clears it."""
+    return lib.tsattn_status()

@@ -1,0 +1,71 @@
+/*
+ * tsattn.h -- C ABI of the attention block on GB300 (sm_103a).
+ *
+ * Operation.  For every batch b and head h,
+ *
+ *     O[b,h] = softmax(scale * Q[b,h] K[b,h]^T) V[b,h]
+ *
+ * with Q (Sq x D), K and V (Sk x D) and O (Sq x D), the softmax taken over
+ * the keys a query row may see: all of them, or, with `causal`, keys
+ * t <= i + Sk - Sq for query row i (a row that sees no key is zero).  This
+ * is the per-device block of the FlashMLA example of the TileScale README
+ * (section "Example of FlashMLA"): blocks of query rows loop over key /
+ * value blocks, S = Q K^T on the tensor cores, a running row maximum and
+ * row sums (online softmax with base-2 exponentials), the weights cast to
+ * the 16-bit input format and O += P V on the tensor cores, O divided by
+ * the row sums at the end.  The example's multi-GPU context parallelism
+ * and its MLA split of the query into a latent and a rotary part are not
+ * part of this block: here Q K^T runs over one head dimension D.
+ *
+ * Formats.  Q, K, V and O are all fp16 or all bf16 (TSGEMM_F16 /
+ * TSGEMM_BF16 of tsgemm.h); D = 128.  Scores, the softmax and the O
+ * accumulator are fp32; the weights are rounded to the input format before
+ * they multiply V; O is rounded to nearest, ties to even.
+ *
+ * Memory.  Q, K, V, O are device pointers of the current device, 16-byte
+ * aligned, laid out [B][H][S][D] row-major (D contiguous); O must not
+ * overlap Q, K or V.  Nothing is allocated.
+ *
+ * Errors.  Argument errors are returned before anything is launched.
+ * Every device wait is bounded (1 s); an expired wait writes
+ * TSGEMM_ERR_TIMEOUT to `status` (a device int, cleared on `stream` before
+ * the launch) or, when `status` is NULL, to a word of the library that
+ * tsattn_status() reads and clears after the caller has synchronised.
+ */
+#ifndef TSATTN_H
+#define TSATTN_H
+
+#include <stdint.h>
+
+#include "tsgemm.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Enqueue the attention forward pass on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream).  Asynchronous. */
+TSGEMM_API tsgemm_status_t tsattn_forward(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int32_t D,
+                                          tsgemm_dtype_t dtype, float scale, int32_t causal,
+                                          const void* Q, const void* K, const void* V, void* O,
+                                          int* status, void* stream);
+
+/* tsattn_forward with test-only flags (TSGEMM_DEBUG_SKIP_FIRST_LOAD: the
+ * first CTA leaves its first key/value block unloaded, so a bounded wait
+ * runs out) and the limit of every device wait in milliseconds (0: 1 s). */
+TSGEMM_API tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int32_t D,
+                                             tsgemm_dtype_t dtype, float scale, int32_t causal,
+                                             const void* Q, const void* K, const void* V, void* O,
+                                             int* status, void* stream, int32_t debug_flags,
+                                             int32_t timeout_ms);
+
+/* The library's own status word of the current device (used when
+ * tsattn_forward is given status = NULL): TSGEMM_OK or TSGEMM_ERR_TIMEOUT.
+ * Reading it clears it.  Synchronise the stream first. */
+TSGEMM_API tsgemm_status_t tsattn_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSATTN_H */

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "tsgemm.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("tsgemm.h", "tsattn.h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,8 +21,8 @@ def ts():
 
 
 def _declared():
-    text = open(HEADER).read()
-    return set(re.findall(r"TSGEMM_API\s+[\w\s\*]+?\b(tsgemm_\w+)\s*\(", text))
+    text = "".join(open(h).read() for h in HEADERS)
+    return set(re.findall(r"TSGEMM_API\s+[\w\s\*]+?\b(ts(?:gemm|attn)_\w+)\s*\(", text))
 
 
 def test_library_exports_every_declared_symbol(ts):
@@ -348,3 +348,19 @@ def test_cluster_split_rules(ts):
         with pytest.raises(ts.TsgemmError) as e:
             ts.choose_config(*args[:6], layout=args[6], cluster_split=2)
         assert e.value.status == code, args
+
+
+# ---------------------------------------------------------- attention --
+
+def test_attention_argument_checks(ts):
+    # host-side validation runs before any device query
+    f = ts.lib.tsattn_forward
+    p = 256  # a 16-byte aligned dummy address; nothing is launched
+    assert f(0, 1, 1, 1, 128, ts.BF16, 1.0, 0, p, p, p, p, None, None) == ts.ERR_INVALID_ARG
+    assert f(1, 1, 1, 1, 128, ts.BF16, 1.0, 0, None, p, p, p, None, None) == ts.ERR_INVALID_ARG
+    assert f(1, 1, 1, 1, 64, ts.BF16, 1.0, 0, p, p, p, p + 4096, None, None) == ts.ERR_UNSUPPORTED
+    assert f(1, 1, 1, 1, 128, ts.F32, 1.0, 0, p, p, p, p + 4096, None, None) == ts.ERR_UNSUPPORTED
+    assert f(1, 1, 1, 1, 128, ts.BF16, float("nan"), 0, p, p, p, p + 4096, None, None) == ts.ERR_INVALID_ARG
+    assert f(1, 1, 1, 1, 128, ts.BF16, 1.0, 0, p + 8, p, p, p + 4096, None, None) == ts.ERR_ALIGNMENT
+    # O overlapping Q
+    assert f(1, 1, 8, 8, 128, ts.BF16, 1.0, 0, p, p + 8192, p + 16384, p + 256, None, None) == ts.ERR_INVALID_ARG

@@ -1,0 +1,117 @@
+"""Parity of the attention block (softmax(scale Q K^T) V on tcgen05) with
+the fp64 oracle, element by element, under the acceptance rule derived
+from the kernel's arithmetic (oracle.accept_attention)."""
+import time
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import TORCH_DT, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def _tensor(shape, seed, dt, dist=("normal", 1.0)):
+    n = int(np.prod(shape))
+    return synth.matrix(n // D, D, dist, seed, dt).reshape(shape)
+
+
+def _run(Qb, Kb, Vb, dt, scale, causal, **kw):
+    from hierarchical_gemm_gb300 import tsgemm
+    import torch
+    Q, K, V = (to_dev(x.reshape(-1, D), dt).reshape(x.shape) for x in (Qb, Kb, Vb))
+    O = torch.full(Q.shape, float("nan"), dtype=TORCH_DT[dt], device="cuda")
+    tsgemm.attention(Q, K, V, scale=scale, causal=causal, O=O, **kw)
+    torch.cuda.synchronize()
+    st = tsgemm.attention_status()
+    return from_dev(O.reshape(-1, D), dt).reshape(Qb.shape), st
+
+
+def _check(shape_q, shape_k, dt, causal, scale=D ** -0.5, seed=0, dist=("normal", 1.0)):
+    Qb = _tensor(shape_q, 70 + seed, dt, dist)
+    Kb = _tensor(shape_k, 71 + seed, dt, dist)
+    Vb = _tensor(shape_k, 72 + seed, dt)
+    O, st = _run(Qb, Kb, Vb, dt, scale, causal)
+    assert st == 0
+    ref, bound = oracle.attention(Qb, Kb, Vb, dt, scale, causal)
+    ok, info = oracle.accept_attention(O, ref, bound, dt)
+    assert ok, info
+    return O, ref
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,Sq,Sk", [(1, 1, 128, 128), (2, 3, 256, 384), (1, 2, 200, 333), (1, 2, 384, 384)])
+def test_shapes(dt, causal, B, H, Sq, Sk):
+    if causal and Sq > Sk:
+        pytest.skip("covered by test_causal_rows_without_keys")
+    _check((B, H, Sq, D), (B, H, Sk, D), dt, causal)
+
+
+def test_causal_rows_without_keys():
+    # more queries than keys: the first Sq - Sk rows see no key and are zero
+    O, ref = _check((1, 1, 300, D), (1, 1, 200, D), "bf16", True)
+    assert np.all(O[0, 0, :100] == 0)
+
+
+def test_causal_fewer_queries_than_keys():
+    _check((1, 2, 128, D), (1, 2, 320, D), "bf16", True)
+
+
+def test_growing_scores_exercise_the_rescale():
+    # keys grow in magnitude along the sequence, so a row's maximum keeps
+    # rising block after block and the output accumulator is rescaled
+    B, H, Sq, Sk = 1, 2, 256, 1024
+    Qb = _tensor((B, H, Sq, D), 80, "bf16")
+    k = oracle.decode(_tensor((B, H, Sk, D), 81, "bf16"), "bf16")
+    k *= (1.0 + np.arange(Sk) / 128.0)[None, None, :, None]
+    Kb = synth.quantise(k, "bf16")
+    Vb = _tensor((B, H, Sk, D), 82, "bf16")
+    O, st = _run(Qb, Kb, Vb, "bf16", 0.25, False)
+    assert st == 0
+    ref, bound = oracle.attention(Qb, Kb, Vb, "bf16", 0.25, False)
+    ok, info = oracle.accept_attention(O, ref, bound, "bf16")
+    assert ok, info
+
+
+def test_larger_causal_and_repeatable_bits():
+    Qb = _tensor((2, 4, 1024, D), 83, "bf16")
+    Kb = _tensor((2, 4, 1024, D), 84, "bf16")
+    Vb = _tensor((2, 4, 1024, D), 85, "bf16")
+    O1, _ = _run(Qb, Kb, Vb, "bf16", D ** -0.5, True)
+    O2, _ = _run(Qb, Kb, Vb, "bf16", D ** -0.5, True)
+    assert np.array_equal(O1, O2)
+    ref, bound = oracle.attention(Qb, Kb, Vb, "bf16", D ** -0.5, True)
+    ok, info = oracle.accept_attention(O1, ref, bound, "bf16")
+    assert ok, info
+
+
+def test_uniform_queries_average_the_values():
+    # Q = 0: every visible key weighs the same
+    Qb = synth.quantise(np.zeros((1, 1, 256, D)), "bf16")
+    Kb = _tensor((1, 1, 512, D), 86, "bf16")
+    Vb = _tensor((1, 1, 512, D), 87, "bf16")
+    O, _ = _run(Qb, Kb, Vb, "bf16", 1.0, False)
+    want = oracle.decode(Vb, "bf16").mean(axis=2)
+    got = oracle.decode(O, "bf16")
+    assert np.all(np.abs(got - want[:, :, None]) <= 2.0 ** -7 * np.abs(want[:, :, None]) + 1e-3)
+
+
+def test_expired_wait_reports_timeout_and_the_context_survives():
+    import torch
+    from hierarchical_gemm_gb300 import tsgemm
+    Qb = _tensor((1, 2, 256, D), 88, "bf16")
+    Kb = _tensor((1, 2, 256, D), 89, "bf16")
+    Vb = _tensor((1, 2, 256, D), 90, "bf16")
+    Q, K, V = (to_dev(x.reshape(-1, D), "bf16").reshape(x.shape) for x in (Qb, Kb, Vb))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    tsgemm.attention(Q, K, V, status=status, debug_flags=tsgemm.DEBUG_SKIP_FIRST_LOAD, timeout_ms=50)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 10.0
+    assert int(status.item()) == tsgemm.ERR_TIMEOUT
+    _check((1, 2, 256, D), (1, 2, 256, D), "bf16", False, seed=18)
