@@ -32,6 +32,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -498,9 +500,163 @@ def run_ours(args):
     }
 
 
+# ------------------------------------------------------------ attention --
+
+ATTN_METRIC = "attention TFLOP/s (4 D flops per visible query-key pair)"
+
+
+def attn_inputs(w, off=0):
+    """Q, K, V bit patterns (B, H, S, D) of an attention workload, N(0, 1)."""
+    import synth
+    D = w["D"]
+
+    def mk(shape, seed):
+        return synth.matrix(int(np.prod(shape)) // D, D, ("normal", 1.0), seed + off, w["dtype"]).reshape(shape)
+    shape_q = (w["B"], w["H"], w["Sq"], D)
+    shape_k = (w["B"], w["H"], w["Sk"], D)
+    return mk(shape_q, w["seed_q"]), mk(shape_k, w["seed_k"]), mk(shape_k, w["seed_v"])
+
+
+def attn_sample_flops(w, rows=128):
+    """Flops of attn_oracle_sample: 4 D per visible pair of the last rows."""
+    Sq, Sk = w["Sq"], w["Sk"]
+    i = np.arange(Sq - rows, Sq, dtype=np.int64)
+    pairs = np.clip(i + Sk - Sq + 1, 0, Sk).sum() if w["causal"] else rows * Sk
+    return 4.0 * w["D"] * float(pairs)
+
+
+def run_attention_reference(args):
+    """The oracle timed as the reference arm on an attention workload: every
+    step is the last 128 query rows of one head."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import synth
+    w = synth.attn_workload(args.workload)
+    Qb, Kb, Vb = attn_inputs(w)
+    for _ in range(args.warmup):
+        attn_oracle_sample(w, Qb, Kb, Vb)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        attn_oracle_sample(w, Qb, Kb, Vb)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = attn_sample_flops(w) / dt / 1e12
+    return {
+        "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "Sq": w["Sq"], "Sk": w["Sk"], "D": w["D"],
+                   "causal": w["causal"], "sample_rows": 128},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": "the last 128 query rows of head (0, 0) per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def attn_oracle_sample(w, Qb, Kb, Vb, rows=128):
+    """The oracle on the last `rows` query rows of head (0, 0) (the causal
+    limit t <= i + Sk - Sq is unchanged when the first rows are dropped)."""
+    import oracle
+    q = np.ascontiguousarray(Qb[:1, :1, -rows:])
+    return oracle.attention(q, Kb[:1, :1], Vb[:1, :1], w["dtype"], w["D"] ** -0.5, w["causal"])
+
+
+def run_attention(args):
+    import numpy as np  # noqa: F811
+    import torch
+
+    import oracle
+    import synth
+    from hierarchical_gemm_gb300 import tsgemm
+
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = synth.attn_workload(args.workload)
+    Qb, Kb, Vb = attn_inputs(w, rank_seed_offset(rank))
+    D, dt = w["D"], w["dtype"]
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dt]
+    to = lambda x: torch.from_numpy(x.reshape(-1).view(np.int16)).to(dev).view(tdt).reshape(x.shape)  # noqa: E731
+    Q, K, V = to(Qb), to(Kb), to(Vb)
+    O = torch.empty_like(Q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = D ** -0.5
+    for _ in range(args.warmup):
+        flush.zero_()
+        tsgemm.attention(Q, K, V, scale=scale, causal=w["causal"], O=O, status=status, stream=stream)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local) if rank == 0 or world > 1 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        tsgemm.attention(Q, K, V, scale=scale, causal=w["causal"], O=O, status=status, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t1 = time.time()
+    clocks = None
+    if sampler:
+        sampler.mark(t0, t1)
+        clocks = sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError("attention device status %d" % int(status.item()))
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    ms_max = max_over_ranks(ms, world, dev)
+    value = aggregate_tflops(w["flops"], ms_max, world)
+    parity = None
+    if rank == 0:
+        ref, bound = attn_oracle_sample(w, Qb, Kb, Vb)
+        got = O[:1, :1, -128:].cpu().reshape(-1).view(torch.int16).numpy().view(np.uint16).reshape(ref.shape)
+        ok, info = oracle.accept_attention(got, ref, bound, dt)
+        parity = {"sampled_outputs": int(ref.size), "ok": bool(ok),
+                  "max_err_over_bound": info.get("max_err_over_bound")}
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    achieved = w["flops"] / (ms * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t_c = time.perf_counter()
+        attn_oracle_sample(w, Qb, Kb, Vb)
+        dt_c = time.perf_counter() - t_c
+        cpu = {"value": attn_sample_flops(w) / dt_c / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": "the last 128 query rows of one head (%.2f s)" % dt_c}
+    if rank != 0:
+        return None
+    return {
+        "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "Sq": w["Sq"], "Sk": w["Sk"], "D": D,
+                   "causal": w["causal"], "l2": "flushed between steps (256 MB write)",
+                   "parallelism": "independent replica per GPU" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": peak_kind + " bf16 burst (cuBLAS-class torch.matmul)",
+                     "kernel": "attn_fwd_sm103", "algorithmic_flops_per_launch": w["flops"]},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clocks, "parity": parity,
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.workload.startswith("attn_"):
+        out = run_attention_reference(args) if args.impl == "reference" else run_attention(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
     rank, world, _ = dist_env()

@@ -9,11 +9,14 @@
 //   * S_j = Q K_j^T is computed by tcgen05.mma into one of two tensor-memory
 //     score buffers (acc_s of the example), so that the scores of block j+1
 //     are computed while block j's softmax runs;
-//   * one warpgroup, a thread per query row, reads its row of S_j, keeps the
-//     running maximum (scores_max) and row sum (logsum) in base-2 units,
-//     writes P_j = 2^(t - m) rounded to the 16-bit input format into shared
-//     memory (acc_s_cast) and, when its maximum has grown, rescales its row
-//     of the output accumulator (scores_scale);
+//   * two warpgroups, two threads per query row, read the row of S_j; both
+//     take the row maximum over all 128 scores (scores_max), so they agree
+//     on it without exchanging anything, and each exponentiates its half of
+//     the keys: P_j = 2^(t - m) rounded to the 16-bit input format into
+//     shared memory (acc_s_cast), its partial row sum (logsum), and, when
+//     the maximum has grown, its half of the row of the output accumulator
+//     rescaled (scores_scale) -- the split of acc_s between warpgroups of
+//     the example, with the maximum recomputed instead of all-gathered;
 //   * O += P_j V_j is computed by tcgen05.mma into a tensor-memory
 //     accumulator (acc_o); at the end each thread divides its row by the
 //     row sum and stores it.
@@ -24,7 +27,7 @@
 // weight, so the result is the same softmax.
 //
 // Warp roles: warp 0 lane 0 issues the TMA loads, warp 1 lane 0 the MMAs,
-// warps 2-5 run the softmax and the epilogue.  Every wait is bounded in time
+// warps 2-9 (two warpgroups) run the softmax and the epilogue.  Every wait is bounded in time
 // (WaitCtl); a CTA that gives up records a timeout, lets its copies and MMAs
 // finish, frees tensor memory and returns.
 #include <cuda.h>
@@ -41,7 +44,8 @@ namespace attn {
 constexpr int kBQ = 128;                // query rows per CTA (TMEM lanes)
 constexpr int kBKV = 128;               // keys per block
 constexpr int kD = 128;                 // head dimension
-constexpr int kThreads = 192;           // producer warp, MMA warp, softmax warpgroup
+constexpr int kThreads = 320;           // producer warp, MMA warp, two softmax warpgroups
+constexpr int kSoftThreads = 256;
 constexpr uint32_t kAtom = 128u * 128u; // 128 rows x 128 bytes: one swizzle atom column
 constexpr uint32_t kTile = 2u * kAtom;  // 128 rows x 128 16-bit elements
 constexpr uint32_t kQOff = 0;
@@ -86,6 +90,161 @@ __host__ __device__ constexpr uint32_t idesc(bool f16, bool b_nmajor) {
            ((128u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
+struct SoftCtx {
+    const AttnParams& p;
+    uint32_t base;   // shared memory (1024-aligned)
+    uint32_t tmem;   // tensor memory base
+    int qb, bh, nkv;
+    int lane, quarter;
+    const WaitCtl& ctl;
+};
+
+// One softmax thread: query row (quarter * 32 + lane) of the block, keys
+// [64 kG, 64 kG + 64) of every key block and the same output columns.
+template <bool kF16, int kG>
+__device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
+    const AttnParams& p = sc.p;
+    auto s_full = [&](int b) { return bars + 8u * (5 + b); };
+    auto s_free = [&](int b) { return bars + 8u * (7 + b); };
+    auto p_full = [&](int b) { return bars + 8u * (9 + b); };
+    auto p_free = [&](int b) { return bars + 8u * (11 + b); };
+    const int lane = sc.lane;
+    const int r = sc.quarter * 32 + lane;  // query row within the block
+    const int qrow = sc.qb * kBQ + r;
+    const uint32_t trow = sc.tmem + (static_cast<uint32_t>(sc.quarter * 32) << 16);
+    const int kv_last = p.causal ? qrow + p.Sk - p.Sq : p.Sk - 1;  // last key this row sees
+    const float c2 = p.scale_log2;
+    // a bounded wait taken by lane 0 for the whole warp
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        int good = 1;
+        if (lane == 0) good = wait_bounded(bar, parity, sc.ctl) ? 1 : 0;
+        return __shfl_sync(0xffffffffu, good, 0) != 0;
+    };
+    float m_used = -INFINITY;  // base-2 maximum the weights are taken against
+    float l = 0.0f;            // sum of this thread's weights
+    bool ok = true;
+    for (int j = 0; j < sc.nkv; ++j) {
+        const int sb = j & 1, pb = j & 1;
+        if (!warp_wait(s_full(sb), static_cast<uint32_t>(j >> 1) & 1u)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        uint32_t s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c);
+            tmem_ld_32x32b_x32(trow + sb * 128u + 32u * c, part);
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(s_free(sb));  // the score buffer may be overwritten
+        // keys past Sk or past the causal limit weigh nothing
+        const int k0 = j * kBKV;
+        if (!(k0 + kBKV - 1 <= kv_last && k0 + kBKV <= p.Sk)) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+                if (k0 + c > kv_last || k0 + c >= p.Sk) s[c] = __float_as_uint(-INFINITY);
+        }
+        float mb = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mb = fmaxf(mb, __uint_as_float(s[c]));
+        const float m_new = fmaxf(m_used, mb * c2);  // (c2 > 0)
+        const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+            // every lane of the warp moves to its own new maximum
+            const float alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m_new);
+            if (m_new > -INFINITY) m_used = m_new;
+            l *= alpha;
+            if (j >= 1) {
+                // O holds P_0 V_0 + ... + P_{j-1} V_{j-1}: wait for the last,
+                // then scale this thread's half of the row
+                if (!warp_wait(p_free((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 64 * kG; c < 64 * kG + 64; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(trow + kOCol + c, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_32x32b_x32(trow + kOCol + c, o);
+                }
+                tmem_st_wait();
+            }
+        }
+        // P_j goes to buffer pb once P V of block j - 2 has read it
+        if (j >= 2 && !warp_wait(p_free(pb), static_cast<uint32_t>((j - 2) >> 1) & 1u)) {
+            ok = false;
+            break;
+        }
+        // p = 2^(c2 s - m): one fused multiply-add per weight; before any
+        // visible key, m = +inf makes every weight 0
+        const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
+        const uint32_t prow = sc.base + kPOff + pb * kTile + kG * kAtom + static_cast<uint32_t>(r) * 128u;
+        float rs = 0.0f;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = 64 * kG + 8 * c8 + 2 * e;
+                const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c2, mneg));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c2, mneg));
+                rs += p0 + p1;
+                w[e] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            }
+            // K-major, 128-byte swizzle: 16-byte chunk c8 of row r at chunk
+            // position c8 ^ (r mod 8)
+            st_shared_v4(prow + ((static_cast<uint32_t>(c8) ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+        }
+        l += rs;
+        fence_proxy_async_shared();  // the P writes are visible to the tensor core
+        tc_fence_before();
+        mbar_arrive(p_full(pb));
+    }
+    // ---------------------------------------------------- epilogue --
+    if (ok && sc.nkv > 0 && !warp_wait(p_free((sc.nkv - 1) & 1), static_cast<uint32_t>((sc.nkv - 1) >> 1) & 1u))
+        ok = false;
+    // the row sum is the two halves' sums (same maximum): exchange them
+    // through the P buffers, which every P V has finished reading
+    const uint32_t lx = sc.base + kPOff;  // [2][128] floats
+    if (ok) asm volatile("st.shared.f32 [%0], %1;" ::"r"(lx + (kG * 128 + r) * 4u), "f"(l) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftThreads) : "memory");
+    if (!ok) return;
+    float lo;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(lo) : "r"(lx + ((1 - kG) * 128 + r) * 4u) : "memory");
+    const float lt = l + lo;
+    tc_fence_after();
+    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+    uint16_t* orow = static_cast<uint16_t*>(p.O) + (static_cast<int64_t>(sc.bh) * p.Sq + qrow) * kD;
+#pragma unroll
+    for (int c = 64 * kG; c < 64 * kG + 64; c += 32) {
+        uint32_t o[32];
+        if (sc.nkv > 0) {
+            tmem_ld_32x32b_x32(trow + kOCol + c, o);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float a = __uint_as_float(o[2 * i]) * inv, b = __uint_as_float(o[2 * i + 1]) * inv;
+            w[i] = kF16 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
+        }
+        if (qrow < p.Sq) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                st_global_v4(orow + c + 8 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+    }
+}
+
 template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -121,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full(b), 1);
-            mbar_init(s_free(b), kBQ);  // every softmax thread
-            mbar_init(p_full(b), kBQ);
+            mbar_init(s_free(b), kSoftThreads);  // every softmax thread
+            mbar_init(p_full(b), kSoftThreads);
             mbar_init(p_free(b), 1);
         }
         mbar_init(drain_bar, 1);
@@ -221,137 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------- softmax and epilogue --
-        const int quarter = warp & 3;                 // TMEM lane quarter of this warp
-        const int r = quarter * 32 + lane;            // query row within the block
-        const int qrow = qb * kBQ + r;
-        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const int kv_last = p.causal ? qrow + p.Sk - p.Sq : p.Sk - 1;  // last key this row sees
-        // a bounded wait taken by lane 0 for the whole warp
-        auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
-            int good = 1;
-            if (lane == 0) good = wait_bounded(bar, parity, ctl) ? 1 : 0;
-            return __shfl_sync(0xffffffffu, good, 0) != 0;
-        };
-        float m_used = -INFINITY;  // base-2 maximum the weights are taken against
-        float l = 0.0f;            // sum of this row's weights
-        bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            const int sb = j & 1, pb = j & 1;
-            if (!warp_wait(s_full(sb), static_cast<uint32_t>(j >> 1) & 1u)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c);
-                tmem_ld_32x32b_x32(trow + sb * 128u + 32u * c, part);
-            }
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(s_free(sb));  // the score buffer may be overwritten
-            // scores to base-2 units; keys past Sk or past the causal limit
-            // weigh nothing
-            const int k0 = j * kBKV;
-            const bool whole = k0 + kBKV - 1 <= kv_last && k0 + kBKV <= p.Sk;
-            float mb = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                float x = __uint_as_float(s[c]) * p.scale_log2;
-                if (!whole && (k0 + c > kv_last || k0 + c >= p.Sk)) x = -INFINITY;
-                s[c] = __float_as_uint(x);
-                mb = fmaxf(mb, x);
-            }
-            const float m_new = fmaxf(m_used, mb);
-            const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
-            if (__any_sync(0xffffffffu, need)) {
-                // every lane of the warp moves to its own new maximum
-                const float alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m_new);
-                if (m_new > -INFINITY) m_used = m_new;
-                l *= alpha;
-                if (j >= 1) {
-                    // O holds P_0 V_0 + ... + P_{j-1} V_{j-1}: wait for the last,
-                    // then scale this row
-                    if (!warp_wait(p_free((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < 128; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld_32x32b_x32(trow + kOCol + c, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st_32x32b_x32(trow + kOCol + c, o);
-                    }
-                    tmem_st_wait();
-                }
-            }
-            // P_j goes to buffer pb once P V of block j - 2 has read it
-            if (j >= 2 && !warp_wait(p_free(pb), static_cast<uint32_t>((j - 2) >> 1) & 1u)) {
-                ok = false;
-                break;
-            }
-            const uint32_t pbase = base + kPOff + pb * kTile + static_cast<uint32_t>(r) * 128u;
-            float rs = 0.0f;
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 64 * a + 8 * c8 + 2 * e;
-                        const float x0 = __uint_as_float(s[c]), x1 = __uint_as_float(s[c + 1]);
-                        const float p0 = m_used == -INFINITY ? 0.0f : ex2_approx(x0 - m_used);
-                        const float p1 = m_used == -INFINITY ? 0.0f : ex2_approx(x1 - m_used);
-                        rs += p0 + p1;
-                        w[e] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-                    }
-                    // K-major, 128-byte swizzle: 16-byte chunk c8 of row r at
-                    // chunk position c8 ^ (r mod 8)
-                    st_shared_v4(pbase + a * kAtom + ((static_cast<uint32_t>(c8) ^ (r & 7)) << 4), w[0], w[1], w[2],
-                                 w[3]);
-                }
-            }
-            l += rs;
-            fence_proxy_async_shared();  // the P writes are visible to the tensor core
-            tc_fence_before();
-            mbar_arrive(p_full(pb));
-        }
-        // -------------------------------------------------- epilogue --
-        if (ok && nkv > 0 && !warp_wait(p_free((nkv - 1) & 1), static_cast<uint32_t>((nkv - 1) >> 1) & 1u))
-            ok = false;
-        if (ok) {
-            tc_fence_after();
-            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            uint16_t* orow = static_cast<uint16_t*>(p.O) + (static_cast<int64_t>(bh) * p.Sq + qrow) * kD;
-#pragma unroll 1
-            for (int c = 0; c < 128; c += 32) {
-                uint32_t o[32];
-                if (nkv > 0) {
-                    tmem_ld_32x32b_x32(trow + kOCol + c, o);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0u;
-                }
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float lo = __uint_as_float(o[2 * i]) * inv, hi = __uint_as_float(o[2 * i + 1]) * inv;
-                    w[i] = kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
-                }
-                if (qrow < p.Sq) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        st_global_v4(orow + c + 8 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-                }
-            }
-        }
+        const SoftCtx sc{p, base, tmem, qb, bh, nkv, lane, warp & 3, ctl};
+        if (warp < 6)
+            softmax_role<kF16, 0>(sc, bars);
+        else
+            softmax_role<kF16, 1>(sc, bars);
     }
 
     // ------------------------------------------------------------ exit --

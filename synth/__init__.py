@@ -125,4 +125,5 @@ def matrix(rows, cols, dist, seed, dtype, out=None):
     return out
 
 
-from .workloads import WORKLOADS, EXTRA_WORKLOADS, workload, inputs, stored  # noqa: E402,F401
+from .workloads import (WORKLOADS, EXTRA_WORKLOADS, ATTN_WORKLOADS, workload, attn_workload,  # noqa: E402,F401
+                        inputs, stored)

@@ -51,6 +51,38 @@ EXTRA_WORKLOADS = {
 }
 
 
+# The attention block (softmax(scale Q K^T) V): Q, K, V of shape (B, H, S, D)
+# drawn from N(0, 1), scale D^-1/2.  Seeds as above (Q: the A seed, K: the
+# B seed, V: the B seed + 0x100).
+ATTN_WORKLOADS = {
+    "attn_b4h32s4096d128_bf16": dict(
+        index=7, B=4, H=32, Sq=4096, Sk=4096, D=128, dtype="bf16", causal=False),
+    "attn_b4h32s4096d128_causal_bf16": dict(
+        index=8, B=4, H=32, Sq=4096, Sk=4096, D=128, dtype="bf16", causal=True),
+    # a smaller case for profiler captures (still 3 x 64 MiB, larger than L2)
+    "attn_b2h16s4096d128_bf16": dict(
+        index=9, B=2, H=16, Sq=4096, Sk=4096, D=128, dtype="bf16", causal=False),
+}
+
+
+def attn_workload(name):
+    w = dict(ATTN_WORKLOADS[name])
+    w["name"] = name
+    w["seed_q"] = _SEED_BASE + w["index"]
+    w["seed_k"] = _SEED_BASE + w["index"] + 0x100
+    w["seed_v"] = _SEED_BASE + w["index"] + 0x200
+    # score / weighted-sum pairs a row visits: all keys, or the causal
+    # t <= i + Sk - Sq
+    Sq, Sk = w["Sq"], w["Sk"]
+    if w["causal"]:
+        i = np.arange(Sq, dtype=np.int64)
+        pairs = int(np.clip(i + Sk - Sq + 1, 0, Sk).sum())
+    else:
+        pairs = Sq * Sk
+    w["flops"] = 4 * w["B"] * w["H"] * pairs * w["D"]
+    return w
+
+
 def workload(name):
     w = dict(WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name])
     w.setdefault("layout", "rrr")
