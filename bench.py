@@ -216,9 +216,13 @@ def measured_peaks():
         return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
 
 
-def kernel_source_hash():
+ATTN_SOURCES = ["hierarchical_gemm_gb300/csrc/attention_sm103.cu",
+                "hierarchical_gemm_gb300/csrc/ptx.cuh"]
+
+
+def kernel_source_hash(sources=None):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -226,7 +230,7 @@ def kernel_source_hash():
 
 def stored_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    with the current kernel source; else None."""
+    with the current kernel source (the files the entry names); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -234,7 +238,7 @@ def stored_traffic(workload):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(e.get("sources")):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -644,9 +648,10 @@ def run_attention(args):
                    "causal": w["causal"], "l2": "flushed between steps (256 MB write)",
                    "parallelism": "independent replica per GPU" if world > 1 else "1 GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": stored_traffic(w["name"]),
                      "peak_kind": peak_kind + " bf16 burst (cuBLAS-class torch.matmul)",
-                     "kernel": "attn_fwd_sm103", "algorithmic_flops_per_launch": w["flops"]},
+                     "kernel": "attn_fwd_sm103", "algorithmic_flops_per_launch": w["flops"],
+                     "algorithmic_bytes_per_launch": 2 * 4 * w["B"] * w["H"] * max(w["Sq"], w["Sk"]) * w["D"]},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clocks, "parity": parity,
     }
 
