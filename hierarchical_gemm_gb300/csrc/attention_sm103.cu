@@ -5,7 +5,10 @@
 // README (section "Example of FlashMLA"), laid out for sm_103a:
 //   * a CTA owns 128 query rows of one (batch, head): Q is loaded once by
 //     TMA into shared memory (128-byte swizzle);
-//   * key / value blocks of 128 rows stream through a two-slot ring;
+//   * key and value blocks of 128 rows stream through two-slot rings of
+//     their own: a K slot is free once S = Q K^T has read it, a V slot once
+//     O += P V has, so the next keys load while this block's softmax and
+//     P V still run;
 //   * S_j = Q K_j^T is computed by tcgen05.mma into one of two tensor-memory
 //     score buffers (acc_s of the example), so that the scores of block j+1
 //     are computed while block j's softmax runs;
@@ -54,7 +57,7 @@ constexpr uint32_t kSlotBytes = 2u * kTile;
 constexpr int kSlots = 2;
 constexpr uint32_t kPOff = kKVOff + kSlots * kSlotBytes;  // two P buffers
 constexpr uint32_t kBarOff = kPOff + 2u * kTile;
-constexpr int kNumBars = 14;
+constexpr int kNumBars = 18;
 constexpr uint32_t kMiscOff = kBarOff + 8u * kNumBars;
 constexpr uint32_t kSmemBytes = 1024u + kMiscOff + 16u;
 constexpr uint32_t kTmemCols = 512;     // S buffers at columns 0 and 128, O at 256
@@ -146,9 +149,18 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
             for (int c = 0; c < 128; ++c)
                 if (k0 + c > kv_last || k0 + c >= p.Sk) s[c] = __float_as_uint(-INFINITY);
         }
-        float mb = -INFINITY;
+        // row maximum: eight independent chains, then a tree (short
+        // dependency chains matter with two warps per scheduler)
+        float mx[8];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mb = fmaxf(mb, __uint_as_float(s[c]));
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
+#pragma unroll
+        for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(s[c + i]));
+        }
+        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m_used, mb * c2);  // (c2 > 0)
         const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
@@ -185,7 +197,9 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
         // visible key, m = +inf makes every weight 0
         const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
         const uint32_t prow = sc.base + kPOff + pb * kTile + kG * kAtom + static_cast<uint32_t>(r) * 128u;
-        float rs = 0.0f;
+        float rsum[8];  // eight independent partial sums, added in a fixed order
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
             uint32_t w[4];
@@ -194,14 +208,15 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
                 const int c = 64 * kG + 8 * c8 + 2 * e;
                 const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c2, mneg));
                 const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c2, mneg));
-                rs += p0 + p1;
+                rsum[2 * e] += p0;
+                rsum[2 * e + 1] += p1;
                 w[e] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
             // K-major, 128-byte swizzle: 16-byte chunk c8 of row r at chunk
             // position c8 ^ (r mod 8)
             st_shared_v4(prow + ((static_cast<uint32_t>(c8) ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
         }
-        l += rs;
+        l += ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
         fence_proxy_async_shared();  // the P writes are visible to the tensor core
         tc_fence_before();
         mbar_arrive(p_full(pb));
@@ -255,13 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t bars = base + kBarOff;
     const uint32_t q_full = bars;
-    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto kv_empty = [&](int s) { return bars + 8u * (3 + s); };
     auto s_full = [&](int b) { return bars + 8u * (5 + b); };
     auto s_free = [&](int b) { return bars + 8u * (7 + b); };
     auto p_full = [&](int b) { return bars + 8u * (9 + b); };
     auto p_free = [&](int b) { return bars + 8u * (11 + b); };  // PV on buffer b done
     const uint32_t drain_bar = bars + 8u * 13;
+    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto k_empty = [&](int s) { return bars + 8u * (3 + s); };
+    auto v_full = [&](int s) { return bars + 8u * (14 + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (16 + s); };
     uint8_t* misc = base_ptr + kMiscOff;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -275,8 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full(b), 1);
@@ -302,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0 && nkv > 0) {
+            // outstanding loads per slot: bits 0-1 K, bits 2-3 V
             uint32_t outstanding = 0, out_par = 0;
             mbar_arrive_expect_tx(q_full, kTile);
             tma_load_3d(qs, &tmQ, q_full, 0, qb * kBQ, bh);
@@ -309,22 +329,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nkv; ++j) {
                 const int st = j & 1;
                 const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                if (!wait_bounded(kv_empty(st), ph ^ 1u, ctl)) break;
-                // tests only: the first CTA leaves its first block unloaded
-                if ((p.debug_flags & 1) && blockIdx.x == 0 && j == 0) continue;
                 const uint32_t ks = base + kKVOff + st * kSlotBytes, vs = ks + kTile;
-                mbar_arrive_expect_tx(kv_full(st), 2u * kTile);
-                tma_load_3d(ks, &tmK, kv_full(st), 0, j * kBKV, bh);
-                tma_load_3d(ks + kAtom, &tmK, kv_full(st), 64, j * kBKV, bh);
-                tma_load_3d(vs, &tmV, kv_full(st), 0, j * kBKV, bh);
-                tma_load_3d(vs + kAtom, &tmV, kv_full(st), 64, j * kBKV, bh);
-                outstanding |= 1u << st;
-                out_par = (out_par & ~(1u << st)) | (ph << st);
+                // tests only: the first CTA leaves its first key block unloaded
+                const bool skip = (p.debug_flags & 1) && blockIdx.x == 0 && j == 0;
+                if (!wait_bounded(k_empty(st), ph ^ 1u, ctl)) break;
+                if (!skip) {
+                    mbar_arrive_expect_tx(k_full(st), kTile);
+                    tma_load_3d(ks, &tmK, k_full(st), 0, j * kBKV, bh);
+                    tma_load_3d(ks + kAtom, &tmK, k_full(st), 64, j * kBKV, bh);
+                    outstanding |= 1u << st;
+                    out_par = (out_par & ~(1u << st)) | (ph << st);
+                }
+                if (!wait_bounded(v_empty(st), ph ^ 1u, ctl)) break;
+                mbar_arrive_expect_tx(v_full(st), kTile);
+                tma_load_3d(vs, &tmV, v_full(st), 0, j * kBKV, bh);
+                tma_load_3d(vs + kAtom, &tmV, v_full(st), 64, j * kBKV, bh);
+                outstanding |= 4u << st;
+                out_par = (out_par & ~(4u << st)) | (ph << (st + 2));
             }
             // every copy this thread started lands before the CTA exits
             wait_bounded(q_full, 0u, ctl, false);
-            for (int s = 0; s < kSlots; ++s)
-                if (outstanding & (1u << s)) wait_bounded(kv_full(s), (out_par >> s) & 1u, ctl, false);
+            for (int s = 0; s < kSlots; ++s) {
+                if (outstanding & (1u << s)) wait_bounded(k_full(s), (out_par >> s) & 1u, ctl, false);
+                if (outstanding & (4u << s)) wait_bounded(v_full(s), (out_par >> (s + 2)) & 1u, ctl, false);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -338,7 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // apart, the k-th 16-key step 2 KiB further.
             auto issue_pv = [&](int i) -> bool {
                 const int pb = i & 1;
-                if (!wait_bounded(p_full(pb), static_cast<uint32_t>(i >> 1) & 1u, ctl)) return false;
+                const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
+                if (!wait_bounded(v_full(i & 1), ph, ctl) || !wait_bounded(p_full(pb), ph, ctl)) return false;
                 tc_fence_after();
                 const uint32_t ps = base + kPOff + pb * kTile;
                 const uint32_t vs = base + kKVOff + (i & 1) * kSlotBytes + kTile;
@@ -349,13 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_f16<1>(tmem + kOCol, ad, bd, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
                 }
                 umma_commit(p_free(pb));          // P buffer read; O holds PV_0..PV_i
-                umma_commit(kv_empty(i & 1));     // K_i and V_i read
+                umma_commit(v_empty(i & 1));      // V_i read
                 return true;
             };
             for (int j = 0; ok && j < nkv; ++j) {
                 const int st = j & 1, sb = j & 1;
                 const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                if (!wait_bounded(kv_full(st), ph, ctl) || !wait_bounded(s_free(sb), ph ^ 1u, ctl)) {
+                if (!wait_bounded(k_full(st), ph, ctl) || !wait_bounded(s_free(sb), ph ^ 1u, ctl)) {
                     ok = false;
                     break;
                 }
@@ -370,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_f16<1>(tmem + sb * 128u, ad, bd, kIdS, k > 0 ? 1u : 0u);
                 }
                 umma_commit(s_full(sb));
+                umma_commit(k_empty(st));  // K_j read
                 if (j >= 1 && !issue_pv(j - 1)) ok = false;
             }
             if (ok) issue_pv(nkv - 1);
