@@ -29,8 +29,10 @@
 // 16-bit formats, and the final division uses the same maximum as every
 // weight, so the result is the same softmax.
 //
-// Warp roles: warp 0 lane 0 issues the TMA loads, warp 1 lane 0 the MMAs,
-// warps 2-9 (two warpgroups) run the softmax and the epilogue.  Every wait is bounded in time
+// Warp roles: warp 0 lane 0 loads Q and the key blocks, warp 10 lane 0 the
+// value blocks (so that a key load never waits behind a value slot), warp 1
+// lane 0 issues the MMAs, warps 2-9 (two warpgroups) run the softmax and the
+// epilogue.  Every wait is bounded in time
 // (WaitCtl); a CTA that gives up records a timeout, lets its copies and MMAs
 // finish, frees tensor memory and returns.
 #include <cuda.h>
@@ -47,7 +49,7 @@ namespace attn {
 constexpr int kBQ = 128;                // query rows per CTA (TMEM lanes)
 constexpr int kBKV = 128;               // keys per block
 constexpr int kD = 128;                 // head dimension
-constexpr int kThreads = 320;           // producer warp, MMA warp, two softmax warpgroups
+constexpr int kThreads = 352;           // K producer, MMA, two softmax warpgroups, V producer
 constexpr int kSoftThreads = 256;
 constexpr uint32_t kAtom = 128u * 128u; // 128 rows x 128 bytes: one swizzle atom column
 constexpr uint32_t kTile = 2u * kAtom;  // 128 rows x 128 16-bit elements
@@ -318,41 +320,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     const uint32_t qs = base + kQOff;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer --
+    if (warp == 0 || warp == 10) {
+        // --------------------------------- TMA producers: Q and K / V --
+        const bool is_k = warp == 0;
         if (lane == 0 && nkv > 0) {
-            // outstanding loads per slot: bits 0-1 K, bits 2-3 V
-            uint32_t outstanding = 0, out_par = 0;
-            mbar_arrive_expect_tx(q_full, kTile);
-            tma_load_3d(qs, &tmQ, q_full, 0, qb * kBQ, bh);
-            tma_load_3d(qs + kAtom, &tmQ, q_full, 64, qb * kBQ, bh);
+            uint32_t outstanding = 0, out_par = 0;  // loads per slot
+            if (is_k) {
+                mbar_arrive_expect_tx(q_full, kTile);
+                tma_load_3d(qs, &tmQ, q_full, 0, qb * kBQ, bh);
+                tma_load_3d(qs + kAtom, &tmQ, q_full, 64, qb * kBQ, bh);
+            }
+            const CUtensorMap* map = is_k ? &tmK : &tmV;
             for (int j = 0; j < nkv; ++j) {
                 const int st = j & 1;
                 const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                const uint32_t ks = base + kKVOff + st * kSlotBytes, vs = ks + kTile;
+                const uint32_t dst = base + kKVOff + st * kSlotBytes + (is_k ? 0u : kTile);
+                const uint32_t full = is_k ? k_full(st) : v_full(st);
+                if (!wait_bounded(is_k ? k_empty(st) : v_empty(st), ph ^ 1u, ctl)) break;
                 // tests only: the first CTA leaves its first key block unloaded
-                const bool skip = (p.debug_flags & 1) && blockIdx.x == 0 && j == 0;
-                if (!wait_bounded(k_empty(st), ph ^ 1u, ctl)) break;
-                if (!skip) {
-                    mbar_arrive_expect_tx(k_full(st), kTile);
-                    tma_load_3d(ks, &tmK, k_full(st), 0, j * kBKV, bh);
-                    tma_load_3d(ks + kAtom, &tmK, k_full(st), 64, j * kBKV, bh);
-                    outstanding |= 1u << st;
-                    out_par = (out_par & ~(1u << st)) | (ph << st);
-                }
-                if (!wait_bounded(v_empty(st), ph ^ 1u, ctl)) break;
-                mbar_arrive_expect_tx(v_full(st), kTile);
-                tma_load_3d(vs, &tmV, v_full(st), 0, j * kBKV, bh);
-                tma_load_3d(vs + kAtom, &tmV, v_full(st), 64, j * kBKV, bh);
-                outstanding |= 4u << st;
-                out_par = (out_par & ~(4u << st)) | (ph << (st + 2));
+                if (is_k && (p.debug_flags & 1) && blockIdx.x == 0 && j == 0) continue;
+                mbar_arrive_expect_tx(full, kTile);
+                tma_load_3d(dst, map, full, 0, j * kBKV, bh);
+                tma_load_3d(dst + kAtom, map, full, 64, j * kBKV, bh);
+                outstanding |= 1u << st;
+                out_par = (out_par & ~(1u << st)) | (ph << st);
             }
             // every copy this thread started lands before the CTA exits
-            wait_bounded(q_full, 0u, ctl, false);
-            for (int s = 0; s < kSlots; ++s) {
-                if (outstanding & (1u << s)) wait_bounded(k_full(s), (out_par >> s) & 1u, ctl, false);
-                if (outstanding & (4u << s)) wait_bounded(v_full(s), (out_par >> (s + 2)) & 1u, ctl, false);
-            }
+            if (is_k) wait_bounded(q_full, 0u, ctl, false);
+            for (int s = 0; s < kSlots; ++s)
+                if (outstanding & (1u << s))
+                    wait_bounded(is_k ? k_full(s) : v_full(s), (out_par >> s) & 1u, ctl, false);
         }
         __syncwarp();
     } else if (warp == 1) {
