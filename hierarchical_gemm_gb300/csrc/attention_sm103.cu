@@ -5,24 +5,26 @@
 // README (section "Example of FlashMLA"), laid out for sm_103a:
 //   * a CTA owns 128 query rows of one (batch, head): Q is loaded once by
 //     TMA into shared memory (128-byte swizzle);
-//   * key and value blocks of 128 rows stream through two-slot rings of
+//   * key and value blocks of 128 rows stream through three-slot rings of
 //     their own: a K slot is free once S = Q K^T has read it, a V slot once
-//     O += P V has, so the next keys load while this block's softmax and
-//     P V still run;
-//   * S_j = Q K_j^T is computed by tcgen05.mma into one of two tensor-memory
-//     score buffers (acc_s of the example), so that the scores of block j+1
-//     are computed while block j's softmax runs;
+//     O += P V has;
+//   * S_j = Q K_j^T is computed by tcgen05.mma into one of three
+//     tensor-memory score buffers (acc_s of the example), two blocks ahead
+//     of the softmax, so the scores of the next block are ready when this
+//     block's softmax ends;
 //   * two warpgroups, two threads per query row, read the row of S_j; both
 //     take the row maximum over all 128 scores (scores_max), so they agree
 //     on it without exchanging anything, and each exponentiates its half of
-//     the keys: P_j = 2^(t - m) rounded to the 16-bit input format into
-//     shared memory (acc_s_cast), its partial row sum (logsum), and, when
-//     the maximum has grown, its half of the row of the output accumulator
-//     rescaled (scores_scale) -- the split of acc_s between warpgroups of
-//     the example, with the maximum recomputed instead of all-gathered;
-//   * O += P_j V_j is computed by tcgen05.mma into a tensor-memory
-//     accumulator (acc_o); at the end each thread divides its row by the
-//     row sum and stores it.
+//     the keys: P_j = 2^(t - m) rounded to the 16-bit input format
+//     (acc_s_cast) and written back into the score buffer it came from, two
+//     weights per 32-bit column, its partial row sum (logsum), and, when the
+//     maximum has grown, its half of the row of the output accumulator
+//     rescaled (scores_scale) -- the split of acc_s between warpgroups of the
+//     example, with the maximum recomputed instead of all-gathered;
+//   * O += P_j V_j is computed by tcgen05.mma with P read from tensor memory
+//     (A operand) and V from shared memory, into a tensor-memory accumulator
+//     (acc_o); at the end each thread divides its row by the row sum and
+//     stores it.
 // The rescale is lazy: a row keeps its old maximum until the new one exceeds
 // it by 2^8, so the output accumulator is read and rewritten only when a
 // row's scores jump; the weights then stay below 2^8, well inside the
@@ -32,9 +34,9 @@
 // Warp roles: warp 0 lane 0 loads Q and the key blocks, warp 10 lane 0 the
 // value blocks (so that a key load never waits behind a value slot), warp 1
 // lane 0 issues the MMAs, warps 2-9 (two warpgroups) run the softmax and the
-// epilogue.  Every wait is bounded in time
-// (WaitCtl); a CTA that gives up records a timeout, lets its copies and MMAs
-// finish, frees tensor memory and returns.
+// epilogue.  Every wait is bounded in time (WaitCtl); a CTA that gives up
+// records a timeout, lets its copies and MMAs finish, frees tensor memory
+// and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,17 +55,19 @@ constexpr int kThreads = 352;           // K producer, MMA, two softmax warpgrou
 constexpr int kSoftThreads = 256;
 constexpr uint32_t kAtom = 128u * 128u; // 128 rows x 128 bytes: one swizzle atom column
 constexpr uint32_t kTile = 2u * kAtom;  // 128 rows x 128 16-bit elements
+constexpr int kSlots = 3;               // K ring and V ring depth
 constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKVOff = kTile;      // ring slot: K block, then V block
-constexpr uint32_t kSlotBytes = 2u * kTile;
-constexpr int kSlots = 2;
-constexpr uint32_t kPOff = kKVOff + kSlots * kSlotBytes;  // two P buffers
-constexpr uint32_t kBarOff = kPOff + 2u * kTile;
-constexpr int kNumBars = 18;
+constexpr uint32_t kKOff = kTile;
+constexpr uint32_t kVOff = kKOff + kSlots * kTile;
+constexpr uint32_t kBarOff = kVOff + kSlots * kTile;
+constexpr int kSBufs = 3;               // score buffers (the P of a block overwrites its scores)
+// barriers: q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[3],
+// p_full[3], p_free[3], drain, pair[4]
+constexpr int kNumBars = 1 + 4 * kSlots + 3 * kSBufs + 1 + 4;
 constexpr uint32_t kMiscOff = kBarOff + 8u * kNumBars;
 constexpr uint32_t kSmemBytes = 1024u + kMiscOff + 16u;
-constexpr uint32_t kTmemCols = 512;     // S buffers at columns 0 and 128, O at 256
-constexpr uint32_t kOCol = 256;
+constexpr uint32_t kTmemCols = 512;     // S buffers at columns 0, 128, 256; O at 384
+constexpr uint32_t kOCol = 384;
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -95,6 +99,23 @@ __host__ __device__ constexpr uint32_t idesc(bool f16, bool b_nmajor) {
            ((128u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
+// Barrier addresses (8 bytes each, from `bars`).
+struct Bars {
+    uint32_t b;
+    __device__ uint32_t q_full() const { return b; }
+    __device__ uint32_t k_full(int s) const { return b + 8u * (1 + s); }
+    __device__ uint32_t k_empty(int s) const { return b + 8u * (1 + kSlots + s); }
+    __device__ uint32_t v_full(int s) const { return b + 8u * (1 + 2 * kSlots + s); }
+    __device__ uint32_t v_empty(int s) const { return b + 8u * (1 + 3 * kSlots + s); }
+    __device__ uint32_t s_full(int i) const { return b + 8u * (1 + 4 * kSlots + i); }
+    __device__ uint32_t p_full(int i) const { return b + 8u * (1 + 4 * kSlots + kSBufs + i); }
+    // P V of a block whose scores used buffer i is complete
+    __device__ uint32_t p_free(int i) const { return b + 8u * (1 + 4 * kSlots + 2 * kSBufs + i); }
+    __device__ uint32_t drain() const { return b + 8u * (1 + 4 * kSlots + 3 * kSBufs); }
+    // the two softmax warps of TMEM lane quarter q (64 threads)
+    __device__ uint32_t pair(int q) const { return b + 8u * (2 + 4 * kSlots + 3 * kSBufs + q); }
+};
+
 struct SoftCtx {
     const AttnParams& p;
     uint32_t base;   // shared memory (1024-aligned)
@@ -107,12 +128,8 @@ struct SoftCtx {
 // One softmax thread: query row (quarter * 32 + lane) of the block, keys
 // [64 kG, 64 kG + 64) of every key block and the same output columns.
 template <bool kF16, int kG>
-__device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
+__device__ __forceinline__ void softmax_role(const SoftCtx& sc, const Bars& bar) {
     const AttnParams& p = sc.p;
-    auto s_full = [&](int b) { return bars + 8u * (5 + b); };
-    auto s_free = [&](int b) { return bars + 8u * (7 + b); };
-    auto p_full = [&](int b) { return bars + 8u * (9 + b); };
-    auto p_free = [&](int b) { return bars + 8u * (11 + b); };
     const int lane = sc.lane;
     const int r = sc.quarter * 32 + lane;  // query row within the block
     const int qrow = sc.qb * kBQ + r;
@@ -120,17 +137,20 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
     const int kv_last = p.causal ? qrow + p.Sk - p.Sq : p.Sk - 1;  // last key this row sees
     const float c2 = p.scale_log2;
     // a bounded wait taken by lane 0 for the whole warp
-    auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+    auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
         int good = 1;
-        if (lane == 0) good = wait_bounded(bar, parity, sc.ctl) ? 1 : 0;
+        if (lane == 0) good = wait_bounded(b, parity, sc.ctl) ? 1 : 0;
         return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
     float m_used = -INFINITY;  // base-2 maximum the weights are taken against
     float l = 0.0f;            // sum of this thread's weights
     bool ok = true;
     for (int j = 0; j < sc.nkv; ++j) {
-        const int sb = j & 1, pb = j & 1;
-        if (!warp_wait(s_full(sb), static_cast<uint32_t>(j >> 1) & 1u)) {
+        const int sb = j % kSBufs;
+        // (S_j complete implies that P V of block j - 2 and every earlier one
+        // is complete too: the MMA thread issued them first, and a commit
+        // covers all of them)
+        if (!warp_wait(bar.s_full(sb), static_cast<uint32_t>(j / kSBufs) & 1u)) {
             ok = false;
             break;
         }
@@ -142,8 +162,6 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
             tmem_ld_32x32b_x32(trow + sb * 128u + 32u * c, part);
         }
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(s_free(sb));  // the score buffer may be overwritten
         // keys past Sk or past the causal limit weigh nothing
         const int k0 = j * kBKV;
         if (!(k0 + kBKV - 1 <= kv_last && k0 + kBKV <= p.Sk)) {
@@ -151,8 +169,7 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
             for (int c = 0; c < 128; ++c)
                 if (k0 + c > kv_last || k0 + c >= p.Sk) s[c] = __float_as_uint(-INFINITY);
         }
-        // row maximum: eight independent chains, then a tree (short
-        // dependency chains matter with two warps per scheduler)
+        // row maximum: eight independent chains, then a tree
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
@@ -171,9 +188,10 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
             if (m_new > -INFINITY) m_used = m_new;
             l *= alpha;
             if (j >= 1) {
-                // O holds P_0 V_0 + ... + P_{j-1} V_{j-1}: wait for the last,
-                // then scale this thread's half of the row
-                if (!warp_wait(p_free((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u)) {
+                // O holds P_0 V_0 + ... + P_{j-1} V_{j-1}: wait for the last
+                // (earlier ones are complete, see above), then scale this
+                // thread's half of the row
+                if (!warp_wait(bar.p_free((j - 1) % kSBufs), static_cast<uint32_t>((j - 1) / kSBufs) & 1u)) {
                     ok = false;
                     break;
                 }
@@ -190,47 +208,46 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, uint32_t bars) {
                 tmem_st_wait();
             }
         }
-        // P_j goes to buffer pb once P V of block j - 2 has read it
-        if (j >= 2 && !warp_wait(p_free(pb), static_cast<uint32_t>((j - 2) >> 1) & 1u)) {
-            ok = false;
-            break;
-        }
         // p = 2^(c2 s - m): one fused multiply-add per weight; before any
         // visible key, m = +inf makes every weight 0
         const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
-        const uint32_t prow = sc.base + kPOff + pb * kTile + kG * kAtom + static_cast<uint32_t>(r) * 128u;
         float rsum[8];  // eight independent partial sums, added in a fixed order
 #pragma unroll
         for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
+        uint32_t w[32];  // this thread's 64 weights, two per 32-bit column
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = 64 * kG + 8 * c8 + 2 * e;
-                const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c2, mneg));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c2, mneg));
-                rsum[2 * e] += p0;
-                rsum[2 * e + 1] += p1;
-                w[e] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-            }
-            // K-major, 128-byte swizzle: 16-byte chunk c8 of row r at chunk
-            // position c8 ^ (r mod 8)
-            st_shared_v4(prow + ((static_cast<uint32_t>(c8) ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 32; ++i) {
+            const int c = 64 * kG + 2 * i;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c2, mneg));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c2, mneg));
+            rsum[(2 * i) & 7] += p0;
+            rsum[(2 * i + 1) & 7] += p1;
+            w[i] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
         l += ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
-        fence_proxy_async_shared();  // the P writes are visible to the tensor core
+        // P_j goes into columns [32 kG, 32 kG + 32) of the score buffer; the
+        // other thread of this row reads all 128 score columns first (a
+        // bounded barrier of the two warps, so that neither can wait forever
+        // on a partner that gave up)
+        mbar_arrive(bar.pair(sc.quarter));
+        if (!warp_wait(bar.pair(sc.quarter), static_cast<uint32_t>(j) & 1u)) {
+            ok = false;
+            break;
+        }
+        tmem_st_32x32b_x32(trow + sb * 128u + 32u * kG, w);
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(pb));
+        mbar_arrive(bar.p_full(sb));
     }
     // ---------------------------------------------------- epilogue --
-    if (ok && sc.nkv > 0 && !warp_wait(p_free((sc.nkv - 1) & 1), static_cast<uint32_t>((sc.nkv - 1) >> 1) & 1u))
+    if (ok && sc.nkv > 0 &&
+        !warp_wait(bar.p_free((sc.nkv - 1) % kSBufs), static_cast<uint32_t>((sc.nkv - 1) / kSBufs) & 1u))
         ok = false;
     // the row sum is the two halves' sums (same maximum): exchange them
-    // through the P buffers, which every P V has finished reading
-    const uint32_t lx = sc.base + kPOff;  // [2][128] floats
+    // through the first key slot, which every S has finished reading
+    const uint32_t lx = sc.base + kKOff;  // [2][128] floats
     if (ok) asm volatile("st.shared.f32 [%0], %1;" ::"r"(lx + (kG * 128 + r) * 4u), "f"(l) : "memory");
-    asm volatile("bar.sync 1, %0;" ::"n"(kSoftThreads) : "memory");
+    asm volatile("bar.sync 5, %0;" ::"n"(kSoftThreads) : "memory");
     if (!ok) return;
     float lo;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(lo) : "r"(lx + ((1 - kG) * 128 + r) * 4u) : "memory");
@@ -270,17 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
-    const uint32_t bars = base + kBarOff;
-    const uint32_t q_full = bars;
-    auto s_full = [&](int b) { return bars + 8u * (5 + b); };
-    auto s_free = [&](int b) { return bars + 8u * (7 + b); };
-    auto p_full = [&](int b) { return bars + 8u * (9 + b); };
-    auto p_free = [&](int b) { return bars + 8u * (11 + b); };  // PV on buffer b done
-    const uint32_t drain_bar = bars + 8u * 13;
-    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto k_empty = [&](int s) { return bars + 8u * (3 + s); };
-    auto v_full = [&](int s) { return bars + 8u * (14 + s); };
-    auto v_empty = [&](int s) { return bars + 8u * (16 + s); };
+    const Bars bar{base + kBarOff};
     uint8_t* misc = base_ptr + kMiscOff;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -292,20 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkv = kv_blocks(p, qb);
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        mbar_init(bar.q_full(), 1);
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(k_full(s), 1);
-            mbar_init(k_empty(s), 1);
-            mbar_init(v_full(s), 1);
-            mbar_init(v_empty(s), 1);
+            mbar_init(bar.k_full(s), 1);
+            mbar_init(bar.k_empty(s), 1);
+            mbar_init(bar.v_full(s), 1);
+            mbar_init(bar.v_empty(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(s_full(b), 1);
-            mbar_init(s_free(b), kSoftThreads);  // every softmax thread
-            mbar_init(p_full(b), kSoftThreads);
-            mbar_init(p_free(b), 1);
+        for (int b = 0; b < kSBufs; ++b) {
+            mbar_init(bar.s_full(b), 1);
+            mbar_init(bar.p_full(b), kSoftThreads);  // every softmax thread
+            mbar_init(bar.p_free(b), 1);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(bar.drain(), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar.pair(q), 64);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmQ);
@@ -326,17 +333,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && nkv > 0) {
             uint32_t outstanding = 0, out_par = 0;  // loads per slot
             if (is_k) {
-                mbar_arrive_expect_tx(q_full, kTile);
-                tma_load_3d(qs, &tmQ, q_full, 0, qb * kBQ, bh);
-                tma_load_3d(qs + kAtom, &tmQ, q_full, 64, qb * kBQ, bh);
+                mbar_arrive_expect_tx(bar.q_full(), kTile);
+                tma_load_3d(qs, &tmQ, bar.q_full(), 0, qb * kBQ, bh);
+                tma_load_3d(qs + kAtom, &tmQ, bar.q_full(), 64, qb * kBQ, bh);
             }
             const CUtensorMap* map = is_k ? &tmK : &tmV;
             for (int j = 0; j < nkv; ++j) {
-                const int st = j & 1;
-                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                const uint32_t dst = base + kKVOff + st * kSlotBytes + (is_k ? 0u : kTile);
-                const uint32_t full = is_k ? k_full(st) : v_full(st);
-                if (!wait_bounded(is_k ? k_empty(st) : v_empty(st), ph ^ 1u, ctl)) break;
+                const int st = j % kSlots;
+                const uint32_t ph = static_cast<uint32_t>(j / kSlots) & 1u;
+                const uint32_t dst = base + (is_k ? kKOff : kVOff) + st * kTile;
+                const uint32_t full = is_k ? bar.k_full(st) : bar.v_full(st);
+                if (!wait_bounded(is_k ? bar.k_empty(st) : bar.v_empty(st), ph ^ 1u, ctl)) break;
                 // tests only: the first CTA leaves its first key block unloaded
                 if (is_k && (p.debug_flags & 1) && blockIdx.x == 0 && j == 0) continue;
                 mbar_arrive_expect_tx(full, kTile);
@@ -346,72 +353,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                 out_par = (out_par & ~(1u << st)) | (ph << st);
             }
             // every copy this thread started lands before the CTA exits
-            if (is_k) wait_bounded(q_full, 0u, ctl, false);
+            if (is_k) wait_bounded(bar.q_full(), 0u, ctl, false);
             for (int s = 0; s < kSlots; ++s)
                 if (outstanding & (1u << s))
-                    wait_bounded(is_k ? k_full(s) : v_full(s), (out_par >> s) & 1u, ctl, false);
+                    wait_bounded(is_k ? bar.k_full(s) : bar.v_full(s), (out_par >> s) & 1u, ctl, false);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && nkv > 0) {
             constexpr uint32_t kIdS = idesc(kF16, false), kIdPV = idesc(kF16, true);
-            bool ok = wait_bounded(q_full, 0u, ctl);
-            // O += P_i V_i.  P (128 rows x 128 keys) is K-major like Q; V
-            // (128 keys x 128 columns, columns contiguous) is the N-major B
-            // operand: 64-column boxes 16 KiB apart, 8-key groups 1 KiB
-            // apart, the k-th 16-key step 2 KiB further.
+            bool ok = wait_bounded(bar.q_full(), 0u, ctl);
+            // O += P_i V_i.  P (128 rows x 128 keys, two per 32-bit column)
+            // is the tensor-memory A operand in the first 64 columns of score
+            // buffer i mod 2; V (128 keys x 128 columns, columns contiguous)
+            // is the N-major B operand: 64-column boxes 16 KiB apart, 8-key
+            // groups 1 KiB apart, the k-th 16-key step 2 KiB further.
             auto issue_pv = [&](int i) -> bool {
-                const int pb = i & 1;
-                const uint32_t ph = static_cast<uint32_t>(i >> 1) & 1u;
-                if (!wait_bounded(v_full(i & 1), ph, ctl) || !wait_bounded(p_full(pb), ph, ctl)) return false;
+                const int pb = i % kSBufs, vs_slot = i % kSlots;
+                if (!wait_bounded(bar.v_full(vs_slot), static_cast<uint32_t>(i / kSlots) & 1u, ctl) ||
+                    !wait_bounded(bar.p_full(pb), static_cast<uint32_t>(i / kSBufs) & 1u, ctl))
+                    return false;
                 tc_fence_after();
-                const uint32_t ps = base + kPOff + pb * kTile;
-                const uint32_t vs = base + kKVOff + (i & 1) * kSlotBytes + kTile;
+                const uint32_t vs = base + kVOff + vs_slot * kTile;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const uint64_t ad = smem_desc_sw128(ps + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
                     const uint64_t bd = smem_desc_sw128(vs + k * 2048u, kAtom, 1024u);
-                    umma_f16<1>(tmem + kOCol, ad, bd, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
+                    umma_f16_ta(tmem + kOCol, tmem + pb * 128u + 8u * k, bd, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
                 }
-                umma_commit(p_free(pb));          // P buffer read; O holds PV_0..PV_i
-                umma_commit(v_empty(i & 1));      // V_i read
+                umma_commit(bar.p_free(pb));          // O holds P_0 V_0 .. P_i V_i
+                umma_commit(bar.v_empty(vs_slot));    // V_i read
                 return true;
             };
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int st = j & 1, sb = j & 1;
-                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                if (!wait_bounded(k_full(st), ph, ctl) || !wait_bounded(s_free(sb), ph ^ 1u, ctl)) {
-                    ok = false;
-                    break;
-                }
+            // S_j = Q K_j^T into score buffer j mod 3: both operands K-major,
+            // two 64-wide swizzle columns of D, the k-th 16-deep step 32
+            // bytes along a row.  The buffer last held P_{j-3}, which P V of
+            // block j - 3 (issued before) has read.
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % kSlots, sb = j % kSBufs;
+                if (!wait_bounded(bar.k_full(st), static_cast<uint32_t>(j / kSlots) & 1u, ctl)) return false;
                 tc_fence_after();
-                // S_j = Q K_j^T: both operands K-major, two 64-wide swizzle
-                // columns of D, the k-th 16-deep step 32 bytes along a row
-                const uint32_t ks = base + kKVOff + st * kSlotBytes;
+                const uint32_t ks = base + kKOff + st * kTile;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t ad = smem_desc_sw128(qs + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
                     const uint64_t bd = smem_desc_sw128(ks + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
                     umma_f16<1>(tmem + sb * 128u, ad, bd, kIdS, k > 0 ? 1u : 0u);
                 }
-                umma_commit(s_full(sb));
-                umma_commit(k_empty(st));  // K_j read
-                if (j >= 1 && !issue_pv(j - 1)) ok = false;
+                umma_commit(bar.s_full(sb));
+                umma_commit(bar.k_empty(st));  // K_j read
+                return true;
+            };
+            // scores run two blocks ahead of P V: S_0, S_1, then P V_j, S_{j+2}
+            for (int j = 0; ok && j < 2 && j < nkv; ++j) ok = issue_s(j);
+            for (int j = 0; ok && j < nkv; ++j) {
+                ok = issue_pv(j);
+                if (ok && j + 2 < nkv) ok = issue_s(j + 2);
             }
-            if (ok) issue_pv(nkv - 1);
             // every MMA issued above completes before tensor memory is freed
-            umma_commit(drain_bar);
-            wait_bounded(drain_bar, 0u, ctl, false);
+            umma_commit(bar.drain());
+            wait_bounded(bar.drain(), 0u, ctl, false);
         }
         __syncwarp();
     } else {
         // ---------------------------------------- softmax and epilogue --
         const SoftCtx sc{p, base, tmem, qb, bh, nkv, lane, warp & 3, ctl};
         if (warp < 6)
-            softmax_role<kF16, 0>(sc, bars);
+            softmax_role<kF16, 0>(sc, bar);
         else
-            softmax_role<kF16, 1>(sc, bars);
+            softmax_role<kF16, 1>(sc, bar);
     }
 
     // ------------------------------------------------------------ exit --

@@ -364,6 +364,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
     }
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16, one CTA: A is 128 lanes (rows)
+// x 16 16-bit elements packed two per 32-bit column, starting at a_tmem.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem], kind::f8f6f4 with 8-bit operands (E4M3 /
 // E5M2 as the instruction descriptor says), fp32 accumulate.  One
 // instruction covers 32 K-elements (32 bytes of a K-major row).
