@@ -169,14 +169,18 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, const Bars& bar)
             for (int c = 0; c < 128; ++c)
                 if (k0 + c > kv_last || k0 + c >= p.Sk) s[c] = __float_as_uint(-INFINITY);
         }
-        // row maximum: eight independent chains, then a tree
+        // row maximum: eight independent chains of three-input maxima, then
+        // a tree
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
 #pragma unroll
-        for (int c = 8; c < 128; c += 8) {
+        for (int c = 8; c < 128; c += 16) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(s[c + i]));
+            for (int i = 0; i < 8; ++i)
+                asm("max.f32 %0, %1, %2, %3;"
+                    : "=f"(mx[i])
+                    : "f"(mx[i]), "f"(__uint_as_float(s[c + i])), "f"(__uint_as_float(s[c + 8 + i])));
         }
         const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
