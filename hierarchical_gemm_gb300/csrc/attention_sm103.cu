@@ -3,28 +3,28 @@
 //
 // It is the per-device block of the FlashMLA example of the TileScale
 // README (section "Example of FlashMLA"), laid out for sm_103a:
-//   * a CTA owns 128 query rows of one (batch, head): Q is loaded once by
-//     TMA into shared memory (128-byte swizzle);
-//   * key and value blocks of 128 rows stream through three-slot rings of
-//     their own: a K slot is free once S = Q K^T has read it, a V slot once
-//     O += P V has;
-//   * S_j = Q K_j^T is computed by tcgen05.mma into one of three
-//     tensor-memory score buffers (acc_s of the example), two blocks ahead
-//     of the softmax, so the scores of the next block are ready when this
-//     block's softmax ends;
-//   * two warpgroups, two threads per query row, read the row of S_j; both
-//     take the row maximum over all 128 scores (scores_max), so they agree
-//     on it without exchanging anything, and each exponentiates its half of
-//     the keys: P_j = 2^(t - m) rounded to the 16-bit input format
-//     (acc_s_cast) and written back into the score buffer it came from, two
-//     weights per 32-bit column, its partial row sum (logsum), and, when the
-//     maximum has grown, its half of the row of the output accumulator
-//     rescaled (scores_scale) -- the split of acc_s between warpgroups of the
-//     example, with the maximum recomputed instead of all-gathered;
+//   * a CTA owns two tiles of 128 query rows (A and B) of one (batch, head);
+//     their Q is loaded once by TMA into shared memory (128-byte swizzle);
+//   * key and value blocks of 128 rows stream through rings of their own: a
+//     K slot is free once both tiles' S = Q K^T have read it, a V slot once
+//     both tiles' O += P V have;
+//   * per tile, S_j = Q K_j^T is computed by tcgen05.mma into the tile's
+//     tensor-memory score buffer (acc_s of the example); one warpgroup per
+//     tile, a thread per query row, reads its row of S_j, keeps the running
+//     maximum (scores_max) and row sum (logsum) in base-2 units, writes
+//     P_j = 2^(t - m) rounded to the 16-bit input format (acc_s_cast) back
+//     into the score buffer, two weights per 32-bit column, and, when its
+//     maximum has grown, rescales its row of the output accumulator
+//     (scores_scale);
 //   * O += P_j V_j is computed by tcgen05.mma with P read from tensor memory
-//     (A operand) and V from shared memory, into a tensor-memory accumulator
-//     (acc_o); at the end each thread divides its row by the row sum and
-//     stores it.
+//     (A operand) and V from shared memory into the tile's tensor-memory
+//     accumulator (acc_o); at the end each thread divides its row by the row
+//     sum and stores it.
+// The two tiles ping-pong: while one tile's warpgroup computes its softmax,
+// the tensor cores run the other tile's P V and next S, so neither the
+// tensor cores nor the exponential units wait for each other.  (The
+// example splits one tile's acc_s between two warpgroups and all-gathers
+// it; two tiles need no exchange between the warpgroups at all.)
 // The rescale is lazy: a row keeps its old maximum until the new one exceeds
 // it by 2^8, so the output accumulator is read and rewritten only when a
 // row's scores jump; the weights then stay below 2^8, well inside the
@@ -32,11 +32,10 @@
 // weight, so the result is the same softmax.
 //
 // Warp roles: warp 0 lane 0 loads Q and the key blocks, warp 10 lane 0 the
-// value blocks (so that a key load never waits behind a value slot), warp 1
-// lane 0 issues the MMAs, warps 2-9 (two warpgroups) run the softmax and the
-// epilogue.  Every wait is bounded in time (WaitCtl); a CTA that gives up
-// records a timeout, lets its copies and MMAs finish, frees tensor memory
-// and returns.
+// value blocks, warp 1 lane 0 issues the MMAs, warps 2-5 run tile A's
+// softmax and epilogue and warps 6-9 tile B's.  Every wait is bounded in
+// time (WaitCtl); a CTA that gives up records a timeout, lets its copies and
+// MMAs finish, frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -48,32 +47,32 @@
 namespace tsg {
 namespace attn {
 
-constexpr int kBQ = 128;                // query rows per CTA (TMEM lanes)
+constexpr int kBQ = 128;                // query rows per tile (TMEM lanes)
+constexpr int kTiles = 2;               // query tiles per CTA
 constexpr int kBKV = 128;               // keys per block
 constexpr int kD = 128;                 // head dimension
 constexpr int kThreads = 352;           // K producer, MMA, two softmax warpgroups, V producer
-constexpr int kSoftThreads = 256;
 constexpr uint32_t kAtom = 128u * 128u; // 128 rows x 128 bytes: one swizzle atom column
 constexpr uint32_t kTile = 2u * kAtom;  // 128 rows x 128 16-bit elements
-constexpr int kSlots = 3;               // K ring and V ring depth
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKOff = kTile;
-constexpr uint32_t kVOff = kKOff + kSlots * kTile;
-constexpr uint32_t kBarOff = kVOff + kSlots * kTile;
-constexpr int kSBufs = 3;               // score buffers (the P of a block overwrites its scores)
-// barriers: q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[3],
-// p_full[3], p_free[3], drain, pair[4]
-constexpr int kNumBars = 1 + 4 * kSlots + 3 * kSBufs + 1 + 4;
+constexpr int kKSlots = 3;              // key ring depth
+constexpr int kVSlots = 2;              // value ring depth
+constexpr uint32_t kQOff = 0;           // Q of tile A, then tile B
+constexpr uint32_t kKOff = kTiles * kTile;
+constexpr uint32_t kVOff = kKOff + kKSlots * kTile;
+constexpr uint32_t kBarOff = kVOff + kVSlots * kTile;
+// barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], and per
+// tile s_full, p_full, p_free; drain
+constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 3 * kTiles + 1;
 constexpr uint32_t kMiscOff = kBarOff + 8u * kNumBars;
 constexpr uint32_t kSmemBytes = 1024u + kMiscOff + 16u;
-constexpr uint32_t kTmemCols = 512;     // S buffers at columns 0, 128, 256; O at 384
-constexpr uint32_t kOCol = 384;
+constexpr uint32_t kTmemCols = 512;     // S of tile t at columns 128 t, O of tile t at 256 + 128 t
+constexpr uint32_t kOCol = 256;
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct AttnParams {
     int32_t B, H, Sq, Sk;
-    int32_t nq;           // query blocks per (batch, head)
+    int32_t nq;           // CTAs (pairs of query tiles) per (batch, head)
     int32_t causal;
     float scale_log2;     // scale * log2(e): scores to base-2 exponent units
     int32_t debug_flags;
@@ -82,12 +81,13 @@ struct AttnParams {
     uint64_t timeout_ns;
 };
 
-// Key / value blocks query block qb has to visit.
-__device__ __forceinline__ int kv_blocks(const AttnParams& p, int qb) {
+// Key / value blocks the query tile starting at row q0 has to visit.
+__device__ __forceinline__ int kv_blocks(const AttnParams& p, int q0) {
+    if (q0 >= p.Sq) return 0;  // a tile wholly past the last query row
     const int nk = (p.Sk + kBKV - 1) / kBKV;
     if (!p.causal) return nk;
-    const int last_q = min(qb * kBQ + kBQ - 1, p.Sq - 1);
-    const int last_k = last_q + p.Sk - p.Sq;  // the last key that block's last row sees
+    const int last_q = min(q0 + kBQ - 1, p.Sq - 1);
+    const int last_k = last_q + p.Sk - p.Sq;  // the last key that tile's last row sees
     if (last_k < 0) return 0;
     return min(nk, last_k / kBKV + 1);
 }
@@ -99,58 +99,44 @@ __host__ __device__ constexpr uint32_t idesc(bool f16, bool b_nmajor) {
            ((128u >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-// Barrier addresses (8 bytes each, from `bars`).
+// Barrier addresses (8 bytes each, from `b`).
 struct Bars {
     uint32_t b;
     __device__ uint32_t q_full() const { return b; }
     __device__ uint32_t k_full(int s) const { return b + 8u * (1 + s); }
-    __device__ uint32_t k_empty(int s) const { return b + 8u * (1 + kSlots + s); }
-    __device__ uint32_t v_full(int s) const { return b + 8u * (1 + 2 * kSlots + s); }
-    __device__ uint32_t v_empty(int s) const { return b + 8u * (1 + 3 * kSlots + s); }
-    __device__ uint32_t s_full(int i) const { return b + 8u * (1 + 4 * kSlots + i); }
-    __device__ uint32_t p_full(int i) const { return b + 8u * (1 + 4 * kSlots + kSBufs + i); }
-    // P V of a block whose scores used buffer i is complete
-    __device__ uint32_t p_free(int i) const { return b + 8u * (1 + 4 * kSlots + 2 * kSBufs + i); }
-    __device__ uint32_t drain() const { return b + 8u * (1 + 4 * kSlots + 3 * kSBufs); }
-    // the two softmax warps of TMEM lane quarter q (64 threads)
-    __device__ uint32_t pair(int q) const { return b + 8u * (2 + 4 * kSlots + 3 * kSBufs + q); }
+    __device__ uint32_t k_empty(int s) const { return b + 8u * (1 + kKSlots + s); }
+    __device__ uint32_t v_full(int s) const { return b + 8u * (1 + 2 * kKSlots + s); }
+    __device__ uint32_t v_empty(int s) const { return b + 8u * (1 + 2 * kKSlots + kVSlots + s); }
+    __device__ uint32_t s_full(int t) const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + t); }
+    __device__ uint32_t p_full(int t) const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + kTiles + t); }
+    // P V of tile t complete
+    __device__ uint32_t p_free(int t) const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + 2 * kTiles + t); }
+    __device__ uint32_t drain() const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + 3 * kTiles); }
 };
 
-struct SoftCtx {
-    const AttnParams& p;
-    uint32_t base;   // shared memory (1024-aligned)
-    uint32_t tmem;   // tensor memory base
-    int qb, bh, nkv;
-    int lane, quarter;
-    const WaitCtl& ctl;
-};
-
-// One softmax thread: query row (quarter * 32 + lane) of the block, keys
-// [64 kG, 64 kG + 64) of every key block and the same output columns.
-template <bool kF16, int kG>
-__device__ __forceinline__ void softmax_role(const SoftCtx& sc, const Bars& bar) {
-    const AttnParams& p = sc.p;
-    const int lane = sc.lane;
-    const int r = sc.quarter * 32 + lane;  // query row within the block
-    const int qrow = sc.qb * kBQ + r;
-    const uint32_t trow = sc.tmem + (static_cast<uint32_t>(sc.quarter * 32) << 16);
+// One softmax thread: query row r of tile t (TMEM lane quarter q, lane l).
+template <bool kF16>
+__device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar, uint32_t tmem, int t, int q0,
+                                            int bh, int nkv, int quarter, int lane, const WaitCtl& ctl) {
+    const int r = quarter * 32 + lane;  // row within the tile
+    const int qrow = q0 + r;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t scol = 128u * t, ocol = kOCol + 128u * t;
     const int kv_last = p.causal ? qrow + p.Sk - p.Sq : p.Sk - 1;  // last key this row sees
     const float c2 = p.scale_log2;
     // a bounded wait taken by lane 0 for the whole warp
     auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
         int good = 1;
-        if (lane == 0) good = wait_bounded(b, parity, sc.ctl) ? 1 : 0;
+        if (lane == 0) good = wait_bounded(b, parity, ctl) ? 1 : 0;
         return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
     float m_used = -INFINITY;  // base-2 maximum the weights are taken against
-    float l = 0.0f;            // sum of this thread's weights
+    float l = 0.0f;            // sum of this row's weights
     bool ok = true;
-    for (int j = 0; j < sc.nkv; ++j) {
-        const int sb = j % kSBufs;
-        // (S_j complete implies that P V of block j - 2 and every earlier one
-        // is complete too: the MMA thread issued them first, and a commit
-        // covers all of them)
-        if (!warp_wait(bar.s_full(sb), static_cast<uint32_t>(j / kSBufs) & 1u)) {
+    for (int j = 0; j < nkv; ++j) {
+        // S_j complete: every MMA issued before it is complete too (a
+        // commit covers all of them), in particular P V of block j - 1
+        if (!warp_wait(bar.s_full(t), static_cast<uint32_t>(j) & 1u)) {
             ok = false;
             break;
         }
@@ -159,7 +145,7 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, const Bars& bar)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c);
-            tmem_ld_32x32b_x32(trow + sb * 128u + 32u * c, part);
+            tmem_ld_32x32b_x32(trow + scol + 32u * c, part);
         }
         tmem_ld_wait();
         // keys past Sk or past the causal limit weigh nothing
@@ -187,83 +173,64 @@ __device__ __forceinline__ void softmax_role(const SoftCtx& sc, const Bars& bar)
         const float m_new = fmaxf(m_used, mb * c2);  // (c2 > 0)
         const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-            // every lane of the warp moves to its own new maximum
+            // every lane of the warp moves to its own new maximum; O holds
+            // P_0 V_0 + ... + P_{j-1} V_{j-1}, complete (see above)
             const float alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m_new);
             if (m_new > -INFINITY) m_used = m_new;
             l *= alpha;
             if (j >= 1) {
-                // O holds P_0 V_0 + ... + P_{j-1} V_{j-1}: wait for the last
-                // (earlier ones are complete, see above), then scale this
-                // thread's half of the row
-                if (!warp_wait(bar.p_free((j - 1) % kSBufs), static_cast<uint32_t>((j - 1) / kSBufs) & 1u)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 64 * kG; c < 64 * kG + 64; c += 32) {
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
                     uint32_t o[32];
-                    tmem_ld_32x32b_x32(trow + kOCol + c, o);
+                    tmem_ld_32x32b_x32(trow + ocol + c, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st_32x32b_x32(trow + kOCol + c, o);
+                    tmem_st_32x32b_x32(trow + ocol + c, o);
                 }
                 tmem_st_wait();
             }
         }
         // p = 2^(c2 s - m): one fused multiply-add per weight; before any
-        // visible key, m = +inf makes every weight 0
+        // visible key, m = +inf makes every weight 0.  P_j goes back into
+        // the first 64 columns of the score buffer, two weights per column,
+        // 32 columns at a time.
         const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
         float rsum[8];  // eight independent partial sums, added in a fixed order
 #pragma unroll
         for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
-        uint32_t w[32];  // this thread's 64 weights, two per 32-bit column
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int c = 64 * kG + 2 * i;
-            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c2, mneg));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c2, mneg));
-            rsum[(2 * i) & 7] += p0;
-            rsum[(2 * i + 1) & 7] += p1;
-            w[i] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = 64 * h + 2 * i;
+                const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c2, mneg));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c2, mneg));
+                rsum[(2 * i) & 7] += p0;
+                rsum[(2 * i + 1) & 7] += p1;
+                w[i] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            }
+            tmem_st_32x32b_x32(trow + scol + 32u * h, w);
         }
         l += ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
-        // P_j goes into columns [32 kG, 32 kG + 32) of the score buffer; the
-        // other thread of this row reads all 128 score columns first (a
-        // bounded barrier of the two warps, so that neither can wait forever
-        // on a partner that gave up)
-        mbar_arrive(bar.pair(sc.quarter));
-        if (!warp_wait(bar.pair(sc.quarter), static_cast<uint32_t>(j) & 1u)) {
-            ok = false;
-            break;
-        }
-        tmem_st_32x32b_x32(trow + sb * 128u + 32u * kG, w);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar.p_full(sb));
+        mbar_arrive(bar.p_full(t));
     }
     // ---------------------------------------------------- epilogue --
-    if (ok && sc.nkv > 0 &&
-        !warp_wait(bar.p_free((sc.nkv - 1) % kSBufs), static_cast<uint32_t>((sc.nkv - 1) / kSBufs) & 1u))
-        ok = false;
-    // the row sum is the two halves' sums (same maximum): exchange them
-    // through the first key slot, which every S has finished reading
-    const uint32_t lx = sc.base + kKOff;  // [2][128] floats
-    if (ok) asm volatile("st.shared.f32 [%0], %1;" ::"r"(lx + (kG * 128 + r) * 4u), "f"(l) : "memory");
-    asm volatile("bar.sync 5, %0;" ::"n"(kSoftThreads) : "memory");
+    // (S of the last block complete implies P V of the block before it is:
+    // the wait for the last P V below cannot be confused with an earlier one)
+    if (ok && nkv > 0 && !warp_wait(bar.p_free(t), static_cast<uint32_t>(nkv - 1) & 1u)) ok = false;
     if (!ok) return;
-    float lo;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(lo) : "r"(lx + ((1 - kG) * 128 + r) * 4u) : "memory");
-    const float lt = l + lo;
     tc_fence_after();
-    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-    uint16_t* orow = static_cast<uint16_t*>(p.O) + (static_cast<int64_t>(sc.bh) * p.Sq + qrow) * kD;
-#pragma unroll
-    for (int c = 64 * kG; c < 64 * kG + 64; c += 32) {
+    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    uint16_t* orow = static_cast<uint16_t*>(p.O) + (static_cast<int64_t>(bh) * p.Sq + qrow) * kD;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
         uint32_t o[32];
-        if (sc.nkv > 0) {
-            tmem_ld_32x32b_x32(trow + kOCol + c, o);
+        if (nkv > 0) {
+            tmem_ld_32x32b_x32(trow + ocol + c, o);
             tmem_ld_wait();
         } else {
 #pragma unroll
@@ -300,23 +267,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.x / p.nq;
     const int qb = p.nq - 1 - static_cast<int>(blockIdx.x % p.nq);  // (causal: longest blocks first)
-    const int nkv = kv_blocks(p, qb);
+    const int q0 = qb * kTiles * kBQ;                                // first query row of tile A
+    const int n_a = kv_blocks(p, q0), n_b = kv_blocks(p, q0 + kBQ);  // blocks tiles A and B visit
+    const int nkv = max(n_a, n_b);                                   // blocks the CTA loads
+    auto n_t = [&](int t) { return t == 0 ? n_a : n_b; };
 
     if (threadIdx.x == 0) {
         mbar_init(bar.q_full(), 1);
-        for (int s = 0; s < kSlots; ++s) {
+        for (int s = 0; s < kKSlots; ++s) {
             mbar_init(bar.k_full(s), 1);
             mbar_init(bar.k_empty(s), 1);
+        }
+        for (int s = 0; s < kVSlots; ++s) {
             mbar_init(bar.v_full(s), 1);
             mbar_init(bar.v_empty(s), 1);
         }
-        for (int b = 0; b < kSBufs; ++b) {
-            mbar_init(bar.s_full(b), 1);
-            mbar_init(bar.p_full(b), kSoftThreads);  // every softmax thread
-            mbar_init(bar.p_free(b), 1);
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(bar.s_full(t), 1);
+            mbar_init(bar.p_full(t), kBQ);  // every softmax thread of the tile
+            mbar_init(bar.p_free(t), 1);
         }
         mbar_init(bar.drain(), 1);
-        for (int q = 0; q < 4; ++q) mbar_init(bar.pair(q), 64);
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmQ);
@@ -329,7 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-    const uint32_t qs = base + kQOff;
 
     if (warp == 0 || warp == 10) {
         // --------------------------------- TMA producers: Q and K / V --
@@ -337,14 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && nkv > 0) {
             uint32_t outstanding = 0, out_par = 0;  // loads per slot
             if (is_k) {
-                mbar_arrive_expect_tx(bar.q_full(), kTile);
-                tma_load_3d(qs, &tmQ, bar.q_full(), 0, qb * kBQ, bh);
-                tma_load_3d(qs + kAtom, &tmQ, bar.q_full(), 64, qb * kBQ, bh);
+                mbar_arrive_expect_tx(bar.q_full(), kTiles * kTile);
+                for (int t = 0; t < kTiles; ++t) {
+                    const uint32_t qs = base + kQOff + t * kTile;
+                    tma_load_3d(qs, &tmQ, bar.q_full(), 0, q0 + t * kBQ, bh);
+                    tma_load_3d(qs + kAtom, &tmQ, bar.q_full(), 64, q0 + t * kBQ, bh);
+                }
             }
+            const int slots = is_k ? kKSlots : kVSlots;
             const CUtensorMap* map = is_k ? &tmK : &tmV;
             for (int j = 0; j < nkv; ++j) {
-                const int st = j % kSlots;
-                const uint32_t ph = static_cast<uint32_t>(j / kSlots) & 1u;
+                const int st = j % slots;
+                const uint32_t ph = static_cast<uint32_t>(j / slots) & 1u;
                 const uint32_t dst = base + (is_k ? kKOff : kVOff) + st * kTile;
                 const uint32_t full = is_k ? bar.k_full(st) : bar.v_full(st);
                 if (!wait_bounded(is_k ? bar.k_empty(st) : bar.v_empty(st), ph ^ 1u, ctl)) break;
@@ -358,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // every copy this thread started lands before the CTA exits
             if (is_k) wait_bounded(bar.q_full(), 0u, ctl, false);
-            for (int s = 0; s < kSlots; ++s)
+            for (int s = 0; s < slots; ++s)
                 if (outstanding & (1u << s))
                     wait_bounded(is_k ? bar.k_full(s) : bar.v_full(s), (out_par >> s) & 1u, ctl, false);
         }
@@ -368,51 +342,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && nkv > 0) {
             constexpr uint32_t kIdS = idesc(kF16, false), kIdPV = idesc(kF16, true);
             bool ok = wait_bounded(bar.q_full(), 0u, ctl);
-            // O += P_i V_i.  P (128 rows x 128 keys, two per 32-bit column)
-            // is the tensor-memory A operand in the first 64 columns of score
-            // buffer i mod 2; V (128 keys x 128 columns, columns contiguous)
-            // is the N-major B operand: 64-column boxes 16 KiB apart, 8-key
-            // groups 1 KiB apart, the k-th 16-key step 2 KiB further.
-            auto issue_pv = [&](int i) -> bool {
-                const int pb = i % kSBufs, vs_slot = i % kSlots;
-                if (!wait_bounded(bar.v_full(vs_slot), static_cast<uint32_t>(i / kSlots) & 1u, ctl) ||
-                    !wait_bounded(bar.p_full(pb), static_cast<uint32_t>(i / kSBufs) & 1u, ctl))
+            // S_t(j) = Q_t K_j^T into tile t's score buffer: both operands
+            // K-major, two 64-wide swizzle columns of D, the k-th 16-deep
+            // step 32 bytes along a row.  The buffer held P_t(j-1), which
+            // P V of tile t (issued before) has read.
+            auto issue_s = [&](int t, int j) -> bool {
+                const int st = j % kKSlots;
+                if (!wait_bounded(bar.k_full(st), static_cast<uint32_t>(j / kKSlots) & 1u, ctl)) return false;
+                tc_fence_after();
+                const uint32_t qs = base + kQOff + t * kTile, ks = base + kKOff + st * kTile;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t ad = smem_desc_sw128(qs + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
+                    const uint64_t bd = smem_desc_sw128(ks + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
+                    umma_f16<1>(tmem + 128u * t, ad, bd, kIdS, k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar.s_full(t));
+                return true;
+            };
+            // O_t += P_t(j) V_j: P (128 rows x 128 keys, two per 32-bit
+            // column) is the tensor-memory A operand in the first 64 columns
+            // of tile t's score buffer; V (128 keys x 128 columns, columns
+            // contiguous) the N-major B operand: 64-column boxes 16 KiB
+            // apart, 8-key groups 1 KiB apart, the k-th 16-key step 2 KiB on.
+            auto issue_pv = [&](int t, int j) -> bool {
+                const int vs_slot = j % kVSlots;
+                if (!wait_bounded(bar.v_full(vs_slot), static_cast<uint32_t>(j / kVSlots) & 1u, ctl) ||
+                    !wait_bounded(bar.p_full(t), static_cast<uint32_t>(j) & 1u, ctl))
                     return false;
                 tc_fence_after();
                 const uint32_t vs = base + kVOff + vs_slot * kTile;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t bd = smem_desc_sw128(vs + k * 2048u, kAtom, 1024u);
-                    umma_f16_ta(tmem + kOCol, tmem + pb * 128u + 8u * k, bd, kIdPV, (i > 0 || k > 0) ? 1u : 0u);
+                    umma_f16_ta(tmem + kOCol + 128u * t, tmem + 128u * t + 8u * k, bd, kIdPV,
+                                (j > 0 || k > 0) ? 1u : 0u);
                 }
-                umma_commit(bar.p_free(pb));          // O holds P_0 V_0 .. P_i V_i
-                umma_commit(bar.v_empty(vs_slot));    // V_i read
+                umma_commit(bar.p_free(t));
                 return true;
             };
-            // S_j = Q K_j^T into score buffer j mod 3: both operands K-major,
-            // two 64-wide swizzle columns of D, the k-th 16-deep step 32
-            // bytes along a row.  The buffer last held P_{j-3}, which P V of
-            // block j - 3 (issued before) has read.
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % kSlots, sb = j % kSBufs;
-                if (!wait_bounded(bar.k_full(st), static_cast<uint32_t>(j / kSlots) & 1u, ctl)) return false;
-                tc_fence_after();
-                const uint32_t ks = base + kKOff + st * kTile;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t ad = smem_desc_sw128(qs + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
-                    const uint64_t bd = smem_desc_sw128(ks + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
-                    umma_f16<1>(tmem + sb * 128u, ad, bd, kIdS, k > 0 ? 1u : 0u);
-                }
-                umma_commit(bar.s_full(sb));
-                umma_commit(bar.k_empty(st));  // K_j read
-                return true;
-            };
-            // scores run two blocks ahead of P V: S_0, S_1, then P V_j, S_{j+2}
-            for (int j = 0; ok && j < 2 && j < nkv; ++j) ok = issue_s(j);
+            // order: S_A(0), S_B(0); then per block j: P V_A(j), S_A(j+1),
+            // P V_B(j), S_B(j+1) -- while one tile's softmax runs, the
+            // tensor cores work on the other tile
+            for (int t = 0; ok && t < kTiles; ++t)
+                if (n_t(t) > 0) ok = issue_s(t, 0);
+            if (ok) umma_commit(bar.k_empty(0));
             for (int j = 0; ok && j < nkv; ++j) {
-                ok = issue_pv(j);
-                if (ok && j + 2 < nkv) ok = issue_s(j + 2);
+                for (int t = 0; ok && t < kTiles; ++t) {
+                    if (j >= n_t(t)) continue;
+                    ok = issue_pv(t, j);
+                    if (ok && j + 1 < n_t(t)) ok = issue_s(t, j + 1);
+                }
+                if (!ok) break;
+                umma_commit(bar.v_empty(j % kVSlots));                     // V_j read by both tiles
+                if (j + 1 < nkv) umma_commit(bar.k_empty((j + 1) % kKSlots));  // K_{j+1} too
             }
             // every MMA issued above completes before tensor memory is freed
             umma_commit(bar.drain());
@@ -421,11 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------- softmax and epilogue --
-        const SoftCtx sc{p, base, tmem, qb, bh, nkv, lane, warp & 3, ctl};
-        if (warp < 6)
-            softmax_role<kF16, 0>(sc, bar);
-        else
-            softmax_role<kF16, 1>(sc, bar);
+        const int t = warp < 6 ? 0 : 1;
+        softmax_row<kF16>(p, bar, tmem, t, q0 + t * kBQ, bh, n_t(t), warp & 3, lane, ctl);
     }
 
     // ------------------------------------------------------------ exit --
@@ -558,7 +538,7 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     prm.H = static_cast<int32_t>(H);
     prm.Sq = static_cast<int32_t>(Sq);
     prm.Sk = static_cast<int32_t>(Sk);
-    prm.nq = static_cast<int32_t>((Sq + kBQ - 1) / kBQ);
+    prm.nq = static_cast<int32_t>((Sq + kTiles * kBQ - 1) / (kTiles * kBQ));
     prm.causal = causal ? 1 : 0;
     prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     prm.debug_flags = debug_flags;
