@@ -179,41 +179,46 @@ __device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar
             if (m_new > -INFINITY) m_used = m_new;
             l *= alpha;
             if (j >= 1) {
+                const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
                 for (int c = 0; c < 128; c += 32) {
                     uint32_t o[32];
                     tmem_ld_32x32b_x32(trow + ocol + c, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 v = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+                        o[i] = __float_as_uint(v.x);
+                        o[i + 1] = __float_as_uint(v.y);
+                    }
                     tmem_st_32x32b_x32(trow + ocol + c, o);
                 }
                 tmem_st_wait();
             }
         }
-        // p = 2^(c2 s - m): one fused multiply-add per weight; before any
-        // visible key, m = +inf makes every weight 0.  P_j goes back into
-        // the first 64 columns of the score buffer, two weights per column,
-        // 32 columns at a time.
+        // p = 2^(c2 s - m): one fused multiply-add per weight, two weights
+        // per packed instruction; before any visible key, m = +inf makes
+        // every weight 0.  P_j goes back into the first 64 columns of the
+        // score buffer, two weights per column, 32 columns at a time.
         const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
-        float rsum[8];  // eight independent partial sums, added in a fixed order
+        const float2 c22 = make_float2(c2, c2), mn2 = make_float2(mneg, mneg);
+        float2 rsum[4];  // eight independent partial sums, added in a fixed order
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
+        for (int i = 0; i < 4; ++i) rsum[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t w[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int c = 64 * h + 2 * i;
-                const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c2, mneg));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c2, mneg));
-                rsum[(2 * i) & 7] += p0;
-                rsum[(2 * i + 1) & 7] += p1;
-                w[i] = kF16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+                const float2 x = fma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c22, mn2);
+                const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                rsum[i & 3] = add2(rsum[i & 3], pw);
+                w[i] = kF16 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
             }
             tmem_st_32x32b_x32(trow + scol + 32u * h, w);
         }
-        l += ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+        l += ((rsum[0].x + rsum[0].y) + (rsum[1].x + rsum[1].y)) + ((rsum[2].x + rsum[2].y) + (rsum[3].x + rsum[3].y));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar.p_full(t));
@@ -237,10 +242,11 @@ __device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar
             for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
         uint32_t w[16];
+        const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float a = __uint_as_float(o[2 * i]) * inv, b = __uint_as_float(o[2 * i + 1]) * inv;
-            w[i] = kF16 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
+            const float2 v = mul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), inv2);
+            w[i] = kF16 ? pack_f16x2(v.x, v.y) : pack_bf16x2(v.x, v.y);
         }
         if (qrow < p.Sq) {
 #pragma unroll

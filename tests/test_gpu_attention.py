@@ -115,3 +115,46 @@ def test_expired_wait_reports_timeout_and_the_context_survives():
     assert time.time() - t0 < 10.0
     assert int(status.item()) == tsgemm.ERR_TIMEOUT
     _check((1, 2, 256, D), (1, 2, 256, D), "bf16", False, seed=18)
+
+
+def test_wide_score_range_underflows_weights():
+    # a large scale spreads a row's scores over hundreds of base-2 units:
+    # most weights underflow to zero, a few dominate
+    _check((1, 2, 256, D), (1, 2, 640, D), "bf16", False, scale=6.0, seed=30)
+    _check((1, 2, 256, D), (1, 2, 640, D), "f16", True, scale=6.0, seed=31)
+
+
+def test_tiny_scale_weights_near_one():
+    _check((1, 2, 256, D), (1, 2, 512, D), "f16", False, scale=1e-3, seed=32)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_full_size_workload_sampled_rows(causal):
+    # the B = 4, H = 32, S = 4096 workload in the launch the benchmark
+    # times; sampled 128-row windows (both tiles of a CTA, a window across
+    # two tiles, the last rows) of three heads against the oracle
+    import torch
+    from hierarchical_gemm_gb300 import tsgemm
+    name = "attn_b4h32s4096d128_causal_bf16" if causal else "attn_b4h32s4096d128_bf16"
+    w = synth.attn_workload(name)
+    B, H, S = w["B"], w["H"], w["Sq"]
+
+    def mk(seed):
+        return synth.matrix(B * H * S, D, ("normal", 1.0), seed, "bf16").reshape(B, H, S, D)
+    Qb, Kb, Vb = mk(w["seed_q"]), mk(w["seed_k"]), mk(w["seed_v"])
+    Q, K, V = (to_dev(x.reshape(-1, D), "bf16").reshape(x.shape) for x in (Qb, Kb, Vb))
+    O = torch.full(Q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    tsgemm.attention(Q, K, V, scale=D ** -0.5, causal=causal, O=O)
+    torch.cuda.synchronize()
+    assert tsgemm.attention_status() == 0
+    for b, h in ((0, 0), (1, 17), (B - 1, H - 1)):
+        Ob = from_dev(O[b, h].contiguous(), "bf16")
+        for r0 in (0, 128, 2048 + 64, S - 128):
+            r1 = r0 + 128
+            kv = r1 if causal else S
+            q = np.ascontiguousarray(Qb[b:b + 1, h:h + 1, r0:r1])
+            k = np.ascontiguousarray(Kb[b:b + 1, h:h + 1, :kv])
+            v = np.ascontiguousarray(Vb[b:b + 1, h:h + 1, :kv])
+            ref, bound = oracle.attention(q, k, v, "bf16", D ** -0.5, causal)
+            ok, info = oracle.accept_attention(Ob[r0:r1][None, None], ref, bound, "bf16")
+            assert ok, (b, h, r0, info)
