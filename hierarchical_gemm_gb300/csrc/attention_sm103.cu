@@ -31,11 +31,15 @@
 // 16-bit formats, and the final division uses the same maximum as every
 // weight, so the result is the same softmax.
 //
-// Warp roles: warp 0 lane 0 loads Q and the key blocks, warp 10 lane 0 the
-// value blocks, warp 1 lane 0 issues the MMAs, warps 2-5 run tile A's
-// softmax and epilogue and warps 6-9 tile B's.  Every wait is bounded in
-// time (WaitCtl); a CTA that gives up records a timeout, lets its copies and
-// MMAs finish, frees tensor memory and returns.
+// Warp roles, in three warpgroups: warps 0-3 run tile A's softmax and
+// epilogue, warps 4-7 tile B's (warp w reads tensor-memory lanes
+// 32 (w mod 4) .. +31); in the third, warp 8 lane 0 loads Q and the key
+// blocks, warp 9 lane 0 issues the MMAs, warp 10 lane 0 loads the value
+// blocks and warp 11 idles.  The third warpgroup gives most of its
+// registers to the other two (setmaxnreg): a softmax thread holds its whole
+// row of 128 scores.  Every wait is bounded in time (WaitCtl); a CTA that
+// gives up records a timeout, lets its copies and MMAs finish, frees tensor
+// memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,7 +55,13 @@ constexpr int kBQ = 128;                // query rows per tile (TMEM lanes)
 constexpr int kTiles = 2;               // query tiles per CTA
 constexpr int kBKV = 128;               // keys per block
 constexpr int kD = 128;                 // head dimension
-constexpr int kThreads = 352;           // K producer, MMA, two softmax warpgroups, V producer
+constexpr int kThreads = 384;           // two softmax warpgroups; producers and MMA issuer
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
+// registers per thread after the split: 256 softmax threads at kRegsSoftmax
+// and 128 others at kRegsOther may not exceed what the CTA was launched with
+// (384 x the kernel's register count; the host checks this before a launch)
+constexpr int kRegsSoftmax = 208, kRegsOther = 64;
+constexpr int kRegPool = 256 * kRegsSoftmax + 128 * kRegsOther;
 constexpr uint32_t kAtom = 128u * 128u; // 128 rows x 128 bytes: one swizzle atom column
 constexpr uint32_t kTile = 2u * kAtom;  // 128 rows x 128 16-bit elements
 constexpr int kKSlots = 3;              // key ring depth
@@ -221,7 +231,8 @@ __device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar
         l += ((rsum[0].x + rsum[0].y) + (rsum[1].x + rsum[1].y)) + ((rsum[2].x + rsum[2].y) + (rsum[3].x + rsum[3].y));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar.p_full(t));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.p_full(t));
     }
     // ---------------------------------------------------- epilogue --
     // (S of the last block complete implies P V of the block before it is:
@@ -290,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(bar.s_full(t), 1);
-            mbar_init(bar.p_full(t), kBQ);  // every softmax thread of the tile
+            mbar_init(bar.p_full(t), 4);  // every softmax warp of the tile
             mbar_init(bar.p_free(t), 1);
         }
         mbar_init(bar.drain(), 1);
@@ -300,16 +311,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
     }
-    if (warp == 1) tmem_alloc<1>(smem_u32(tmem_holder), kTmemCols);
+    if (warp == kWarpMma) tmem_alloc<1>(smem_u32(tmem_holder), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-
-    if (warp == 0 || warp == 10) {
+    // (each role's code sits in the branch of its register budget)
+    if (warp < kWarpK) {
+        // ---------------------------------------- softmax and epilogue --
+        setmaxnreg_inc<kRegsSoftmax>();
+        const int t = warp >> 2;
+        softmax_row<kF16>(p, bar, tmem, t, q0 + t * kBQ, bh, n_t(t), warp & 3, lane, ctl);
+    } else {
+    setmaxnreg_dec<kRegsOther>();
+    if (warp == kWarpK || warp == kWarpV) {
         // --------------------------------- TMA producers: Q and K / V --
-        const bool is_k = warp == 0;
+        const bool is_k = warp == kWarpK;
         if (lane == 0 && nkv > 0) {
             uint32_t outstanding = 0, out_par = 0;  // loads per slot
             if (is_k) {
@@ -343,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_bounded(is_k ? bar.k_full(s) : bar.v_full(s), (out_par >> s) & 1u, ctl, false);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && nkv > 0) {
             constexpr uint32_t kIdS = idesc(kF16, false), kIdPV = idesc(kF16, true);
@@ -408,16 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bounded(bar.drain(), 0u, ctl, false);
         }
         __syncwarp();
-    } else {
-        // ---------------------------------------- softmax and epilogue --
-        const int t = warp < 6 ? 0 : 1;
-        softmax_row<kF16>(p, bar, tmem, t, q0 + t * kBQ, bh, n_t(t), warp & 3, lane, ctl);
+    }
     }
 
     // ------------------------------------------------------------ exit --
     tc_fence_before();
     cta_barrier_any();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc<1>(tmem, kTmemCols);
@@ -513,6 +528,15 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
             ds.ready = true;
         }
         if (!ds.attr[f16 ? 1 : 0]) {
+            // the warpgroups' register split must fit in what the CTA is
+            // launched with, or the softmax warps would wait for registers
+            // forever
+            cudaFuncAttributes fa{};
+            if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return TSGEMM_ERR_CUDA;
+            }
+            if (fa.numRegs * kThreads < kRegPool) return TSGEMM_ERR_UNSUPPORTED;
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes)) != cudaSuccess) {
                 (void)cudaGetLastError();

@@ -462,6 +462,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Per-thread register budget of the executing warpgroup (all four warps
+// run the same instruction): dec gives registers back to the CTA's pool,
+// inc takes them from it and waits until the pool holds enough.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Packed fp32 pairs (sm_100 and later): two round-to-nearest fused
 // multiply-adds, adds or multiplies in one instruction.
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
