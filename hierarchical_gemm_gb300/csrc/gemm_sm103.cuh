@@ -108,6 +108,7 @@ struct Unit {
     int sk;          // 0: not stream-K; 1: a later K range of a tile, whose
                      // partial another CTA adds; 2: the tile's first K range,
                      // whose CTA adds the others' partials and stores C
+    bool last;       // stream-K mode: the slot's last unit (its ring is then idle)
 };
 
 // Tile row and column of linear tile `tile`: tiles are rastered in groups
@@ -161,34 +162,44 @@ __device__ __forceinline__ int64_t sk_slot_of(const GemmParams& p, int64_t x, in
 
 // The j-th work unit of slot g of the G slots (CTAs, or CTA clusters);
 // false past the slot's last.  Split mode: units g, g + G, g + 2G, ...
-// Stream-K mode: the slot's whole tiles (g, g + G, ... below full_tiles),
-// then the segments of its stream-K range, one per tile it touches.  A
-// range that starts inside a tile contributes that tile's later K slices
-// (sk = 1); one that ends inside a tile holds its first K slices (sk = 2)
-// and is the slot's last unit.
+// Stream-K mode: the slot's whole tiles (g, g + G, ... below full_tiles)
+// but the last, then the segments of its stream-K range, one per tile it
+// touches, then its last whole tile.  A range that starts inside a tile
+// contributes that tile's later K slices (sk = 1) and is the first
+// segment; one that ends inside a tile holds its first K slices (sk = 2),
+// the last segment, whose CTA adds the others' partials while its tensor
+// cores already work on the last whole tile.  (With no whole tiles the
+// stream-K segments are all there is.)
 __device__ __forceinline__ bool unit_at(const GemmParams& p, int64_t g, int64_t G, int64_t j, Unit& r) {
     if (p.sk_tiles == 0) {
         const int64_t u = g + j * G;
         if (u >= p.units) return false;
         r = decode_unit(p, u);
+        r.last = false;
         return true;
     }
     r.split = 0;
     r.nsplit = 1;
     r.slot = -1;
     r.sk = 0;
+    r.last = false;
     const int64_t ndp = g < p.full_tiles ? (p.full_tiles - 1 - g) / G + 1 : 0;
-    if (j < ndp) {
-        tile_coords(p, g + j * G, r.tm, r.tn);
-        r.kb0 = 0;
-        r.kb1 = p.kblocks;
-        return true;
-    }
     const int64_t kb = p.kblocks;
     const int64_t a = sk_begin(p, g, G), b = sk_begin(p, g + 1, G);
-    const int64_t jj = j - ndp;
+    const int64_t nsk = b > a ? (b - 1) / kb - a / kb + 1 : 0;  // stream-K segments of the slot
+    const int64_t first_dp = ndp > 0 ? ndp - 1 : 0;              // whole tiles before them
+    if (j < first_dp || (ndp > 0 && j == first_dp + nsk)) {
+        const int64_t d = j < first_dp ? j : ndp - 1;
+        tile_coords(p, g + d * G, r.tm, r.tn);
+        r.kb0 = 0;
+        r.kb1 = p.kblocks;
+        r.last = d == ndp - 1;
+        return true;
+    }
+    const int64_t jj = j - first_dp;
+    if (jj >= nsk) return false;
     const int64_t start = jj == 0 ? a : (a / kb + jj) * kb;
-    if (start >= b) return false;
+    r.last = ndp == 0 && jj == nsk - 1;
     const int64_t t = start / kb;
     const int64_t end = min(b, (t + 1) * kb);
     tile_coords(p, p.full_tiles + t, r.tm, r.tn);
@@ -298,9 +309,10 @@ struct CStager {
 //     its partial to its slot's workspace and counts itself in.  The
 //     segment holding the tile's first K range (sk = 2) waits for the
 //     nsplit - 1 others, adds their partials after its own in K order and
-//     stores C; it is its CTA's last unit, so the operand ring is idle and,
-//     when the partials fit, they are bulk-copied into it and read from
-//     shared memory.
+//     stores C.  When it is its CTA's last unit the operand ring is idle
+//     and, if the partials fit, they are bulk-copied into it and read from
+//     shared memory; otherwise (a whole tile follows, the ring is busy)
+//     they are read from global memory while that tile's mainloop runs.
 // `h` indexes the counter (and, in split mode, the workspace tile) of this
 // 128-row half; `aux` holds the stream-K workspace slots and the ring;
 // `epi_sync` is the epilogue's bounded barrier (both warpgroups) and
@@ -313,6 +325,21 @@ struct EpiAux {
     uint32_t ring_bytes;
     uint32_t red_bar;     // barrier of the bulk copies into the ring
 };
+
+// A stream-K owner segment that is not its CTA's last unit reads its
+// contributors' partials from global memory; one thread asks for them in L2
+// before the segment's own accumulator is ready (the contributors, first
+// segments of their slots, are long done by then).
+template <int BN>
+__device__ __forceinline__ void prefetch_sk_partials(const GemmParams& p, const Unit& un, const EpiAux& aux,
+                                                     int etid) {
+    if (un.sk != 2 || un.last || etid != 0) return;
+    constexpr uint32_t kChunkBytes = 4u * 8u * 128u * 4u;
+    for (int s = 1; s < un.nsplit; ++s)
+        for (int c = 0; c < BN; c += 32)
+            bulk_prefetch_l2(p.ws + (aux.wsi + s * aux.wstride) * (kBM * BN) + (c >> 5) * (kChunkBytes / 4),
+                             kChunkBytes);
+}
 
 template <int BN, int kOut, class Sync, class Release>
 __device__ __forceinline__ bool drain_sk_owner(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
@@ -332,7 +359,7 @@ __device__ __forceinline__ bool drain_sk_owner(const GemmParams& p, const CUtens
     if (!epi_sync()) return false;
     if (!*flag) return false;
     __threadfence();
-    const bool staged = static_cast<uint32_t>(m) * kHalfBytes <= aux.ring_bytes;
+    const bool staged = un.last && static_cast<uint32_t>(m) * kHalfBytes <= aux.ring_bytes;
     if (staged) {
         // contributor s's partial lands at ring + (s - 1) * kHalfBytes, in
         // the workspace's order; every thread reads its own 512 bytes of a
@@ -874,6 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Unit un;
             if (!next_unit(j, un)) break;
             const int tm = un.tm;
+            prefetch_sk_partials<BN>(p, un, aux, etid);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, ctl) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);

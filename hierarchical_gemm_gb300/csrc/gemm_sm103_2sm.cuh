@@ -293,6 +293,7 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
             if (!unit_at(p, cluster_id, nclusters, j, un)) break;
             un.tn = un.tn * kPairs + static_cast<int>(pair);  // this pair's tile column
             const int tm = un.tm;
+            prefetch_sk_partials<BN>(p, un, aux, etid);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, ctl) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);

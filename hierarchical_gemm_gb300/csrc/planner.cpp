@@ -38,6 +38,11 @@ constexpr double kReduceBytesPerCycle = 14.0; // split-K partial writes + reads 
 constexpr double kUnitOverhead = 600.0;       // pipeline fill / drain per unit (model)
 constexpr bool kAutoStreamK = true;          // the planner proposes stream-K itself
 constexpr double kFixupCycles = 11000.0;      // stream-K: segment hand-overs and the final add (measured)
+// the same when a whole tile follows: the owner's add from global memory
+// and its slowdown of the mainloop beside it (measured ~10 us), less the
+// part that tile's mainloop hides, but at least kHiddenFixupCycles
+constexpr double kMidFixupCycles = 27000.0;
+constexpr double kHiddenFixupCycles = 1500.0;
 constexpr double kStagedBytesPerCycle = 64.0; // stream-K: partials bulk-copied into the idle ring
 constexpr int kMaxSplits = 32;
 constexpr int kDefaultTimeoutMs = 1000;
@@ -112,10 +117,11 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, in
 }
 
 // Stream-K: the last `sk` tiles' K slices spread evenly over the slots,
-// after ceil((tiles - sk) / slots) rounds of whole tiles.  A tile cut
-// between slots costs its later parts a partial write (mostly hidden
-// behind their next mainloop) and its first part's CTA, at the very end, a
-// copy of the partials into the idle ring and the final add.
+// run before the last of ceil((tiles - sk) / slots) rounds of whole tiles.
+// A tile cut between slots costs its later parts a partial write and its
+// first part's CTA the final add, both hidden behind the next mainloop;
+// with no whole tiles the add comes at the very end, after a copy of the
+// partials into the idle ring.
 Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int cn, int64_t sk,
                      int num_sms) {
     const int64_t tiles = ceil_div(M, bm) * ceil_div(ceil_div(N, bn), cn);
@@ -136,8 +142,9 @@ Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm,
                               (kBM * kBK * 2.0 + (bm == 256 ? bn / 2 : bn) * kBK * 2.0);
     const double fetch = owners_parts * half_bytes <= ring_bytes ? owners_parts * half_bytes / kStagedBytesPerCycle
                                                                  : owners_parts * half_bytes / kReduceBytesPerCycle;
-    double compute = dp_rounds * (kblocks * per_kb + kUnitOverhead) + sk_slices * per_kb + 2 * kUnitOverhead +
-                     kFixupCycles + fetch;
+    const double tail = dp_rounds >= 1 ? std::max(kHiddenFixupCycles, kMidFixupCycles - kblocks * per_kb)
+                                       : kFixupCycles + fetch;
+    double compute = dp_rounds * (kblocks * per_kb + kUnitOverhead) + sk_slices * per_kb + 2 * kUnitOverhead + tail;
     double bytes = static_cast<double>(in_bytes(din)) * (M * K + K * N) +
                    static_cast<double>(out_bytes(dout)) * M * N +
                    2.0 * 4.0 * static_cast<double>(slots) * bm * bn * cn;

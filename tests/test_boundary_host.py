@@ -290,39 +290,58 @@ def test_stream_k_needs_a_slice_per_slot(ts):
     assert e.value.status == ts.ERR_UNSUPPORTED
 
 
-def _sk_walk(tiles_sk, kb, G):
-    """The kernel's stream-K decomposition, restated: every K slice of every
-    stream-K tile is covered once, contributors are their slot's first
-    segment, and each owner's contributors are the next m slots."""
+def _sk_walk(tiles_sk, kb, G, full=0):
+    """The kernel's stream-K schedule, restated: each slot runs its whole
+    tiles (g, g + G, ... below `full`) but the last, then the segments of
+    its stream-K range, then its last whole tile.  Every K slice of every
+    stream-K tile and every whole tile is covered once, contributors are
+    their slot's first stream-K segment, each owner's contributors are the
+    next m slots and come no later in their slots' order than the owner in
+    its own, and the owner segment is the last of its slot's range (the
+    slot's last unit only when no whole tile follows)."""
     W = tiles_sk * kb
     cover = [[0] * kb for _ in range(tiles_sk)]
+    whole = [0] * full
     owners, contrib = {}, {}
+    pos = {}  # (slot, tile) -> index of the unit in the slot's order
     for g in range(G):
         a, b = g * W // G, (g + 1) * W // G
-        j = 0
-        while True:
-            start = a if j == 0 else (a // kb + j) * kb
-            if start >= b:
-                break
+        nsk = (b - 1) // kb - a // kb + 1 if b > a else 0
+        ndp = (full - 1 - g) // G + 1 if g < full else 0
+        first_dp = max(ndp - 1, 0)
+        order = [("dp", d) for d in range(first_dp)] + [("sk", jj) for jj in range(nsk)]
+        if ndp > 0:
+            order.append(("dp", ndp - 1))
+        for j, (kind, i) in enumerate(order):
+            last = j == len(order) - 1
+            if kind == "dp":
+                whole[g + i * G] += 1
+                continue
+            start = a if i == 0 else (a // kb + i) * kb
+            assert start < b
             t = start // kb
             end = min(b, (t + 1) * kb)
             for k in range(start - t * kb, end - t * kb):
                 cover[t][k] += 1
+            pos[(g, t)] = j
             if start > t * kb:
-                assert j == 0
+                assert i == 0
                 contrib.setdefault(t, []).append(g)
             elif end < (t + 1) * kb:
                 owners[t] = (g, ((t + 1) * kb * G - 1) // W - g)
-                assert end == b  # the owner segment is the slot's last
-            j += 1
+                assert end == b and i == nsk - 1  # the owner segment ends the range
+                assert last == (ndp == 0)
     assert all(c == 1 for row in cover for c in row)
+    assert all(c == 1 for c in whole)
     assert set(contrib) == set(owners)
     for t, (g, m) in owners.items():
         assert contrib[t] == list(range(g + 1, g + m + 1))
+        assert all(pos[(c, t)] <= pos[(g, t)] for c in contrib[t])
 
 
 @pytest.mark.parametrize("args", [(16, 64, 76), (104, 16, 76), (64, 32, 152), (30, 6, 152), (20, 16, 36),
-                                  (30, 40, 76), (104, 64, 76), (16, 1024, 76), (68, 128, 76)])
+                                  (30, 40, 76), (104, 64, 76, 152), (16, 1024, 76), (68, 128, 76, 4028),
+                                  (30, 40, 76, 100), (104, 64, 76, 76)])
 def test_stream_k_decomposition(args):
     _sk_walk(*args)
 
