@@ -74,3 +74,18 @@ def test_bench_arguments():
         bench.parse_args(["--warmup", "2"])
     a = bench.parse_args(["--impl", "reference", "--steps", "3", "--warmup", "3"])
     assert a.impl == "reference"
+
+
+def test_peak_choice_follows_the_clock_regime():
+    peaks, _ = bench.measured_peaks()
+    burst, kind_b = bench.bf16_peak({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert "burst" in kind_b and burst == float(peaks.get("bf16_tflops", bench.FALLBACK_BF16_TFLOPS))
+    # the power cap noted but the clock at its maximum: still the burst figure
+    same, kind_s = bench.bf16_peak({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
+    assert same == burst and "burst" in kind_s
+    capped, kind_c = bench.bf16_peak({"sm_mhz": 1518.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
+    if "bf16_tflops_sustained" in peaks:
+        assert "sustained" in kind_c and capped == float(peaks["bf16_tflops_sustained"])
+    else:
+        assert capped == burst
+    assert bench.bf16_peak(None)[0] == burst
