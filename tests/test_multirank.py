@@ -77,6 +77,7 @@ def test_bench_arguments():
 
 
 def test_peak_choice_follows_the_clock_regime():
+    import bench
     peaks, _ = bench.measured_peaks()
     burst, kind_b = bench.bf16_peak({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
     assert "burst" in kind_b and burst == float(peaks.get("bf16_tflops", bench.FALLBACK_BF16_TFLOPS))
