@@ -282,9 +282,11 @@ struct CStager {
         }
     }
 
-    // All of this warp's stores have completed.
+    // All of this warp's stores have read their staging buffers, so the
+    // CTA may leave: the writes to C complete on their own, before the
+    // grid is done (nothing in the kernel reads C back).
     __device__ __forceinline__ void drain() {
-        if (lane == 0) bulk_wait_group_all();
+        if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
     }
 };
@@ -928,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
-        out.drain();  // this warp's output stores have landed
+        out.drain();  // this warp's output stores have read shared memory
     }
 
     // ------------------------------------------------------------ exit --

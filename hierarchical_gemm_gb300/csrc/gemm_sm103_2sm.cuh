@@ -313,7 +313,7 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
                 acc_phase ^= 1u;
             }
         }
-        out.drain();  // this warp's output stores have landed
+        out.drain();  // this warp's output stores have read shared memory
     }
 
     // ------------------------------------------------------------ exit --
