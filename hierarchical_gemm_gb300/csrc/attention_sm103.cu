@@ -43,6 +43,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -83,6 +84,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 struct AttnParams {
     int32_t B, H, Sq, Sk;
     int32_t nq;           // CTAs (pairs of query tiles) per (batch, head)
+    int32_t group;        // causal: (batch, head)s per chunk of the launch order
     int32_t causal;
     float scale_log2;     // scale * log2(e): scores to base-2 exponent units
     int32_t debug_flags;
@@ -282,8 +284,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.nq;
-    const int qb = p.nq - 1 - static_cast<int>(blockIdx.x % p.nq);  // (causal: longest blocks first)
+    // Launch order.  Non-causal: (batch, head) by (batch, head), all CTAs
+    // of one alike.  Causal: chunks of p.group (batch, head)s whose K and V
+    // fit in L2 together; within a chunk the longest query pairs first, one
+    // per (batch, head), so the launch ends on the shortest CTAs.
+    int bh, qb;
+    if (p.causal) {
+        const int span = p.group * p.nq;
+        const int chunk = static_cast<int>(blockIdx.x) / span;
+        const int gc = min(p.group, p.B * p.H - chunk * p.group);  // (batch, head)s in this chunk
+        const int idx = static_cast<int>(blockIdx.x) - chunk * span;
+        qb = p.nq - 1 - idx / gc;
+        bh = chunk * p.group + idx % gc;
+    } else {
+        bh = blockIdx.x / p.nq;
+        qb = p.nq - 1 - static_cast<int>(blockIdx.x % p.nq);
+    }
     const int q0 = qb * kTiles * kBQ;                                // first query row of tile A
     const int n_a = kv_blocks(p, q0), n_b = kv_blocks(p, q0 + kBQ);  // blocks tiles A and B visit
     const int nkv = max(n_a, n_b);                                   // blocks the CTA loads
@@ -569,6 +585,9 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     prm.Sq = static_cast<int32_t>(Sq);
     prm.Sk = static_cast<int32_t>(Sk);
     prm.nq = static_cast<int32_t>((Sq + kTiles * kBQ - 1) / (kTiles * kBQ));
+    // about 64 MB of K and V per chunk of the causal launch order
+    const int64_t kv_head_bytes = 2 * Sk * static_cast<int64_t>(D) * 2;
+    prm.group = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(B * H, (64ll << 20) / kv_head_bytes)));
     prm.causal = causal ? 1 : 0;
     prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     prm.debug_flags = debug_flags;

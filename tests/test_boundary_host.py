@@ -383,3 +383,30 @@ def test_attention_argument_checks(ts):
     assert f(1, 1, 1, 1, 128, ts.BF16, 1.0, 0, p + 8, p, p, p + 4096, None, None) == ts.ERR_ALIGNMENT
     # O overlapping Q
     assert f(1, 1, 8, 8, 128, ts.BF16, 1.0, 0, p, p + 8192, p + 16384, p + 256, None, None) == ts.ERR_INVALID_ARG
+
+
+# ------------------------------------------------- attention launch order --
+
+def _causal_order(BH, nq, group):
+    """The attention kernel's causal launch order, restated: CTA b takes
+    chunk b // (group nq) of `group` (batch, head)s; within it the longest
+    query pairs (largest qb) come first, one per (batch, head)."""
+    out = []
+    for b in range(BH * nq):
+        span = group * nq
+        chunk = b // span
+        gc = min(group, BH - chunk * group)
+        idx = b - chunk * span
+        out.append((chunk * group + idx % gc, nq - 1 - idx // gc))
+    return out
+
+
+@pytest.mark.parametrize("BH,nq,group", [(1, 1, 1), (6, 2, 6), (128, 16, 32), (129, 16, 32), (33, 3, 7), (5, 16, 5)])
+def test_causal_launch_order_covers_every_tile_once(BH, nq, group):
+    order = _causal_order(BH, nq, group)
+    assert sorted(order) == sorted((bh, qb) for bh in range(BH) for qb in range(nq))
+    # within each chunk the query pairs never grow along the launch order
+    span = group * nq
+    for c0 in range(0, BH * nq, span):
+        qbs = [qb for _, qb in order[c0:c0 + span]]
+        assert qbs == sorted(qbs, reverse=True)
