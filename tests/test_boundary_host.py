@@ -131,11 +131,14 @@ def test_planner_choices_for_the_workloads(ts):
     assert c["block_m"] == 256 and c["grid"] == 152
     c = ts.choose_config(1024, 1024, 65536, "bf16", "f32", 152)
     assert c["splits"] > 1
-    # 4096^3: the tiles of the last, partial wave are split along K
+    # 4096^3 bf16: CTA pairs on 256 x 256 tiles, stream-K over the tiles
+    # past two whole rounds (256 - 2 x 76 = 104), run between those rounds
     c = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152)
-    slots = 152 // (c["block_m"] // 128)
-    tiles = (4096 // c["block_m"]) * (4096 // c["block_n"])
-    assert c["splits"] == 1 or c["split_tiles"] == tiles % slots
+    assert (c["block_m"], c["block_n"], c["splits"], c["stream_k_tiles"]) == (256, 256, 1, 104)
+    # 4096^3 E4M3: a tile's mainloop is half as long, too short to hide the
+    # stream-K add, so no split (measured faster)
+    c = ts.choose_config(4096, 4096, 4096, "e4m3", "bf16", 152, layout="rcr")
+    assert (c["block_m"], c["block_n"], c["splits"], c["stream_k_tiles"]) == (256, 256, 1, 0)
 
 
 def test_forced_fields_are_honoured(ts):
