@@ -229,6 +229,19 @@ def bf16_peak(clocks):
     return float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), kind + " bf16 burst (cuBLAS-class torch.matmul)"
 
 
+def roofline_point(flops, algo_bytes, ms, tensor_peak, tensor_desc):
+    """(bound, achieved, peak, unit, description) of a kernel that does
+    `flops` and moves `algo_bytes` in `ms`: below the ridge (tensor peak /
+    HBM bandwidth) it is bound by streaming its operands and is reported in
+    GB/s against the measured HBM copy rate, else in TFLOP/s against
+    `tensor_peak`."""
+    peaks, kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    if flops / algo_bytes < tensor_peak * 1e12 / (hbm_peak * 1e9):
+        return "hbm", algo_bytes / (ms * 1e-3) / 1e9, hbm_peak, "GB/s", kind + " HBM copy bandwidth"
+    return "tensor", flops / (ms * 1e-3) / 1e12, tensor_peak, "TFLOP/s", tensor_desc
+
+
 ATTN_SOURCES = ["hierarchical_gemm_gb300/csrc/attention_sm103.cu",
                 "hierarchical_gemm_gb300/csrc/ptx.cuh"]
 
@@ -480,14 +493,7 @@ def run_ours(args):
         peak *= FP8_TO_BF16
         peak_desc += " x %.0f (nominal fp8 : bf16 dense ratio)" % FP8_TO_BF16
     algo_bytes = synth.workloads.in_nbytes(din) * (M * K + K * N) + synth.workloads.out_nbytes(dout) * M * N
-    hbm_peak = float(measured_peaks()[0].get("hbm_gbs", 6800.0))
-    if flops / algo_bytes < peak * 1e12 / (hbm_peak * 1e9):
-        # below the ridge: the shape is bound by streaming its operands
-        achieved = algo_bytes / (ms * 1e-3) / 1e9
-        bound, unit, peak, peak_desc = "hbm", "GB/s", hbm_peak, measured_peaks()[1] + " HBM copy bandwidth"
-    else:
-        achieved = flops / (ms * 1e-3) / 1e12
-        bound, unit = "tensor", "TFLOP/s"
+    bound, achieved, peak, unit, peak_desc = roofline_point(flops, algo_bytes, ms, peak, peak_desc)
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": stored_traffic(w["name"]),
                 "peak_kind": peak_desc,

@@ -90,3 +90,15 @@ def test_peak_choice_follows_the_clock_regime():
     else:
         assert capped == burst
     assert bench.bf16_peak(None)[0] == burst
+
+
+def test_roofline_point_picks_the_bound_by_intensity():
+    import bench
+    peaks, _ = bench.measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    # the skinny projection: 60.1 GFLOP over 479.2 MB (125 F/B) is HBM-bound
+    b, a, p, u, _ = bench.roofline_point(60129542144.0, 479199232, 0.0919, 1912.5, "t")
+    assert (b, u, p) == ("hbm", "GB/s", hbm) and abs(a - 479199232 / 0.0919e-3 / 1e9) < 1e-6
+    # 4096^3: 1365 F/B, tensor-bound
+    b, a, p, u, d = bench.roofline_point(2.0 * 4096 ** 3, 100663296, 0.0886, 1912.5, "t")
+    assert (b, u, p, d) == ("tensor", "TFLOP/s", 1912.5, "t") and abs(a - 2.0 * 4096 ** 3 / 0.0886e-3 / 1e12) < 1e-6
