@@ -158,3 +158,16 @@ def test_full_size_workload_sampled_rows(causal):
             ref, bound = oracle.attention(q, k, v, "bf16", D ** -0.5, causal)
             ok, info = oracle.accept_attention(Ob[r0:r1][None, None], ref, bound, "bf16")
             assert ok, (b, h, r0, info)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_query_row(causal):
+    # decode-like: one query row per (batch, head); the CTA's second query
+    # tile is empty and its first holds one valid row (causal: the row is
+    # the last query, so it sees every key)
+    _check((2, 4, 1, D), (2, 4, 1000, D), "bf16", causal, seed=40)
+
+
+def test_many_keys_with_a_ragged_tail():
+    _check((1, 2, 256, D), (1, 2, 4097, D), "f16", False, seed=41)
+    _check((1, 2, 256, D), (1, 2, 4097, D), "bf16", True, seed=42)
