@@ -14,20 +14,14 @@
 //     and each CTA's tensor memory receives its own 128 rows of the result;
 //   * both CTAs' TMA loads complete on the leader's full barrier, which
 //     expects the bytes of both; the leader's commits arrive on the empty
-//     and accumulator-full barriers of both CTAs (multicast);
+//     and accumulator-full barriers of both CTAs (one commit addressed to
+//     both);
 //   * each CTA's epilogue warpgroup drains its own 128 rows and tells the
 //     leader (remote mbarrier arrive) when the accumulator is free again.
 // Everything else -- the persistent schedule over work units, the split-K
 // workspace reduction, the bounded waits -- is the one-SM kernel's.
 //
-// With kPairs = 2 the cluster holds two such pairs side by side along N
-// (4 x 1 CTAs: ranks 0-1 and 2-3), computing the tiles (tm, 2j) and
-// (tm, 2j + 1) of the same A rows.  The CTAs of the two pairs that hold the
-// same 128 A rows each load half of them and TMA-multicast it to both, so
-// each SM fetches 8 KiB of A per K-slice instead of 16 (the cluster network
-// of the TileScale hierarchy sharing operand tiles through distributed
-// shared memory).  A slot of a CTA is then written by both pairs, so its
-// empty barrier waits for both pairs' MMA commits.
+// The pair is the only cluster shape: no operand tile is multicast.
 #pragma once
 
 #include "gemm_sm103.cuh"
@@ -51,43 +45,11 @@ __host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
     return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 7) + 16u;
 }
 
-// The loads of one K-slice by a CTA of a two-pair cluster: its own B
-// columns, and half `pair` (64 rows) of the 128 A rows that the CTAs of
-// rank `half` in both pairs need, multicast to both.  Every byte completes
-// on the barrier `fb` of the destination's pair leader.
-template <int kLayout, int kBCols, bool kF8>
-__device__ __forceinline__ void load_slice_mc(uint32_t a_dst, uint32_t b_dst, const CUtensorMap* tmA,
-                                              const CUtensorMap* tmB, uint32_t fb, bool leader, uint32_t half,
-                                              uint32_t pair, int kb, int32_t row, int32_t col) {
-    static_assert(!kF8 || (a_kmajor(kLayout) && b_kmajor(kLayout)), "8-bit operands are K-major");
-    constexpr int kSK = slice_k<kF8>();
-    const uint16_t mask = static_cast<uint16_t>((1u << half) | (1u << (half + 2u)));
-    const uint32_t a_part = a_dst + pair * 8192u;  // rows [64 pair, 64 pair + 64) of the A tile
-    const int32_t arow = row + 64 * static_cast<int32_t>(pair);
-    if constexpr (a_kmajor(kLayout))
-        tma_load_2d_pair_mc(a_part, tmA, fb, mask, kb * kSK, arow);  // 128 bytes (K) x 64 (M)
-    else
-        tma_load_2d_pair_mc(a_part, tmA, fb, mask, arow, kb * kSK);  // 64 (M) x 64 (K)
-    auto ld = [&](uint32_t dst, int32_t c0, int32_t c1) {
-        if (leader)
-            tma_load_2d(dst, tmB, fb, c0, c1);
-        else
-            tma_load_2d_pair(dst, tmB, fb, c0, c1);
-    };
-    if constexpr (b_kmajor(kLayout)) {
-        ld(b_dst, kb * kSK, col);  // one 128-byte (K) x kBCols (N) box
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBCols / 64; ++j) ld(b_dst + j * 8192u, col + j * 64, kb * kSK);
-    }
-}
-
-template <int BN, int kOut, int kLayout, bool kF8 = false, int kPairs = 1>
-__global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1)
+template <int BN, int kOut, int kLayout, bool kF8 = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_sm103_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     using PS = PairShape<BN>;
-    static_assert(kPairs == 1 || kPairs == 2, "one or two CTA pairs per cluster");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -110,19 +72,16 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();  // 2 * pair + half
-    const uint32_t half = rank & 1u;          // 0: the pair's leader, 1: its peer
-    const uint32_t pair = rank >> 1;          // which pair of the cluster
-    const uint32_t lead_rank = rank & ~1u;
+    const uint32_t half = cluster_ctarank();  // 0: the pair's leader, 1: its peer
     const bool leader = half == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);   // the leader's producer arrives once
-            mbar_init(empty_bar(s), kPairs);  // one multicast commit from each pair's leader
+            mbar_init(empty_bar(s), 1);  // the leader's commit, which arrives in both CTAs
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 1);                    // one multicast commit
+            mbar_init(tfull_bar(a), 1);                    // the leader's commit
             mbar_init(tempty_bar(a), 2 * kEpiWarps);  // every epilogue warp of the pair
         }
         mbar_init(drain_bar, 1);
@@ -142,11 +101,10 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-    for (uint32_t r = 0; r < 2u * kPairs; ++r)
-        if (r != rank) ctl.peer_abort[ctl.npeers++] = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), r);
+    ctl.peer_abort[ctl.npeers++] = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), half ^ 1u);
 
-    const int64_t cluster_id = blockIdx.x / (2 * kPairs);
-    const int64_t nclusters = gridDim.x / (2 * kPairs);
+    const int64_t cluster_id = blockIdx.x / 2;
+    const int64_t nclusters = gridDim.x / 2;
 
     if (warp == 0) {
         // ------------------------------------------- TMA producer (both) --
@@ -172,25 +130,15 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
                     } else {
                         const uint32_t a_dst = base + stage * PS::kStageBytes;
                         const int32_t arow = un.tm * (2 * kBM) + static_cast<int32_t>(half) * kBM;
-                        const int32_t tn = un.tn * kPairs + static_cast<int32_t>(pair);
-                        const int32_t bcol = tn * BN + static_cast<int32_t>(half) * PS::kBCols;
-                        if constexpr (kPairs == 1) {
-                            if (leader) {
-                                mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
-                                load_slice<kLayout, PS::kBCols, false, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
-                                                                            full_bar(stage), kb, arow, bcol);
-                            } else {
-                                load_slice<kLayout, PS::kBCols, true, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
-                                                                           mapa_shared(full_bar(stage), 0u), kb,
-                                                                           arow, bcol);
-                            }
+                        const int32_t bcol = un.tn * BN + static_cast<int32_t>(half) * PS::kBCols;
+                        if (leader) {
+                            mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
+                            load_slice<kLayout, PS::kBCols, false, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                        full_bar(stage), kb, arow, bcol);
                         } else {
-                            // the pair leader's barrier counts the bytes landing in
-                            // both CTAs of the pair, from either pair's loads
-                            const uint32_t fb = leader ? full_bar(stage) : mapa_shared(full_bar(stage), lead_rank);
-                            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
-                            load_slice_mc<kLayout, PS::kBCols, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB, fb,
-                                                                    leader, half, pair, kb, arow, bcol);
+                            load_slice<kLayout, PS::kBCols, true, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                       mapa_shared(full_bar(stage), 0u), kb, arow,
+                                                                       bcol);
                         }
                         outstanding |= 1u << stage;
                         out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
@@ -233,9 +181,8 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
                         const uint32_t a_addr = base + stage * PS::kStageBytes;
                         mma_slice<kLayout, 2, kF8>(d_tmem, a_addr, a_addr + PS::kABytes, p.idesc,
                                               kb > un.kb0 ? 1u : 0u);
-                        // slot free in every CTA whose slot these MMAs read or whose
-                        // loads wrote into it
-                        umma_commit_pair(empty_bar(stage), static_cast<uint16_t>((1u << (2 * kPairs)) - 1u));
+                        // slot free in both CTAs, whose slots these MMAs read
+                        umma_commit_pair(empty_bar(stage), 0x3u);
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -243,13 +190,13 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(tfull_bar(acc), static_cast<uint16_t>(0x3u << lead_rank));
+                umma_commit_pair(tfull_bar(acc), 0x3u);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
-            umma_commit_pair(drain_bar, static_cast<uint16_t>(1u << lead_rank));
+            umma_commit_pair(drain_bar, 0x1u);
             wait_bounded(drain_bar, 0u, ctl, false);
         }
         __syncwarp();
@@ -283,15 +230,14 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
                 if (leader)
                     mbar_arrive(tempty_bar(a));
                 else
-                    mbar_arrive_cluster(tempty_bar(a), lead_rank);
+                    mbar_arrive_cluster(tempty_bar(a), 0u);
             }
         };
-        const EpiAux aux{(cluster_id * kPairs + pair) * 2 + half, 2 * kPairs, base,
+        const EpiAux aux{cluster_id * 2 + half, 2, base,
                          static_cast<uint32_t>(S) * PS::kStageBytes, red_bar};
         for (int64_t j = 0;; ++j) {
             Unit un;
             if (!unit_at(p, cluster_id, nclusters, j, un)) break;
-            un.tn = un.tn * kPairs + static_cast<int>(pair);  // this pair's tile column
             const int tm = un.tm;
             prefetch_sk_partials<BN>(p, un, aux, etid);
             int ok = 1;
@@ -303,7 +249,7 @@ __global__ void __cluster_dims__(2 * kPairs, 1, 1) __launch_bounds__(kThreads, 1
             const int row0 = tm * (2 * kBM) + static_cast<int>(half) * kBM + q * 32;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PS::kAccCols;
             // workspace tile and counter of this CTA's 128-row half
-            const int64_t wh = (un.slot * kPairs + pair) * 2 + half;
+            const int64_t wh = un.slot * 2 + half;
             const int a_now = acc;
             if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, wh, aux, c_begin, etid, last_flag,
                                       ctl, epi_sync, [&]() { release_acc(a_now); }))

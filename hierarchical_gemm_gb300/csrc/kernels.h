@@ -16,10 +16,8 @@ const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8, int cs);
 int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages, int cs);
 
 // The CTA-pair kernel (256 x block_n tiles, block_n 128 or 256), launched
-// with clusters of `pairs` CTA pairs along N (1, or 2 for block_n 256: the
-// pairs share A tiles by TMA multicast); null for an unsupported
-// combination.
-const void* kernel_2sm(int block_n, int out_kind, int layout, bool in8, int pairs);
+// as 2 x 1 clusters; null for an unsupported combination.
+const void* kernel_2sm(int block_n, int out_kind, int layout, bool in8);
 
 // Dynamic shared memory per CTA of the pair kernel with `stages` slots.
 int64_t kernel_2sm_smem_bytes(int block_n, int out_kind, int stages);
@@ -29,12 +27,12 @@ const void* kernel_1sm_layout0(int block_n, int out_kind);
 const void* kernel_1sm_layout1(int block_n, int out_kind);
 const void* kernel_1sm_layout2(int block_n, int out_kind);
 const void* kernel_1sm_layout3(int block_n, int out_kind);
-const void* kernel_2sm_layout0(int block_n, int out_kind, int pairs);
-const void* kernel_2sm_layout1(int block_n, int out_kind, int pairs);
-const void* kernel_2sm_layout2(int block_n, int out_kind, int pairs);
-const void* kernel_2sm_layout3(int block_n, int out_kind, int pairs);
+const void* kernel_2sm_layout0(int block_n, int out_kind);
+const void* kernel_2sm_layout1(int block_n, int out_kind);
+const void* kernel_2sm_layout2(int block_n, int out_kind);
+const void* kernel_2sm_layout3(int block_n, int out_kind);
 const void* kernel_1sm_f8(int block_n, int out_kind);
 const void* kernel_1sm_cs(int block_n, int out_kind);
-const void* kernel_2sm_f8(int block_n, int out_kind, int pairs);
+const void* kernel_2sm_f8(int block_n, int out_kind);
 
 }  // namespace tsg

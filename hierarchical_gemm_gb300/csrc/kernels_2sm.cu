@@ -1,6 +1,6 @@
 // kernels_2sm.cu -- the host-side lookup of the CTA-pair kernel's
-// instantiations (by tile width, output format, operand layout, input width
-// and pairs per cluster) and of the shared memory each needs.
+// instantiations (by tile width, output format, operand layout and input
+// width) and of the shared memory each needs.
 #include "gemm_sm103_2sm.cuh"
 #include "kernels.h"
 
@@ -8,13 +8,13 @@
 
 namespace tsg {
 
-const void* kernel_2sm(int block_n, int out_kind, int layout, bool in8, int pairs) {
-    if (in8) return layout == 1 ? kernel_2sm_f8(block_n, out_kind, pairs) : nullptr;
+const void* kernel_2sm(int block_n, int out_kind, int layout, bool in8) {
+    if (in8) return layout == 1 ? kernel_2sm_f8(block_n, out_kind) : nullptr;
     switch (layout) {
-        case 0: return kernel_2sm_layout0(block_n, out_kind, pairs);
-        case 1: return kernel_2sm_layout1(block_n, out_kind, pairs);
-        case 2: return kernel_2sm_layout2(block_n, out_kind, pairs);
-        case 3: return kernel_2sm_layout3(block_n, out_kind, pairs);
+        case 0: return kernel_2sm_layout0(block_n, out_kind);
+        case 1: return kernel_2sm_layout1(block_n, out_kind);
+        case 2: return kernel_2sm_layout2(block_n, out_kind);
+        case 3: return kernel_2sm_layout3(block_n, out_kind);
         default: return nullptr;
     }
 }

@@ -78,23 +78,21 @@ struct Estimate {
 };
 
 // bm = 128: one CTA per 128 x bn tile; bm = 256: a CTA pair per 256 x bn
-// tile, each SM computing 128 rows and loading half of the B slice; cn = 2:
-// two pairs per cluster on adjacent tiles, each SM loading half of its A
-// slice (the other half arrives by multicast).  A work unit covers cn
-// tiles.  The last `split_tiles` units of the schedule are split into
-// `splits` K parts (all of them, or only the tail wave's, or none).
-Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int cn, int splits,
+// tile, each SM computing 128 rows and loading half of the B slice.  The
+// last `split_tiles` tiles of the schedule are split into `splits` K parts
+// (all of them, or only the tail wave's, or none).
+Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int splits,
                   int64_t split_tiles, int num_sms) {
-    const int64_t tiles = ceil_div(M, bm) * ceil_div(ceil_div(N, bn), cn);
+    const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
     const int64_t full = tiles - split_tiles;
     const int64_t units = full + split_tiles * splits;
-    const int64_t slots = std::max(1, num_sms / ((bm / kBM) * cn));
+    const int64_t slots = std::max(1, num_sms / (bm / kBM));
     const int64_t grid = std::min<int64_t>(units, slots);
     const int64_t kblocks = ceil_div(K, slice_k(din));
     const double kb_split = std::ceil(static_cast<double>(kblocks) / splits);
     const double mma = kBM * bn * static_cast<double>(kBK) / kMacsPerCycle;
     const double b_bytes = (bm == 256 ? bn / 2 : bn) * kBK * 2.0;
-    const double load = (kBM * kBK * 2.0 / cn + b_bytes) / kL2BytesPerCycle;
+    const double load = (kBM * kBK * 2.0 + b_bytes) / kL2BytesPerCycle;
     const double per_kb = std::max(mma, load);
     // round-robin over `grid` slots: whole tiles first, then split parts
     const double whole_rounds = static_cast<double>(ceil_div(full, grid));
@@ -109,7 +107,7 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, in
         // (in every round of split units)
         compute += split_rounds * 2.0 * (splits - 1) / splits * static_cast<double>(kBM) * bn * 4.0 /
                    kReduceBytesPerCycle;
-        const double ws = 2.0 * 4.0 * (splits - 1) * static_cast<double>(split_tiles) * bm * bn * cn;
+        const double ws = 2.0 * 4.0 * (splits - 1) * static_cast<double>(split_tiles) * bm * bn;
         bytes += ws;
     }
     const double hbm = bytes / kHbmBytesPerCycle;
@@ -122,14 +120,14 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, in
 // first part's CTA the final add, both hidden behind the next mainloop;
 // with no whole tiles the add comes at the very end, after a copy of the
 // partials into the idle ring.
-Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int cn, int64_t sk,
+Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int64_t sk,
                      int num_sms) {
-    const int64_t tiles = ceil_div(M, bm) * ceil_div(ceil_div(N, bn), cn);
-    const int64_t slots = std::max(1, num_sms / ((bm / kBM) * cn));
+    const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
+    const int64_t slots = std::max(1, num_sms / (bm / kBM));
     const int64_t kblocks = ceil_div(K, slice_k(din));
     const double mma = kBM * bn * static_cast<double>(kBK) / kMacsPerCycle;
     const double b_bytes = (bm == 256 ? bn / 2 : bn) * kBK * 2.0;
-    const double load = (kBM * kBK * 2.0 / cn + b_bytes) / kL2BytesPerCycle;
+    const double load = (kBM * kBK * 2.0 + b_bytes) / kL2BytesPerCycle;
     const double per_kb = std::max(mma, load);
     const double dp_rounds = static_cast<double>(ceil_div(tiles - sk, slots));
     const double sk_slices = std::ceil(static_cast<double>(sk) * kblocks / slots);
@@ -147,7 +145,7 @@ Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm,
     double compute = dp_rounds * (kblocks * per_kb + kUnitOverhead) + sk_slices * per_kb + 2 * kUnitOverhead + tail;
     double bytes = static_cast<double>(in_bytes(din)) * (M * K + K * N) +
                    static_cast<double>(out_bytes(dout)) * M * N +
-                   2.0 * 4.0 * static_cast<double>(slots) * bm * bn * cn;
+                   2.0 * 4.0 * static_cast<double>(slots) * bm * bn;
     const double hbm = bytes / kHbmBytesPerCycle;
     return {std::max(compute, hbm) + 0.05 * compute, compute};
 }
@@ -212,7 +210,6 @@ static tsgemm_status_t choose_cluster_split(int64_t M, int64_t N, int64_t K, int
     if (f.stages > smax_fit || (f.stages != 0 && f.stages < 2)) return TSGEMM_ERR_UNSUPPORTED;
     c.stages = f.stages ? f.stages : smax_fit;
     c.group_m = f.group_m ? f.group_m : 8;
-    c.cluster_n = 1;
     c.cluster_split = 2;
     const int64_t tiles = ceil_div(M, 128) * ceil_div(N, bn);
     c.units = tiles;
@@ -245,15 +242,12 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
         return TSGEMM_ERR_INVALID_ARG;
     if (f.units != 0 || f.workspace_bytes != 0) return TSGEMM_ERR_INVALID_ARG;  // derived fields
     if (f.split_tiles < 0 || (f.split_tiles > 0 && f.splits < 2)) return TSGEMM_ERR_INVALID_ARG;
-    if (f.cluster_n < 0 || f.cluster_n > 2) return TSGEMM_ERR_UNSUPPORTED;
-    if (f.cluster_n == 2 && (f.block_m == 128 || (f.block_n != 0 && f.block_n != 256) || num_sms < 4))
-        return TSGEMM_ERR_UNSUPPORTED;
     if (f.stream_k_tiles < -1) return TSGEMM_ERR_INVALID_ARG;
     if (f.cluster_split < 0 || f.cluster_split > 2) return TSGEMM_ERR_UNSUPPORTED;
     if (f.cluster_split == 2) {
         // the DSMEM K split: one-SM tiles, each split in two between the
         // CTAs of a 2 x 1 cluster; RRR layout and 16-bit inputs
-        if (f.block_m == 256 || f.splits > 1 || f.split_tiles > 0 || f.stream_k_tiles > 0 || f.cluster_n == 2)
+        if (f.block_m == 256 || f.splits > 1 || f.split_tiles > 0 || f.stream_k_tiles > 0)
             return TSGEMM_ERR_INVALID_ARG;
         if (layout != TSGEMM_LAYOUT_RRR || is_8bit(dtype_in) || num_sms < 2) return TSGEMM_ERR_UNSUPPORTED;
     }
@@ -268,7 +262,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
 
     // Candidate tile widths: never wider than N rounded up to 64.
     const int64_t n_pad = ceil_div(N, 64) * 64;
-    int best_bm = 0, best_bn = 0, best_cn = 1, best_s = 0;
+    int best_bm = 0, best_bn = 0, best_s = 0;
     int64_t best_st = 0, best_sk = 0;
     double best = 0;
     const int bms[2] = {256, 128};  // pairs first: ties go to the pair
@@ -277,15 +271,11 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
         if (f.block_m && bm != f.block_m) continue;
         if (bm == 256 && num_sms < 2) continue;
         for (int bn : bns) {
-          if (bm == 256 && bn != 128 && bn != 256) continue;
-          if (f.block_n && bn != f.block_n) continue;
-          if (!f.block_n && bn > n_pad && bn != 64 && !(bm == 256 && bn == 128)) continue;
-          // pairs per cluster: one first, so that ties keep it
-          for (int cn = 1; cn <= 2; ++cn) {
-            if (f.cluster_n ? cn != f.cluster_n : cn != 1) continue;
-            if (cn == 2 && (bm != 256 || bn != 256 || num_sms < 4)) continue;
-            const int64_t slots = num_sms / ((bm / kBM) * cn);
-            const int64_t tiles = ceil_div(M, bm) * ceil_div(ceil_div(N, bn), cn);
+            if (bm == 256 && bn != 128 && bn != 256) continue;
+            if (f.block_n && bn != f.block_n) continue;
+            if (!f.block_n && bn > n_pad && bn != 64 && !(bm == 256 && bn == 128)) continue;
+            const int64_t slots = num_sms / (bm / kBM);
+            const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
             const int smax = f.splits ? f.splits
                                       : static_cast<int>(std::min<int64_t>(
                                             std::min<int64_t>(kMaxSplits, slots), std::max<int64_t>(1, kblocks / 4)));
@@ -304,12 +294,11 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                     // every slot needs at least one K slice, so that the
                     // slots sharing a tile are consecutive
                     if (sk <= 0 || sk > tiles || sk * kblocks < slots) continue;
-                    const Estimate e = estimate_sk(M, N, K, dtype_in, dtype_out, bm, bn, cn, sk, num_sms);
+                    const Estimate e = estimate_sk(M, N, K, dtype_in, dtype_out, bm, bn, sk, num_sms);
                     if (best_bn == 0 || e.cycles < best * 0.999) {
                         best = e.cycles;
                         best_bm = bm;
                         best_bn = bn;
-                        best_cn = cn;
                         best_s = 1;
                         best_st = 0;
                         best_sk = sk;
@@ -332,20 +321,18 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                 for (int64_t st : options) {
                     if (st < 0 || st > tiles) continue;
                     if (!f.splits && parts_straddle(tiles - st, st, s, slots)) continue;
-                    const Estimate e = estimate(M, N, K, dtype_in, dtype_out, bm, bn, cn, s, st, num_sms);
+                    const Estimate e = estimate(M, N, K, dtype_in, dtype_out, bm, bn, s, st, num_sms);
                     // strict improvement required: ties keep the earlier candidate
                     if (best_bn == 0 || e.cycles < best * 0.999) {
                         best = e.cycles;
                         best_bm = bm;
                         best_bn = bn;
-                        best_cn = cn;
                         best_s = s;
                         best_st = st;
                         best_sk = 0;
                     }
                 }
             }
-          }
         }
     }
     if (best_bn == 0) return TSGEMM_ERR_UNSUPPORTED;
@@ -358,14 +345,13 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     if (f.stages > smax_fit || (f.stages != 0 && f.stages < 2)) return TSGEMM_ERR_UNSUPPORTED;
     c.stages = f.stages ? f.stages : smax_fit;
     c.group_m = f.group_m ? f.group_m : 8;
-    c.cluster_n = best_cn;
     c.cluster_split = 1;
-    const int64_t tiles = ceil_div(M, best_bm) * ceil_div(ceil_div(N, best_bn), best_cn);
+    const int64_t tiles = ceil_div(M, best_bm) * ceil_div(N, best_bn);
     c.split_tiles = best_s > 1 ? best_st : 0;
     c.stream_k_tiles = best_sk;
     c.units = (tiles - c.split_tiles) + c.split_tiles * best_s;
-    // a pair kernel launches two CTAs per unit slot, a two-pair cluster four
-    const int64_t ctas_per_slot = (best_bm / kBM) * best_cn;
+    // a pair kernel launches two CTAs per unit slot
+    const int64_t ctas_per_slot = best_bm / kBM;
     int64_t slots = (f.grid ? f.grid : num_sms) / ctas_per_slot;
     if (slots < 1) return TSGEMM_ERR_UNSUPPORTED;
     if (best_sk > 0) {
@@ -380,7 +366,7 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
         c.units = tiles - best_sk + segs;
         c.grid = static_cast<int32_t>(slots * ctas_per_slot);
         // one fp32 partial slot per CTA half of each slot
-        c.workspace_bytes = slots * best_bm * static_cast<int64_t>(best_bn) * best_cn * 4;
+        c.workspace_bytes = slots * best_bm * static_cast<int64_t>(best_bn) * 4;
         c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
         c.debug_flags = f.debug_flags;
         *out = c;
@@ -390,9 +376,9 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     // part 0 of a split tile waits for parts 1..S-1, which must run on other
     // CTAs (pairs) at the same time: S may not exceed the grid's slots
     if (c.split_tiles > 0 && best_s > c.grid / ctas_per_slot) return TSGEMM_ERR_UNSUPPORTED;
-    // S fp32 partial slots per split unit (cn tiles); each part fills the
-    // chunks it does not own
-    c.workspace_bytes = c.split_tiles * best_s * best_bm * static_cast<int64_t>(best_bn) * best_cn * 4;
+    // S fp32 partial slots per split tile; each part fills the chunks it
+    // does not own
+    c.workspace_bytes = c.split_tiles * best_s * best_bm * static_cast<int64_t>(best_bn) * 4;
     c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
     c.debug_flags = f.debug_flags;
     *out = c;

@@ -129,9 +129,9 @@ struct WaitCtl {
     volatile int* abort;   // shared memory
     int* status;           // global status word of the plan
     uint64_t timeout_ns;
-    // shared::cluster addresses of the abort flags of the other CTAs of the
-    // cluster (at most 3), which a CTA that gives up sets too
-    uint32_t peer_abort[3] = {0u, 0u, 0u};
+    // shared::cluster address of the abort flag of the other CTA of a 2 x 1
+    // cluster, which a CTA that gives up sets too
+    uint32_t peer_abort[1] = {0u};
     int npeers = 0;
 };
 
@@ -230,20 +230,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
         "bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(m), "r"(bar_cluster), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// Multicast form of tma_load_2d_pair: the box lands at `dst` in every CTA
-// of `cta_mask` (bit i = cluster rank i).  The bytes that land in a CTA
-// complete on the barrier at the offset of `bar_cluster` in the even CTA of
-// that destination's pair (the address passed is the issuing pair's even
-// CTA's barrier).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster,
-                                                    uint16_t cta_mask, int32_t c0, int32_t c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
-        "bytes.multicast::cluster [%0], [%1, {%4, %5}], [%2], %3;" ::"r"(dst),
-        "l"(m), "r"(bar_cluster), "h"(cta_mask), "r"(c0), "r"(c1)
         : "memory");
 }
 

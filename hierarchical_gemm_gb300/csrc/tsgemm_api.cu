@@ -141,7 +141,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     const bool pair = cfg.block_m == 256;
     const bool in8 = tsg::is_8bit(dtype_in);
     const int cs = cfg.cluster_split == 2 ? 2 : 1;
-    const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out), layout, in8, cfg.cluster_n)
+    const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out), layout, in8)
                             : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out), layout, in8, cs);
     const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages)
                               : tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages, cs);
@@ -161,7 +161,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     if (pair || cs == 2) {
         // Persistent clusters: launch no more than can be resident at once
         // (a cluster's CTAs must share a GPC).
-        const int per_cluster = pair ? 2 * cfg.cluster_n : 2;
+        const int per_cluster = 2;
         cudaLaunchConfig_t lc{};
         lc.gridDim = dim3(static_cast<unsigned>(cfg.grid), 1, 1);
         lc.blockDim = dim3(tsg::kThreads, 1, 1);
@@ -202,8 +202,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     p->smem = smem;
     // split-K (stream-K) counters: one per 128-row half of each tile of a
     // split (stream-K) unit (pairs reduce halves)
-    p->num_tiles = (cfg.stream_k_tiles > 0 ? cfg.stream_k_tiles : cfg.split_tiles) * (cfg.block_m / 128) *
-                   cfg.cluster_n;
+    p->num_tiles = (cfg.stream_k_tiles > 0 ? cfg.stream_k_tiles : cfg.split_tiles) * (cfg.block_m / 128);
 
     if (cudaMalloc(&p->status_d, sizeof(int)) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -234,9 +233,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.N = static_cast<int32_t>(N);
     gp.K = static_cast<int32_t>(K);
     gp.tiles_m = static_cast<int32_t>((M + cfg.block_m - 1) / cfg.block_m);
-    // (a two-pair cluster's unit spans two tile columns)
-    const int64_t tiles_n = (N + cfg.block_n - 1) / cfg.block_n;
-    gp.tiles_n = static_cast<int32_t>((tiles_n + cfg.cluster_n - 1) / cfg.cluster_n);
+    gp.tiles_n = static_cast<int32_t>((N + cfg.block_n - 1) / cfg.block_n);
     gp.splits = cfg.splits;
     gp.kblocks = static_cast<int32_t>((K + tsg::slice_k(dtype_in) - 1) / tsg::slice_k(dtype_in));
     gp.group_m = cfg.group_m;
@@ -304,16 +301,14 @@ static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* 
     };
     // Every box is 128 bytes (one swizzle row) along the contiguous
     // dimension: 64 16-bit or 128 8-bit elements.
-    //   A stored M x K: 128 B (K) x 128 (M) boxes (x 64 when two pairs share
-    //   A, each loading half);                      A stored K x M: 64 (M) x 64 (K)
+    //   A stored M x K: 128 B (K) x 128 (M) boxes;  A stored K x M: 64 (M) x 64 (K)
     //   B stored K x N: 64 (N) x 64 (K) boxes;      B stored N x K: 128 B (K) x
     //   the CTA's columns (N) -- block_n, or block_n / 2 for a CTA pair
     // (8-bit operands are always stored K-major, the first form of each).
     const cuuint32_t kbox = static_cast<cuuint32_t>(128 / eb);
     const bool ak = tsg::a_kmajor(p->layout), bk = tsg::b_kmajor(p->layout);
     const cuuint32_t b_cols = static_cast<cuuint32_t>(p->cfg.block_m == 256 ? p->cfg.block_n / 2 : p->cfg.block_n);
-    const cuuint32_t a_rows = p->cfg.cluster_n == 2 ? 64 : 128;
-    const bool ok_a = ak ? tile_map(&p->tmA, A, p->K, p->M, kbox, a_rows) : tile_map(&p->tmA, A, p->M, p->K, 64, 64);
+    const bool ok_a = ak ? tile_map(&p->tmA, A, p->K, p->M, kbox, 128) : tile_map(&p->tmA, A, p->M, p->K, 64, 64);
     const bool ok_b = bk ? tile_map(&p->tmB, B, p->K, p->N, kbox, b_cols) : tile_map(&p->tmB, B, p->N, p->K, 64, 64);
     return ok_a && ok_b ? TSGEMM_OK : TSGEMM_ERR_CUDA;
 }

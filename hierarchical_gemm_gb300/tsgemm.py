@@ -46,8 +46,8 @@ class Config(ctypes.Structure):
                 ("group_m", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("timeout_ms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-                ("split_tiles", ctypes.c_int64), ("cluster_n", ctypes.c_int32),
-                ("stream_k_tiles", ctypes.c_int64), ("cluster_split", ctypes.c_int32)]
+                ("split_tiles", ctypes.c_int64), ("stream_k_tiles", ctypes.c_int64),
+                ("cluster_split", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

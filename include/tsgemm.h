@@ -101,17 +101,13 @@ typedef struct {
     int32_t grid;         /* CTAs launched (persistent) */
     int64_t units;        /* work units = whole tiles + split_tiles * splits */
     int64_t workspace_bytes; /* split-K (stream-K) partials owned by the plan:
-                                split_tiles * splits * block_m * block_n *
-                                cluster_n * 4 bytes (see stream_k_tiles) */
+                                split_tiles * splits * block_m * block_n * 4
+                                bytes (see stream_k_tiles) */
     int32_t timeout_ms;   /* limit of every device-side wait */
     int32_t debug_flags;  /* tests only: TSGEMM_DEBUG_* */
     int64_t split_tiles;  /* work units split into `splits` K parts: the last
                              ones of the schedule (all, or the last partial
                              wave). Forced with splits > 1; 0 then means all. */
-    int32_t cluster_n;    /* CTA pairs per cluster along N (block_m 256 only):
-                             1, or 2 = two pairs compute adjacent 256 x 256
-                             tiles of the same A rows and share those A tiles
-                             by TMA multicast (a work unit is then 2 tiles) */
     int64_t stream_k_tiles; /* stream-K: the last stream_k_tiles tiles (units)
                                of the schedule have their K slices spread
                                evenly over all CTAs (CTA pairs), after rounds
@@ -119,8 +115,8 @@ typedef struct {
                                finished by the CTA holding its first K slices.
                                Excludes splits > 1. Forced: > 0 a count, -1
                                none, 0 the planner's choice. The workspace is
-                               then one block_m x block_n x cluster_n fp32
-                               partial per slot. */
+                               then one block_m x block_n fp32 partial per
+                               slot. */
     int32_t cluster_split;  /* 2: the DSMEM split of K (block_m 128, RRR
                                layout, 16-bit inputs): the two CTAs of a 2 x 1
                                cluster compute the two halves of every tile's

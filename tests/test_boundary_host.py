@@ -241,21 +241,33 @@ def test_fp8_dtype_names(ts):
     assert ts.dtype_code(torch.float8_e5m2) == ts.E5M2 == 4
 
 
-# ------------------------------------------- two CTA pairs per cluster --
+# ----------------------------------------------- no multicast option --
 
-def test_cluster_n_rules(ts):
-    cfg = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, cluster_n=2, stream_k_tiles=-1)
-    assert cfg["cluster_n"] == 2 and cfg["block_m"] == 256 and cfg["block_n"] == 256
-    assert cfg["grid"] % 4 == 0 and cfg["grid"] <= 152
-    # a unit is two tiles: 16 tile rows x 8 column pairs
-    assert cfg["units"] == 16 * 8 + cfg["split_tiles"] * (cfg["splits"] - 1)
-    assert cfg["workspace_bytes"] == cfg["split_tiles"] * cfg["splits"] * 256 * 512 * 4
-    for force in [dict(cluster_n=2, block_m=128), dict(cluster_n=2, block_n=128), dict(cluster_n=3)]:
-        with pytest.raises(ts.TsgemmError) as e:
-            ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, **force)
-        assert e.value.status == ts.ERR_UNSUPPORTED, force
-    # unforced plans on one SM tile keep one pair (or no pair) per cluster
-    assert ts.choose_config(128, 28672, 8192, "bf16", "bf16", 152)["cluster_n"] == 1
+def test_no_multicast_cluster_option(ts):
+    # The CTA pair (2 x 1 cluster) is the only cluster shape of the GEMM:
+    # there is no field that selects clusters of several pairs sharing
+    # operand tiles by multicast.
+    assert "cluster_n" not in ts.Config().as_dict()
+    with pytest.raises(TypeError):
+        ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, cluster_n=2)
+    cfg = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152)
+    assert cfg["block_m"] == 256 and cfg["grid"] % 2 == 0
+
+
+def test_library_has_no_multicast_load():
+    # No source of the library issues a multicast TMA load (the only
+    # .multicast::cluster left is the pair's tcgen05.commit, an mbarrier
+    # arrive addressed to both CTAs of the pair).
+    import glob
+    import os
+    import re
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "hierarchical_gemm_gb300", "csrc")
+    for path in glob.glob(os.path.join(csrc, "*")):
+        with open(path) as f:
+            for line in f:
+                if "multicast::cluster" in line:
+                    assert re.search(r"tcgen05\.commit", line), (path, line)
 
 
 # ---------------------------------------------------------- stream-K --

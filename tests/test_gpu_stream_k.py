@@ -5,7 +5,7 @@ The K slices of the schedule's last tiles are spread evenly over all CTAs
 its first K slices, which adds the other parts' fp32 partials in K order.
 The cases cover the owner reading one partial and several, from the idle
 operand ring (bulk copies) and straight from global memory, one-SM tiles,
-CTA pairs and two-pair clusters, the 8-bit inputs, ragged shapes and an
+CTA pairs, the 8-bit inputs, ragged shapes and an
 expired bounded wait.  Integer inputs make every order of fp32 addition
 exact, so those results are compared bit for bit.
 """
@@ -40,8 +40,8 @@ CASES = [
     (1024, 1024, 2048, dict(block_m=128, block_n=128, stream_k_tiles=64)),
     # one-SM, ragged M / N / K, a few tiles
     (1000, 1288, 328, dict(block_m=128, block_n=128, stream_k_tiles=30)),
-    # two pairs per cluster sharing A, ragged N
-    (2048, 2304, 1024, dict(block_m=256, block_n=256, cluster_n=2, stream_k_tiles=20)),
+    # pairs, ragged N
+    (2048, 2304, 1024, dict(block_m=256, block_n=256, stream_k_tiles=20)),
     # pairs with 128-wide tiles
     (1536, 1536, 2560, dict(block_m=256, block_n=128, stream_k_tiles=30)),
 ]
