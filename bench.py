@@ -3,17 +3,24 @@
 
 One step is one C = A * B of the benchmark workload (default: M = N = K =
 4096, bf16 inputs drawn from N(0, 1), fp32 accumulation, bf16 output) on
-inputs already resident in HBM.  The L2 cache (129 MB, larger than the
-96 MB working set) is flushed between steps by writing a 256 MB buffer; each
-step's GEMM is timed with CUDA events on the launching stream.
+inputs already resident in HBM.  Between steps the L2 cache (129 MB) is
+flushed by a read-only sweep of a 256 MB buffer (a sum into one scalar): the
+sweep evicts the previous step's lines, including the dirty lines of its
+output, and leaves none dirty, so no write-back of earlier data falls into a
+timed step.  Each step's GEMM is timed with CUDA events on the launching
+stream.
 
 Prints one JSON line.  `value` is TFLOP/s (2*M*N*K per step) over all ranks;
 `e2e` is the same metric through the same C ABI call with pinned host
 buffers, the host->device copies of A and B and the device->host copy of C
 inside the timed region; `roofline` relates the kernel to the measured bf16
-tensor peak (for 8-bit inputs: twice that, the nominal fp8 : bf16 ratio);
-`cpu_baseline` is the fp64 oracle timed on the host cores.  --workload picks
-another seeded workload (the five benchmark configurations, or the FP8 ones).
+tensor peak (for 8-bit inputs: twice that, the nominal fp8 : bf16 ratio),
+or, below the ridge, to the measured HBM copy bandwidth; `cpu_baseline` is
+the fp64 oracle timed on the host cores.  `workloads` holds the same
+measurement (time per step, roofline, clocks, a sampled parity check) for
+every other benchmark configuration and the 8-bit workloads, each timed
+over the same number of steps after the headline.  --workload picks another
+headline workload.
 
 With --impl reference the fp64 CPU oracle itself is timed on the same
 metric (a bounded sample of rows of the product per step).
@@ -43,12 +50,11 @@ METRIC = "GEMM TFLOP/s and % of GB300 dense BF16 peak (4096^3; 16384x16384x8192)
 FLUSH_BYTES = 256 << 20
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# Source files whose change invalidates a stored ncu traffic figure.
-KERNEL_SOURCES = ["hierarchical_gemm_gb300/csrc/gemm_sm103.cuh",
-                  "hierarchical_gemm_gb300/csrc/gemm_sm103_2sm.cuh",
-                  "hierarchical_gemm_gb300/csrc/ptx.cuh",
-                  "hierarchical_gemm_gb300/csrc/kernels_1sm.cu",
-                  "hierarchical_gemm_gb300/csrc/kernels_2sm.cu"]
+# Every workload timed after the headline one: the five benchmark
+# configurations and the 8-bit workloads.
+EXTRA_DEFAULT = ["gemm_256_f16_f32", "gemm_4096_bf16", "skinny_128x28672x8192_bf16",
+                 "gemm_16384x16384x8192_bf16", "longk_1024x1024x65536_int_f32",
+                 "gemm_4096_e4m3_rcr", "gemm_16384x16384x8192_e4m3_rcr"]
 # nominal dense fp8 : bf16 tensor throughput on GB300 (4.5 : 2.25 PFLOP/s)
 FP8_TO_BF16 = 2.0
 
@@ -81,7 +87,10 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--plan", default="",
-                    help="force plan fields, e.g. block_m=256,block_n=128,splits=1")
+                    help="force plan fields of the headline workload, e.g. block_m=256,block_n=128,splits=1")
+    ap.add_argument("--workloads", default="all",
+                    help="workloads timed after the headline: 'all' (every benchmark configuration and "
+                         "the 8-bit workloads), 'none', or a comma-separated list")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -242,13 +251,20 @@ def roofline_point(flops, algo_bytes, ms, tensor_peak, tensor_desc):
     return "tensor", flops / (ms * 1e-3) / 1e12, tensor_peak, "TFLOP/s", tensor_desc
 
 
-ATTN_SOURCES = ["hierarchical_gemm_gb300/csrc/attention_sm103.cu",
-                "hierarchical_gemm_gb300/csrc/ptx.cuh"]
+def kernel_sources():
+    """Every file the library is built from (kernels, launch code, planner,
+    instantiation tables, headers): a change to any of them may change a
+    kernel's schedule and so its DRAM traffic."""
+    import glob
+    files = glob.glob(os.path.join(ROOT, "hierarchical_gemm_gb300", "csrc", "*"))
+    files += glob.glob(os.path.join(ROOT, "include", "*.h"))
+    return sorted(os.path.relpath(f, ROOT) for f in files if os.path.isfile(f))
 
 
-def kernel_source_hash(sources=None):
+def kernel_source_hash():
     h = hashlib.sha256()
-    for rel in sources or KERNEL_SOURCES:
+    for rel in kernel_sources():
+        h.update(rel.encode())
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -256,7 +272,7 @@ def kernel_source_hash(sources=None):
 
 def stored_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    with the current kernel source (the files the entry names); else None."""
+    with the current library source; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -264,7 +280,7 @@ def stored_traffic(workload):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash(e.get("sources")):
+    if not e or e.get("source_hash") != kernel_source_hash():
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -322,9 +338,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w["name"], "M": w["M"], "N": w["N"], "K": w["K"],
-                   "dtype_in": w["dtype_in"], "dtype_out": w["dtype_out"],
-                   "sample_rows": rows},
+        "config": gemm_config(w, 1),
+        "sample_rows": rows,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -334,11 +349,132 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ ours --
 
+class L2Sweep:
+    """Read-only L2 flush: a sum of a 256 MB buffer (about twice the L2)
+    into one scalar.  Reading evicts every line the previous step left in
+    L2, dirty ones included (their write-back happens here, outside the
+    timed region), and writes nothing but the scalar."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        torch.sum(self.buf, dtype=torch.float32, out=self.sink)
+
+
+def time_plan(plan, A, B, C, steps, warmup, dev, stream, flush, sampler_gpu, world):
+    """Warm up, then time `steps` launches of the plan (each after an L2
+    sweep) with CUDA events on the launching stream.  Returns (ms per step,
+    max over ranks; clock summary or None)."""
+    import torch
+    from hierarchical_gemm_gb300 import tsgemm
+    for _ in range(warmup):
+        flush()
+        plan.run(A, B, C, stream)
+    torch.cuda.synchronize(dev)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError("device status %d (%s) after warm-up" % (st, tsgemm.status_string(st)))
+    sampler = ClockSampler(sampler_gpu) if sampler_gpu is not None else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        plan.run(A, B, C, stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_wall1 = time.time()
+    clocks = None
+    if sampler:
+        sampler.mark(t_wall0, t_wall1)
+        clocks = sampler.stop()
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError("device status %d (%s)" % (st, tsgemm.status_string(st)))
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
+    return max_over_ranks(ms, world, dev), clocks
+
+
+def sampled_parity(C, A_np, B_np, w, count=1024, seed=7):
+    """The oracle at `count` random outputs of this run's C."""
+    import torch
+    import oracle
+    M, N = w["M"], w["N"]
+    r = np.random.default_rng(seed)
+    rows = r.integers(0, M, count)
+    cols = r.integers(0, N, count)
+    Ch = C.cpu()
+    Ch = Ch.numpy() if w["dtype_out"] == "f32" else Ch.view(torch.int16).numpy().view(np.uint16)
+    ref, sabs = oracle.gemm_sampled(A_np, B_np, w["dtype_in"], rows, cols)
+    ok, info = oracle.accept(Ch[rows, cols], ref, sabs, w["dtype_out"], exact=w["exact"])
+    return {"sampled_outputs": int(count), "ok": bool(ok), "exact": bool(w["exact"]),
+            "max_err_over_bound": info.get("max_err_over_bound"), "mismatches": info.get("mismatches")}
+
+
+def gemm_roofline(w, ms, clocks, cfg):
+    """The roofline object of one GEMM workload timed at `ms` per launch."""
+    import synth
+    M, N, K = w["M"], w["N"], w["K"]
+    din, dout = w["dtype_in"], w["dtype_out"]
+    flops = 2.0 * M * N * K
+    peak, peak_desc = bf16_peak(clocks)
+    eight_bit = din in ("e4m3", "e5m2")
+    if eight_bit:
+        peak *= FP8_TO_BF16
+        peak_desc += " x %.0f (nominal fp8 : bf16 dense ratio)" % FP8_TO_BF16
+    algo_bytes = synth.workloads.in_nbytes(din) * (M * K + K * N) + synth.workloads.out_nbytes(dout) * M * N
+    bound, achieved, peak, unit, peak_desc = roofline_point(flops, algo_bytes, ms, peak, peak_desc)
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": stored_traffic(w["name"]),
+            "peak_kind": peak_desc,
+            "kernel": "gemm_sm103_%s<BN=%d%s>" % ("2sm" if cfg["block_m"] == 256 else "1sm", cfg["block_n"],
+                                                 ", 8-bit" if eight_bit else ""),
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": algo_bytes}
+
+
+def gemm_config(w, world):
+    """The `config` object of a GEMM workload's line (the same for both
+    arms of the benchmark)."""
+    return {"workload": w["name"], "M": w["M"], "N": w["N"], "K": w["K"], "dtype_in": w["dtype_in"],
+            "layout": w["layout"], "dtype_out": w["dtype_out"], "accumulate": "f32",
+            "l2": "flushed between steps (read-only sweep of a 256 MB buffer)",
+            "parallelism": "independent replica per GPU" if world > 1 else "1 GPU"}
+
+
+PLAN_KEYS = ("block_m", "block_n", "splits", "split_tiles", "stream_k_tiles", "stages", "group_m", "grid")
+
+
+def load_workload(name, dev, off):
+    """Seeded host inputs of a workload and their device copies as the
+    library is handed them (per the workload's layout)."""
+    import torch
+    import synth
+    w = synth.workload(name)
+    A_np = synth.matrix(w["M"], w["K"], w["dist_a"], w["seed_a"] + off, w["dtype_in"])
+    B_np = synth.matrix(w["K"], w["N"], w["dist_b"], w["seed_b"] + off, w["dtype_in"])
+    A_st, B_st = synth.stored(A_np, B_np, w["layout"])
+    A = to_device_bits(A_st, w["dtype_in"], dev)
+    B = to_device_bits(B_st, w["dtype_in"], dev)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    C = torch.empty((w["M"], w["N"]), dtype=tdt[w["dtype_out"]], device=dev)
+    return w, A_np, B_np, A_st, B_st, A, B, C
+
+
 def run_ours(args):
-    import numpy as np
     import torch
 
-    import synth
     from hierarchical_gemm_gb300 import tsgemm
 
     rank, world, local = dist_env()
@@ -350,76 +486,25 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = synth.workload(args.workload)
+    off = rank_seed_offset(rank)
+    w, A_np, B_np, A_st, B_st, A, B, C = load_workload(args.workload, dev, off)
     M, N, K = w["M"], w["N"], w["K"]
     din, dout = w["dtype_in"], w["dtype_out"]
     layout = w["layout"]
-    off = rank_seed_offset(rank)
-    A_np = synth.matrix(M, K, w["dist_a"], w["seed_a"] + off, din)
-    B_np = synth.matrix(K, N, w["dist_b"], w["seed_b"] + off, din)
-    A_st, B_st = synth.stored(A_np, B_np, layout)  # as the library is handed them
-    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    A = to_device_bits(A_st, din, dev)
-    B = to_device_bits(B_st, din, dev)
-    C = torch.empty((M, N), dtype=tdt[dout], device=dev)
     force = {k: int(v) for k, v in (kv.split("=") for kv in args.plan.split(",") if kv)}
     plan = tsgemm.Plan(M, N, K, din, dout, layout=layout, **force)
     cfg = plan.config
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Sweep(dev)
     stream = torch.cuda.current_stream(dev)
     flops = 2.0 * M * N * K
+    sampler_gpu = local if (rank == 0 or world > 1) else None
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        plan.run(A, B, C, stream)
-    torch.cuda.synchronize(dev)
-    if plan.status() != 0:
-        raise RuntimeError("device status %d after warm-up" % plan.status())
-
-    sampler = ClockSampler(local) if rank == 0 or world > 1 else None
-    if sampler:
-        sampler.start()
-        time.sleep(0.25)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        plan.run(A, B, C, stream)
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    t_wall1 = time.time()
+    ms_max, clocks = time_plan(plan, A, B, C, args.steps, args.warmup, dev, stream, flush, sampler_gpu, world)
     launches = args.steps
-    if sampler:
-        sampler.mark(t_wall0, t_wall1)
-        clocks = sampler.stop()
-    else:
-        clocks = None
-    st = plan.status()
-    if st != 0:
-        raise RuntimeError("device status %d (%s)" % (st, tsgemm.status_string(st)))
-    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(times) / len(times)
-    ms_max = max_over_ranks(ms, world, dev)
     value = aggregate_tflops(flops, ms_max, world)
 
     # spot check of this run's output against the oracle (sampled outputs)
-    parity = None
-    if rank == 0:
-        import oracle
-        r = np.random.default_rng(7)
-        rows = r.integers(0, M, 1024)
-        cols = r.integers(0, N, 1024)
-        Ch = C.cpu()
-        Ch = Ch.numpy() if dout == "f32" else Ch.view(torch.int16).numpy().view(np.uint16)
-        ref, sabs = oracle.gemm_sampled(A_np, B_np, din, rows, cols)
-        ok, info = oracle.accept(Ch[rows, cols], ref, sabs, dout)
-        parity = {"sampled_outputs": int(rows.size), "ok": bool(ok),
-                  "max_err_over_bound": info.get("max_err_over_bound")}
+    parity = sampled_parity(C, A_np, B_np, w) if rank == 0 else None
 
     # End to end through the C ABI with pinned host buffers.  Every step
     # uploads its A and B from pinned host memory, runs the GEMM and reads C
@@ -431,7 +516,7 @@ def run_ours(args):
         e2e_steps = args.e2e_steps or min(args.steps, 50)
         A_pin = to_device_bits(A_st, din, pin=True)
         B_pin = to_device_bits(B_st, din, pin=True)
-        C_pin = torch.empty((M, N), dtype=tdt[dout]).pin_memory()
+        C_pin = torch.empty((M, N), dtype=C.dtype).pin_memory()
         A_d = [torch.empty_like(A) for _ in range(2)]
         B_d = [torch.empty_like(B) for _ in range(2)]
         C_d = [torch.empty_like(C) for _ in range(2)]
@@ -486,27 +571,43 @@ def run_ours(args):
             raise RuntimeError("device status after the end-to-end loop")
         for pl in plans:
             pl.close()
+        del A_pin, B_pin, C_pin, A_d, B_d, C_d
 
-    peak, peak_desc = bf16_peak(clocks)
-    eight_bit = din in ("e4m3", "e5m2")
-    if eight_bit:
-        peak *= FP8_TO_BF16
-        peak_desc += " x %.0f (nominal fp8 : bf16 dense ratio)" % FP8_TO_BF16
-    algo_bytes = synth.workloads.in_nbytes(din) * (M * K + K * N) + synth.workloads.out_nbytes(dout) * M * N
-    bound, achieved, peak, unit, peak_desc = roofline_point(flops, algo_bytes, ms, peak, peak_desc)
-    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": stored_traffic(w["name"]),
-                "peak_kind": peak_desc,
-                "kernel": "gemm_sm103_%s<BN=%d%s>" % ("2sm" if cfg["block_m"] == 256 else "1sm", cfg["block_n"],
-                                                     ", 8-bit" if eight_bit else ""),
-                "algorithmic_flops_per_launch": flops,
-                "algorithmic_bytes_per_launch": algo_bytes}
+    roofline = gemm_roofline(w, ms_max, clocks, cfg)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, rows, secs, used = oracle_rows_tflops(A_np, B_np, din, args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
                "sample": "rows 0..%d of the %dx%dx%d product (%.1f s)" % (rows - 1, M, N, K, secs)}
+    plan.close()
+    del A, B, C
+
+    # Every other benchmark configuration (and the 8-bit workloads), each
+    # timed the same way over the same number of steps.
+    names = EXTRA_DEFAULT if args.workloads == "all" else \
+        ([] if args.workloads == "none" else [x for x in args.workloads.split(",") if x])
+    workloads = {}
+    for name in names:
+        if name == w["name"]:
+            continue
+        wx, Ax_np, Bx_np, _, _, Ax, Bx, Cx = load_workload(name, dev, off)
+        px = tsgemm.Plan(wx["M"], wx["N"], wx["K"], wx["dtype_in"], wx["dtype_out"], layout=wx["layout"])
+        cx = px.config
+        ms_x, clocks_x = time_plan(px, Ax, Bx, Cx, args.steps, args.warmup, dev, stream, flush, sampler_gpu,
+                                   world)
+        workloads[name] = {
+            "ms_per_step": ms_x, "steps": args.steps, "gpu_launches": args.steps,
+            "value": aggregate_tflops(wx["flops"], ms_x, world), "unit": "TFLOP/s",
+            "config": {"M": wx["M"], "N": wx["N"], "K": wx["K"], "dtype_in": wx["dtype_in"],
+                       "dtype_out": wx["dtype_out"], "layout": wx["layout"],
+                       "plan": {k: cx[k] for k in PLAN_KEYS}},
+            "roofline": gemm_roofline(wx, ms_x, clocks_x, cx),
+            "clocks": clocks_x,
+            "parity": sampled_parity(Cx, Ax_np, Bx_np, wx) if rank == 0 else None,
+        }
+        px.close()
+        del Ax, Bx, Cx, Ax_np, Bx_np
 
     if rank != 0:
         return None
@@ -515,16 +616,15 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": din, "data": "synthetic",
-        "config": {"workload": w["name"], "M": M, "N": N, "K": K, "dtype_in": din, "layout": layout,
-                   "dtype_out": dout, "accumulate": "f32", "l2": "flushed between steps (256 MB write)",
-                   "plan": {k: cfg[k] for k in ("block_m", "block_n", "splits", "stages", "group_m", "grid")},
-                   "parallelism": "independent replica per GPU" if world > 1 else "1 GPU"},
+        "config": gemm_config(w, world),
+        "plan": {k: cfg[k] for k in PLAN_KEYS},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
         "parity": parity,
+        "workloads": workloads,
     }
 
 
@@ -612,11 +712,11 @@ def run_attention(args):
     Q, K, V = to(Qb), to(Kb), to(Vb)
     O = torch.empty_like(Q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Sweep(dev)
     stream = torch.cuda.current_stream(dev)
     scale = D ** -0.5
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         tsgemm.attention(Q, K, V, scale=scale, causal=w["causal"], O=O, status=status, stream=stream)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(local) if rank == 0 or world > 1 else None
@@ -629,7 +729,7 @@ def run_attention(args):
     torch.cuda.synchronize(dev)
     t0 = time.time()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         starts[i].record(stream)
         tsgemm.attention(Q, K, V, scale=scale, causal=w["causal"], O=O, status=status, stream=stream)
         ends[i].record(stream)
@@ -668,7 +768,7 @@ def run_attention(args):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dt, "data": "synthetic",
         "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "Sq": w["Sq"], "Sk": w["Sk"], "D": D,
-                   "causal": w["causal"], "l2": "flushed between steps (256 MB write)",
+                   "causal": w["causal"], "l2": "flushed between steps (read-only sweep of a 256 MB buffer)",
                    "parallelism": "independent replica per GPU" if world > 1 else "1 GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": stored_traffic(w["name"]),

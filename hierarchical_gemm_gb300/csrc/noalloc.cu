@@ -39,7 +39,6 @@ struct DeviceSetup {
     unsigned char* scratch = nullptr;  // device address of g_scratch
     bool cc_ok = false;
     int num_sms = 0;
-    bool attr_set[4][3] = {};          // kernel attribute set, by (block_n / 64 - 1, out kind)
 };
 
 std::mutex g_mu;
@@ -90,8 +89,11 @@ bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
 }
 
 // Per-device set-up, done by the first call on each device with that device
-// current: look up the device address of the scratch array and check the
-// device.  Returns null on failure.
+// current: check the device, look up the device address of the scratch
+// array, and raise the shared-memory limit of every kernel this entry point
+// can launch (the one-SM kernel for 16-bit inputs in the RRR layout, every
+// tile width and output format), so that no later call does one-time
+// work.  Returns null on failure.
 DeviceSetup* setup_device(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
     DeviceSetup& s = g_setup[dev];
@@ -113,6 +115,16 @@ DeviceSetup* setup_device(int dev) {
             return nullptr;
         }
         s.scratch = static_cast<unsigned char*>(ptr);
+        for (int bn = 64; bn <= 256; bn += 64) {
+            for (int out = tsg::kOutF16; out <= tsg::kOutF32; ++out) {
+                const void* kern = tsg::kernel_1sm(bn, out, TSGEMM_LAYOUT_RRR, false, 1);
+                if (!kern || cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(tsg::kSmemPerCtaMax)) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    return nullptr;
+                }
+            }
+        }
     }
     s.done = true;
     return &s;
@@ -178,15 +190,6 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     const int64_t need = tsg::kernel_1sm_smem_bytes(cfg.block_n, out_kind, cfg.stages, 1);
     if (!kern || need > tsg::kSmemPerCtaMax) return TSGEMM_ERR_UNSUPPORTED;
     const int64_t smem = need > tsg::kSmemPerCtaMax / 2 + 1024 ? need : tsg::kSmemPerCtaMax / 2 + 1024;
-    bool& attr = ds->attr_set[cfg.block_n / 64 - 1][out_kind];
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tsg::kSmemPerCtaMax)) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return TSGEMM_ERR_CUDA;
-        }
-        attr = true;
-    }
 
     CUtensorMap tmA;  // the type carries the alignment the encoder requires
     CUtensorMap tmB;

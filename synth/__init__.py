@@ -119,9 +119,23 @@ def matrix(rows, cols, dist, seed, dtype, out=None):
     if out is None:
         out = np.empty((rows, cols), dtype=elem_dtype(dtype))
     flat = out.reshape(-1)
-    for s in range(0, n, _CHUNK):
+
+    def fill(s):
         c = min(_CHUNK, n - s)
         flat[s:s + c] = quantise(_draw(dist, seed, s, c), dtype)
+
+    # Every element depends only on its own counter, so chunks are filled
+    # independently, on several threads for large matrices (numpy releases
+    # the interpreter lock inside these array operations).
+    starts = range(0, n, _CHUNK)
+    if len(starts) <= 1:
+        for s in starts:
+            fill(s)
+    else:
+        import concurrent.futures as cf
+        import os
+        with cf.ThreadPoolExecutor(max_workers=max(1, min(len(starts), os.cpu_count() or 1, 16))) as ex:
+            list(ex.map(fill, starts))
     return out
 
 
