@@ -362,7 +362,7 @@ class L2Sweep:
 
     def __call__(self):
         import torch
-        torch.sum(self.buf, dtype=torch.float32, out=self.sink)
+        torch.sum(self.buf, dim=0, out=self.sink)
 
 
 def time_plan(plan, A, B, C, steps, warmup, dev, stream, flush, sampler_gpu, world):

@@ -32,8 +32,9 @@
 //     of a tile (all tiles, or only those of the last, partial wave);
 //     partial tiles go to an fp32 workspace and are added in split order;
 //   * stream-K: the K slices of the schedule's last tiles are spread evenly
-//     over all CTAs, so every CTA ends at the same time; a tile cut between
-//     CTAs is finished by the CTA that holds its first K slices.
+//     over all CTAs, so every CTA ends at the same time; the partials of a
+//     tile cut between CTAs are added, in K order, by whichever CTA
+//     completes the set (usually the one holding its first K slices).
 //
 // Every wait is bounded in time (see WaitCtl); a CTA that gives up records a
 // timeout in the status word, lets its in-flight copies and MMAs finish,
@@ -91,8 +92,11 @@ struct GemmParams {
     uint32_t idesc;       // tcgen05 instruction descriptor
     uint32_t pad_;
     void* C;
-    float* ws;            // fp32 partials of the split tiles (S > 1)
-    int* counters;        // arrival counters of the split tiles, zero between launches
+    float* ws;            // fp32 partials of the split tiles (S > 1), or of the
+                          // stream-K segments that continue a tile (one per slot)
+    float* ws_own;        // stream-K: the partials of tile owners (one per slot)
+    int* counters;        // arrival counters per split (stream-K) tile half,
+                          // 32-column chunk and lane quarter; zero between launches
     int* status;          // plan status word
     uint64_t timeout_ns;
 };
@@ -101,14 +105,14 @@ struct GemmParams {
 // stream-K segment of a tile.
 struct Unit {
     int tm, tn;      // tile row and column
-    int split;       // K part of this unit (split mode)
-    int nsplit;      // 1: the whole tile; stream-K owner: 1 + contributors
+    int split;       // place of this unit's partial in the tile's part order
+    int nsplit;      // 1: the whole tile; else the tile's parts (S, or a
+                     // stream-K owner and its contributors)
     int kb0, kb1;    // K-slices [kb0, kb1)
     int64_t slot;    // index of the tile among the split (or stream-K) tiles
-    int sk;          // 0: not stream-K; 1: a later K range of a tile, whose
-                     // partial another CTA adds; 2: the tile's first K range,
-                     // whose CTA adds the others' partials and stores C
-    bool last;       // stream-K mode: the slot's last unit (its ring is then idle)
+    int sk;          // 0: not stream-K; 1: a later K range of a tile (a
+                     // contributor); 2: the tile's first K range (its owner,
+                     // part 0)
 };
 
 // Tile row and column of linear tile `tile`: tiles are rastered in groups
@@ -167,22 +171,20 @@ __device__ __forceinline__ int64_t sk_slot_of(const GemmParams& p, int64_t x, in
 // touches, then its last whole tile.  A range that starts inside a tile
 // contributes that tile's later K slices (sk = 1) and is the first
 // segment; one that ends inside a tile holds its first K slices (sk = 2),
-// the last segment, whose CTA adds the others' partials while its tensor
-// cores already work on the last whole tile.  (With no whole tiles the
-// stream-K segments are all there is.)
+// the last segment, which usually finds the others' partials ready and
+// adds them while its tensor cores already work on the last whole tile.
+// (With no whole tiles the stream-K segments are all there is.)
 __device__ __forceinline__ bool unit_at(const GemmParams& p, int64_t g, int64_t G, int64_t j, Unit& r) {
     if (p.sk_tiles == 0) {
         const int64_t u = g + j * G;
         if (u >= p.units) return false;
         r = decode_unit(p, u);
-        r.last = false;
         return true;
     }
     r.split = 0;
     r.nsplit = 1;
     r.slot = -1;
     r.sk = 0;
-    r.last = false;
     const int64_t ndp = g < p.full_tiles ? (p.full_tiles - 1 - g) / G + 1 : 0;
     const int64_t kb = p.kblocks;
     const int64_t a = sk_begin(p, g, G), b = sk_begin(p, g + 1, G);
@@ -193,26 +195,23 @@ __device__ __forceinline__ bool unit_at(const GemmParams& p, int64_t g, int64_t 
         tile_coords(p, g + d * G, r.tm, r.tn);
         r.kb0 = 0;
         r.kb1 = p.kblocks;
-        r.last = d == ndp - 1;
         return true;
     }
     const int64_t jj = j - first_dp;
     if (jj >= nsk) return false;
     const int64_t start = jj == 0 ? a : (a / kb + jj) * kb;
-    r.last = ndp == 0 && jj == nsk - 1;
     const int64_t t = start / kb;
     const int64_t end = min(b, (t + 1) * kb);
     tile_coords(p, p.full_tiles + t, r.tm, r.tn);
     r.kb0 = static_cast<int>(start - t * kb);
     r.kb1 = static_cast<int>(end - t * kb);
-    if (r.kb0 > 0) {
-        r.sk = 1;
+    if (r.kb0 > 0 || r.kb1 < kb) {
+        // the tile is cut between slots g_o (its owner) .. g_l, consecutive
+        const int64_t g_o = sk_slot_of(p, t * kb, G), g_l = sk_slot_of(p, (t + 1) * kb - 1, G);
+        r.sk = r.kb0 > 0 ? 1 : 2;
         r.slot = t;
-        r.nsplit = 2;
-    } else if (r.kb1 < kb) {
-        r.sk = 2;
-        r.slot = t;
-        r.nsplit = 1 + static_cast<int>(sk_slot_of(p, (t + 1) * kb - 1, G) - g);
+        r.split = static_cast<int>(g - g_o);
+        r.nsplit = 1 + static_cast<int>(g_l - g_o);
     }
     return true;
 }
@@ -295,290 +294,170 @@ struct CStager {
 // at `tbase`; this thread holds row `row_local`, and its warp's 32 rows
 // start at row `row0` of C).
 //   * A whole tile is converted and stored to C.
-//   * The S parts of a tile split along K share the reduction: 32-column
-//     chunk j of the tile belongs to part j mod S.  Every part writes the
-//     fp32 partial of the chunks it does not own to the workspace and counts
-//     itself in; once all S have, each part adds, for every chunk it owns,
-//     the S partials in split order (0 + p_0 + p_1 + ... + p_{S-1}, its own
-//     from tensor memory) and stores C.  The bits do not depend on which
-//     part owns a chunk or on timing.  The last part to finish reading
-//     resets the tile's counter.  All S parts wait for each other, so they
-//     must run at the same time on S different CTAs (or pairs): the planner
-//     keeps S within the grid, and since the schedule is static and every
-//     CTA walks its units in order, parts that straddle two rounds still
-//     meet.
-//   * Stream-K: a segment holding a later K range of a tile (sk = 1) writes
-//     its partial to its slot's workspace and counts itself in.  The
-//     segment holding the tile's first K range (sk = 2) waits for the
-//     nsplit - 1 others, adds their partials after its own in K order and
-//     stores C.  When it is its CTA's last unit the operand ring is idle
-//     and, if the partials fit, they are bulk-copied into it and read from
-//     shared memory; otherwise (a whole tile follows, the ring is busy)
-//     they are read from global memory while that tile's mainloop runs.
-// `h` indexes the counter (and, in split mode, the workspace tile) of this
-// 128-row half; `aux` holds the stream-K workspace slots and the ring;
-// `epi_sync` is the epilogue's bounded barrier (both warpgroups) and
-// `release` hands the accumulator back to the MMA issuer.  Returns false if
-// the CTA is aborting.
+//   * A unit that holds part of a tile's K range -- one of the S parts of a
+//     split tile, or a stream-K segment of a tile cut between slots -- adds
+//     its fp32 partial to the others' in a fixed part order (K order):
+//     0 + p_0 + p_1 + ... + p_{n-1}.  Part 0 of a stream-K tile is the
+//     segment holding the tile's first K slices (its owner), parts 1..n-1
+//     the later ranges.  The bits do not depend on which part adds or when.
+//     Each epilogue warp works on its 32 rows one 32-column chunk at a time,
+//     on its own: if the other n - 1 parts have already counted that chunk
+//     in, it adds their partials now; otherwise it writes its partial to the
+//     workspace and counts itself in, and the part whose count completes
+//     the chunk adds.  No part ever waits for another, so the parts need
+//     not run at the same time: a plan stays correct when its CTAs run one
+//     after another (more parts than CTAs, or SMs held by other work).
+// `h` indexes the split (stream-K) tile's 128-row half: its counters and,
+// in split mode, its workspace slots.
 struct EpiAux {
     int64_t wsi;          // stream-K: this slot's workspace index (128 x BN fp32 each)
     int64_t wstride;      // stream-K: workspace index step from one slot to the next
-    uint32_t ring;        // shared-memory operand ring
-    uint32_t ring_bytes;
-    uint32_t red_bar;     // barrier of the bulk copies into the ring
 };
 
-// A stream-K owner segment that is not its CTA's last unit reads its
-// contributors' partials from global memory; one thread asks for them in L2
-// before the segment's own accumulator is ready (the contributors, first
-// segments of their slots, are long done by then).
+// Layout of one 128-row x 32-column fp32 partial chunk in the workspace, in
+// the order the epilogue warps hold it: [4 lane quarters][8 float4][32
+// lanes], so that every warp access is 512 contiguous bytes.
+constexpr int kChunkFloats = 4 * 8 * 128;
+
+// Where part s of the unit's tile keeps the partial of 32-column chunk
+// `chunk`, at this lane's first float of lane quarter q.
+//   split mode: S slots per tile half, [h][part][BN / 32 chunks];
+//   stream-K: part 0 (the owner) in the owner area of its slot, part s >= 1
+//   in the area of its own slot (the slots of a cut tile are consecutive).
+template <int BN>
+__device__ __forceinline__ float* part_chunk(const GemmParams& p, const Unit& un, const EpiAux& aux, int64_t h,
+                                             int s, int chunk, int q, int lane) {
+    const int64_t off = static_cast<int64_t>(chunk) * kChunkFloats + q * (8 * 128) + lane * 4;
+    if (un.sk == 0) return p.ws + ((h * un.nsplit + s) * (BN / 32)) * kChunkFloats + off;
+    const int64_t idx = aux.wsi + static_cast<int64_t>(s - un.split) * aux.wstride;
+    return (s == 0 ? p.ws_own : p.ws) + idx * (kBM * BN) + off;
+}
+
+// Counter of (tile half h, chunk, lane quarter q): how many parts have
+// written that partial; reset to zero by the part that adds.
+template <int BN>
+__device__ __forceinline__ int* part_counter(const GemmParams& p, int64_t h, int chunk, int q) {
+    return p.counters + (h * (BN / 32) + chunk) * 4 + q;
+}
+
+// A stream-K owner segment asks for its contributors' partials in L2 before
+// its own accumulator is ready (the contributors, first segments of their
+// slots, are usually long done by then).
 template <int BN>
 __device__ __forceinline__ void prefetch_sk_partials(const GemmParams& p, const Unit& un, const EpiAux& aux,
                                                      int etid) {
-    if (un.sk != 2 || un.last || etid != 0) return;
-    constexpr uint32_t kChunkBytes = 4u * 8u * 128u * 4u;
+    if (un.sk != 2 || etid != 0) return;
+    constexpr uint32_t kChunkBytes = kChunkFloats * 4u;
     for (int s = 1; s < un.nsplit; ++s)
         for (int c = 0; c < BN; c += 32)
-            bulk_prefetch_l2(p.ws + (aux.wsi + s * aux.wstride) * (kBM * BN) + (c >> 5) * (kChunkBytes / 4),
+            bulk_prefetch_l2(p.ws + (aux.wsi + s * aux.wstride) * (kBM * BN) + (c >> 5) * kChunkFloats,
                              kChunkBytes);
 }
 
-template <int BN, int kOut, class Sync, class Release>
-__device__ __forceinline__ bool drain_sk_owner(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
-                                               const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
-                                               const EpiAux& aux, int c_begin, int etid, volatile int* flag,
-                                               const WaitCtl& ctl, Sync&& epi_sync, Release&& release) {
-    const int col0 = un.tn * BN;
-    const int c_end = c_begin + BN / 2;
-    const int m = un.nsplit - 1;  // contributors, in K order: slots g + 1 .. g + m
+template <int BN, int kOut, class Release>
+__device__ __forceinline__ void drain_parts(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
+                                            const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
+                                            const EpiAux& aux, int c_begin, Release&& release) {
+    const int n = un.nsplit, me = un.split;
     const int q = row_local >> 5, lane = row_local & 31;
-    constexpr int kChunkFloats = 4 * 8 * 128;
-    constexpr uint32_t kHalfBytes = kBM * BN * 4;
-    auto src = [&](int s, int c) -> const float* {  // partial of contributor s (1..m), chunk of column c
-        return p.ws + (aux.wsi + s * aux.wstride) * (kBM * BN) + (c >> 5) * kChunkFloats;
-    };
-    if (etid == 0) *flag = wait_count_bounded(p.counters + h, m, ctl) ? 1 : 0;
-    if (!epi_sync()) return false;
-    if (!*flag) return false;
-    __threadfence();
-    const bool staged = un.last && static_cast<uint32_t>(m) * kHalfBytes <= aux.ring_bytes;
-    if (staged) {
-        // contributor s's partial lands at ring + (s - 1) * kHalfBytes, in
-        // the workspace's order; every thread reads its own 512 bytes of a
-        // chunk as 8 conflict-free 16-byte loads
-        if (etid == 0) {
-            fence_proxy_async_global();
-            mbar_arrive_expect_tx(aux.red_bar, static_cast<uint32_t>(m) * kHalfBytes);
-            for (int s = 1; s <= m; ++s)
-                for (int c = 0; c < BN; c += 32)
-                    bulk_load(aux.ring + (s - 1) * kHalfBytes + (c >> 5) * kChunkFloats * 4, src(s, c),
-                              kChunkFloats * 4, aux.red_bar);
-        }
-        int good = 1;
-        if (lane == 0) good = wait_bounded(aux.red_bar, 0u, ctl) ? 1 : 0;
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) {
-            // let the copies land before the CTA can exit
-            if (lane == 0) wait_bounded(aux.red_bar, 0u, ctl, false);
-            __syncwarp();
-            return false;
-        }
-    }
-#pragma unroll 1
-    for (int c = c_begin; c < c_end; c += 32) {
-        float acc[32];
-        {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c, r);
-            tmem_ld_wait();
-            if (c + 32 >= c_end) release();
-            // the sum starts from a cleared (+0) accumulator
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(0.0f, __uint_as_float(r[j]));
-        }
-#pragma unroll 1
-        for (int s = 1; s <= m; ++s) {
-            float4 v4[8];
-            if (staged) {
-                const uint32_t a = aux.ring + (s - 1) * kHalfBytes + (c >> 5) * kChunkFloats * 4 + q * 4096 + lane * 16;
-#pragma unroll
-                for (int v = 0; v < 8; ++v) v4[v] = ld_shared_f4(a + v * 512);
-            } else {
-                const float* g = src(s, c) + q * (8 * 128) + lane * 4;
-#pragma unroll
-                for (int v = 0; v < 8; ++v) v4[v] = ld_global_cg_f4(g + v * 128);
-            }
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                acc[4 * v] = __fadd_rn(acc[4 * v], v4[v].x);
-                acc[4 * v + 1] = __fadd_rn(acc[4 * v + 1], v4[v].y);
-                acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], v4[v].z);
-                acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], v4[v].w);
-            }
-        }
-        uint32_t r[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
-        out.put(p, tmC, row0, col0 + c, r);
-    }
-    if (!epi_sync()) return false;
-    if (etid == 0) p.counters[h] = 0;  // ready for the next launch
-    return true;
-}
-
-template <int BN, int kOut, class Sync, class Release>
-__device__ __forceinline__ bool drain_unit(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
-                                           const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
-                                           const EpiAux& aux, int c_begin, int etid, volatile int* flag,
-                                           const WaitCtl& ctl, Sync&& epi_sync, Release&& release) {
     const int col0 = un.tn * BN;
-    const int c_end = c_begin + BN / 2;  // this warpgroup's half of the columns
-    if (un.sk == 2)
-        return drain_sk_owner<BN, kOut>(p, tmC, out, un, tbase, row0, row_local, h, aux, c_begin, etid, flag, ctl,
-                                        epi_sync, release);
-    if (un.sk == 1) {
-        // a later K range of a stream-K tile: its partial, for the owner
-        const int q = row_local >> 5, lane = row_local & 31;
-        float* mine = p.ws + aux.wsi * (kBM * BN) + q * (8 * 128) + lane * 4;
+    constexpr int kNc = BN / 64;  // 32-column chunks in this warpgroup's half
+    // Parts start at different chunks, so that (when they run side by side)
+    // each completes, and adds, about 1/n of the chunks, at its end.
+    const int first = me * kNc / n;
 #pragma unroll 1
-        for (int c = c_begin; c < c_end; c += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c, r);
-            tmem_ld_wait();
-            if (c + 32 >= c_end) release();
-            float* dst = mine + (c >> 5) * (4 * 8 * 128);
+    for (int k = 0; k < kNc; ++k) {
+        int cl = first + k;
+        if (cl >= kNc) cl -= kNc;
+        const int c = c_begin + cl * 32;
+        const int chunk = c >> 5;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c, r);
+        tmem_ld_wait();
+        if (k == kNc - 1) release();  // this thread's accumulator part is in registers
+        int* cnt = part_counter<BN>(p, h, chunk, q);
+        int last = 0;
+        if (lane == 0) last = ld_acquire_gpu(cnt) == n - 1 ? 1 : 0;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) {
+            float* dst = part_chunk<BN>(p, un, aux, h, me, chunk, q, lane);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
                 st_global_v4(dst + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+            __threadfence();  // the partial is visible before it is counted
+            __syncwarp();
+            if (lane == 0) last = atom_acq_rel_gpu_add(cnt, 1) == n - 1 ? 1 : 0;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last) continue;
         }
-        __threadfence();  // the partial is visible before it is counted
-        if (!epi_sync()) return false;
-        if (etid == 0) red_release_gpu_add(p.counters + h, 1);
-        return true;
-    }
-    if (un.nsplit == 1) {
+        __threadfence();  // the other parts' partials, counted in, are read after the count
+        // 0 + p_0 + ... + p_{n-1}: the others' partials come two loads ahead
+        // of the add; this part's own term (in registers) at its place
+        auto other = [&](int i) { return i < me ? i : i + 1; };
+        auto fetch = [&](int i, float4 (&dst)[8]) {
+            if (i < n - 1) {
+                const float* src = part_chunk<BN>(p, un, aux, h, other(i), chunk, q, lane);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) dst[v] = ld_global_cg_f4(src + v * 128);
+            }
+        };
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+        auto add_own = [&]() {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(acc[j], __uint_as_float(r[j]));
+        };
+        auto add = [&](const float4 (&src)[8]) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                acc[4 * v] = __fadd_rn(acc[4 * v], src[v].x);
+                acc[4 * v + 1] = __fadd_rn(acc[4 * v + 1], src[v].y);
+                acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], src[v].z);
+                acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], src[v].w);
+            }
+        };
+        float4 pa[8], pb[8];
+        fetch(0, pa);
+        fetch(1, pb);
 #pragma unroll 1
-        for (int c = c_begin; c < c_end; c += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c, r);
-            tmem_ld_wait();
-            if (c + 32 >= c_end) release();  // this thread's accumulator part is in registers
-            out.put(p, tmC, row0, col0 + c, r);
+        for (int i = 0; i < n - 1; i += 2) {
+            if (i == me) add_own();
+            add(pa);
+            fetch(i + 2, pa);
+            if (i + 1 < n - 1) {
+                if (i + 1 == me) add_own();
+                add(pb);
+                fetch(i + 3, pb);
+            }
         }
-        return true;
+        if (me == n - 1) add_own();
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(acc[j]);
+        out.put(p, tmC, row0, col0 + c, w);
+        if (lane == 0) *reinterpret_cast<volatile int*>(cnt) = 0;  // ready for the next launch
     }
-    // Each partial chunk of a 128 x BN half tile is stored in the order the
-    // epilogue warps hold it, so every warp access is 512 contiguous bytes:
-    // [part][BN/32 chunks][4 lane quarters][8 float4][32 lanes].
-    const int S = un.nsplit, me = un.split;
-    const int q = row_local >> 5, lane = row_local & 31;
-    constexpr int kChunks = BN / 32;
-    constexpr int kChunkFloats = 4 * 8 * 128;
-    auto part = [&](int s, int chunk) -> float* {
-        return p.ws + ((h * S + s) * kChunks + chunk) * kChunkFloats + q * (8 * 128) + lane * 4;
-    };
-    auto owned = [&](int c) { return (c >> 5) % S == me; };
-    // 1. the chunks this part does not own go to the workspace
-    int mine = 0;  // chunks of this warpgroup's half that this part owns
+}
+
+template <int BN, int kOut, class Release>
+__device__ __forceinline__ void drain_unit(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
+                                           const Unit& un, uint32_t tbase, int row0, int row_local, int64_t h,
+                                           const EpiAux& aux, int c_begin, Release&& release) {
+    if (un.nsplit > 1) {
+        drain_parts<BN, kOut>(p, tmC, out, un, tbase, row0, row_local, h, aux, c_begin, release);
+        return;
+    }
+    const int col0 = un.tn * BN;
+    const int c_end = c_begin + BN / 2;  // this warpgroup's half of the columns
 #pragma unroll 1
     for (int c = c_begin; c < c_end; c += 32) {
-        if (owned(c)) {
-            ++mine;
-            continue;
-        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c, r);
         tmem_ld_wait();
-        float* dst = part(me, c >> 5);
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-            st_global_v4(dst + v * 128, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        if (c + 32 >= c_end) release();  // this thread's accumulator part is in registers
+        out.put(p, tmC, row0, col0 + c, r);
     }
-    if (mine == 0) release();
-    __threadfence();  // the partials are visible before they are counted
-    if (!epi_sync()) return false;
-    if (etid == 0) {
-        red_release_gpu_add(p.counters + h, 1);
-        *flag = wait_count_bounded(p.counters + h, S, ctl) ? 1 : 0;
-    }
-    if (!epi_sync()) return false;
-    if (!*flag) return false;
-    __threadfence();
-    // 2. the owned chunks: items (owned chunk, part s != me) in order, two
-    // items' loads in flight ahead of the one being added; this part's own
-    // term is read from tensor memory at its place in the order
-    const int nothers = S - 1;
-    const int nitems = mine * nothers;
-    auto item = [&](int i, int& c, int& s) {
-        const int k = i / nothers, j = i - k * nothers;
-        // the k-th owned chunk of [c_begin, c_end): chunks are owned every S
-        const int first = ((c_begin >> 5) + ((me - (c_begin >> 5)) % S + S) % S);
-        c = (first + k * S) << 5;
-        s = j < me ? j : j + 1;
-    };
-    auto fetch = [&](int i, float4 (&dst)[8]) {
-        if (i < nitems) {
-            int c, s;
-            item(i, c, s);
-            const float* src = part(s, c >> 5);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) dst[v] = ld_global_cg_f4(src + v * 128);
-        }
-    };
-    float acc[32];
-    auto add_own = [&](int c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(acc[j], __uint_as_float(r[j]));
-    };
-    int done_chunks = 0;
-    auto consume = [&](int i, const float4 (&src)[8]) {
-        int c, s;
-        item(i, c, s);
-        if (s == (me == 0 ? 1 : 0)) {  // the chunk's first term: the sum starts from +0
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
-            if (me == 0) add_own(c);
-        }
-        if (s == me + 1) {  // this part's term comes right before p_{me+1}
-            if (me != 0) add_own(c);
-        }
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            acc[4 * v] = __fadd_rn(acc[4 * v], src[v].x);
-            acc[4 * v + 1] = __fadd_rn(acc[4 * v + 1], src[v].y);
-            acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], src[v].z);
-            acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], src[v].w);
-        }
-        if (s == S - 1 || (me == S - 1 && s == S - 2)) {  // the chunk's last stored term
-            if (me == S - 1) add_own(c);
-            if (++done_chunks == mine) release();  // every accumulator read of this thread is done
-            uint32_t r[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
-            out.put(p, tmC, row0, col0 + c, r);
-        }
-    };
-    float4 pa[8], pb[8];
-    fetch(0, pa);
-    fetch(1, pb);
-#pragma unroll 1
-    for (int i = 0; i < nitems; i += 2) {
-        consume(i, pa);
-        fetch(i + 2, pa);
-        if (i + 1 < nitems) {
-            consume(i + 1, pb);
-            fetch(i + 3, pb);
-        }
-    }
-    // 3. count this part out; the last of the S resets the counter for the
-    // next launch (2 S counts in all)
-    if (!epi_sync()) return false;
-    if (etid == 0 && atom_acq_rel_gpu_add(p.counters + h, 1) == 2 * S - 1) p.counters[h] = 0;
-    // no thread may still be reading `flag` when the next unit rewrites it
-    return true;
 }
 
 // TMA loads of K-slice kb into a ring slot: A rows [row, row + 128) at
@@ -654,7 +533,7 @@ constexpr uint32_t kCsBytes = kCsBufBytes + 4u * 8u;
 template <int BN, int kOut, bool kCS = false>
 __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
     return 1024u /* alignment slack */ + stages * TileShape<BN>::kStageBytes + epi_smem_bytes<kOut>() +
-           (kCS ? kCsBytes : 0u) + 8u * (2 * stages + 7) /* barriers */ + 16u /* tmem holder, flags */;
+           (kCS ? kCsBytes : 0u) + 8u * (2 * stages + 5) /* barriers */ + 16u /* tmem holder, abort flag */;
 }
 
 // Cluster split (a 2 x 1 cluster of one-SM CTAs per tile): CTA 1 computes
@@ -737,12 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
-    const uint32_t epi_bar = bars + 8u * (2 * S + 5);
-    const uint32_t red_bar = bars + 8u * (2 * S + 6);
-    uint8_t* misc = base_ptr + (bars - base) + 8u * (2 * S + 7);
+    uint8_t* misc = base_ptr + (bars - base) + 8u * (2 * S + 5);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -757,13 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(a), kEpiThreads);
         }
         mbar_init(drain_bar, 1);
-        mbar_init(epi_bar, kEpiWarps);
-        mbar_init(red_bar, 1);
         if constexpr (kCS) {
             for (int w = 0; w < 4; ++w) mbar_init(cs_bars + 8u * w, 128);  // every lane of a warpgroup
         }
         *abort_flag = 0;
-        *last_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -879,23 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         CStager<kOut> out{epi_smem + static_cast<uint32_t>(e) * 2u * epi_buf_bytes<kOut>(), 0u, lane};
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t epi_phase = 0;
-        // Bounded barrier of the four epilogue warps (an mbarrier with one
-        // arrival per warp), so that no epilogue warp can wait forever on a
-        // warp that gave up.
-        auto epi_sync = [&]() -> bool {
-            __syncwarp();
-            int good = 1;
-            if (lane == 0) {
-                mbar_arrive(epi_bar);
-                good = wait_bounded(epi_bar, epi_phase, ctl) ? 1 : 0;
-            }
-            good = __shfl_sync(0xffffffffu, good, 0);
-            epi_phase ^= 1u;
-            return good != 0;
-        };
-        const EpiAux aux{static_cast<int64_t>(blockIdx.x), 1, base, static_cast<uint32_t>(S) * TS::kStageBytes,
-                         red_bar};
+        const EpiAux aux{static_cast<int64_t>(blockIdx.x), 1};
         const int wg = e >> 2;
         const uint32_t cs_mine = cs_buf + static_cast<uint32_t>(wg) * (kCsBufBytes / 2) + static_cast<uint32_t>(q) * 4096u;
         uint32_t cs_phase = 0;
@@ -921,9 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         cs_bars + 8u * wg, cs_bars + 8u * (2 + wg), cs_phase, ctl, release))
                     break;
             } else {
-                if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, aux, c_begin, etid,
-                                          last_flag, ctl, epi_sync, release))
-                    break;
+                drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, un.slot, aux, c_begin, release);
             }
             if (++acc == 2) {
                 acc = 0;

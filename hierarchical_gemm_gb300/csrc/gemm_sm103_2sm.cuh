@@ -42,7 +42,7 @@ struct PairShape {
 
 template <int BN, int kOut>
 __host__ __device__ constexpr uint32_t smem_bytes_2sm(int stages) {
-    return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 7) + 16u;
+    return 1024u + stages * PairShape<BN>::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * stages + 5) + 16u;
 }
 
 template <int BN, int kOut, int kLayout, bool kF8 = false>
@@ -63,12 +63,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * S + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * S + 4);
-    const uint32_t epi_bar = bars + 8u * (2 * S + 5);
-    const uint32_t red_bar = bars + 8u * (2 * S + 6);
-    uint8_t* misc = base_ptr + S * PS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 7);
+    uint8_t* misc = base_ptr + S * PS::kStageBytes + epi_smem_bytes<kOut>() + 8u * (2 * S + 5);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -85,10 +82,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(tempty_bar(a), 2 * kEpiWarps);  // every epilogue warp of the pair
         }
         mbar_init(drain_bar, 1);
-        mbar_init(epi_bar, kEpiWarps);
-        mbar_init(red_bar, 1);
         *abort_flag = 0;
-        *last_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -210,18 +204,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         CStager<kOut> out{epi_smem + static_cast<uint32_t>(e) * 2u * epi_buf_bytes<kOut>(), 0u, lane};
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t epi_phase = 0;
-        auto epi_sync = [&]() -> bool {
-            __syncwarp();
-            int good = 1;
-            if (lane == 0) {
-                mbar_arrive(epi_bar);
-                good = wait_bounded(epi_bar, epi_phase, ctl) ? 1 : 0;
-            }
-            good = __shfl_sync(0xffffffffu, good, 0);
-            epi_phase ^= 1u;
-            return good != 0;
-        };
         // Release accumulator `a` to the leader's MMA issuer.
         auto release_acc = [&](int a) {
             tc_fence_before();
@@ -233,8 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mbar_arrive_cluster(tempty_bar(a), 0u);
             }
         };
-        const EpiAux aux{cluster_id * 2 + half, 2, base,
-                         static_cast<uint32_t>(S) * PS::kStageBytes, red_bar};
+        const EpiAux aux{cluster_id * 2 + half, 2};
         for (int64_t j = 0;; ++j) {
             Unit un;
             if (!unit_at(p, cluster_id, nclusters, j, un)) break;
@@ -251,9 +232,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // workspace tile and counter of this CTA's 128-row half
             const int64_t wh = un.slot * 2 + half;
             const int a_now = acc;
-            if (!drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, wh, aux, c_begin, etid, last_flag,
-                                      ctl, epi_sync, [&]() { release_acc(a_now); }))
-                break;
+            drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, wh, aux, c_begin,
+                                 [&]() { release_acc(a_now); });
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;

@@ -1,8 +1,9 @@
 // noalloc.cu -- the split-K GEMM for callers that cannot allocate device
 // memory (see tsgemm_run_splitk_noalloc in include/tsgemm.h).
 //
-// The split-K kernel needs scratch memory: an fp32 partial tile per split, an
-// arrival counter per output tile and a status word.  tsgemm_plan allocates
+// The split-K kernel needs scratch memory: an fp32 partial tile per split,
+// arrival counters per split tile (one per 32-column chunk and 32-row lane
+// quarter) and a status word.  tsgemm_plan allocates
 // these with cudaMalloc; this entry point instead carves them out of one
 // file-scope device array of fixed size, which every GPU that loads the
 // library holds until the process exits.  Nothing here calls cudaMalloc,
@@ -20,15 +21,17 @@
 namespace {
 
 // Layout of the scratch array:
-//   [0, 256)                 status word (int) when the caller passes none
-//   [256, 256 + 4 * tiles)   per-tile arrival counters
-//   [kWsOffset, end)         fp32 split-K partials
+//   [0, 256)                       status word (int) when the caller passes none
+//   [256, 256 + 128 * max tiles)   arrival counters, 32 per split tile at most
+//                                  (block_n / 32 chunks x 4 lane quarters)
+//   [kWsOffset, end)               fp32 split-K partials
 constexpr size_t kScratchBytes = TSGEMM_NOALLOC_SCRATCH_BYTES;
 constexpr size_t kCounterOffset = 256;
 constexpr size_t kMaxTiles = TSGEMM_NOALLOC_MAX_TILES;
-static_assert(TSGEMM_NOALLOC_SCRATCH_BYTES - (256 + ((TSGEMM_NOALLOC_MAX_TILES * 4 + 255) / 256) * 256) >= TSGEMM_NOALLOC_WS_BYTES, "workspace capacity");
-constexpr size_t kWsOffset = kCounterOffset + ((kMaxTiles * sizeof(int) + 255) / 256) * 256;
-static_assert(kWsOffset < kScratchBytes, "scratch layout");
+constexpr size_t kCountersPerTile = 32;
+constexpr size_t kWsOffset = kCounterOffset + kMaxTiles * kCountersPerTile * sizeof(int);
+static_assert(kWsOffset % 256 == 0, "scratch layout");
+static_assert(kScratchBytes - kWsOffset >= TSGEMM_NOALLOC_WS_BYTES, "workspace capacity");
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -235,9 +238,11 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     int* own_status = reinterpret_cast<int*>(ds->scratch);
     float* ws = reinterpret_cast<float*>(ds->scratch + kWsOffset);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The array keeps the previous call's contents: the tile counters (and
-    // the status word this call reports into) must start at zero.
-    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(tiles) * sizeof(int), s) != cudaSuccess ||
+    // The array keeps the previous call's contents: the split tiles'
+    // counters (and the status word this call reports into) must start at
+    // zero.
+    const size_t ncounters = static_cast<size_t>(cfg.split_tiles) * (cfg.block_n / 32) * 4;
+    if ((ncounters > 0 && cudaMemsetAsync(counters, 0, ncounters * sizeof(int), s) != cudaSuccess) ||
         cudaMemsetAsync(status ? status : own_status, 0, sizeof(int), s) != cudaSuccess) {
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;
@@ -259,6 +264,7 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     gp.idesc = idesc_for(dtype_in, cfg.block_n);
     gp.C = C;
     gp.ws = ws;
+    gp.ws_own = nullptr;  // (stream-K only)
     gp.counters = counters;
     gp.status = status ? status : own_status;
     gp.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms) * 1000000ull;

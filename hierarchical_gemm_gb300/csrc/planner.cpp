@@ -43,7 +43,6 @@ constexpr double kFixupCycles = 11000.0;      // stream-K: segment hand-overs an
 // part that tile's mainloop hides, but at least kHiddenFixupCycles
 constexpr double kMidFixupCycles = 27000.0;
 constexpr double kHiddenFixupCycles = 1500.0;
-constexpr double kStagedBytesPerCycle = 64.0; // stream-K: partials bulk-copied into the idle ring
 constexpr int kMaxSplits = 32;
 constexpr int kDefaultTimeoutMs = 1000;
 
@@ -118,8 +117,7 @@ Estimate estimate(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, in
 // run before the last of ceil((tiles - sk) / slots) rounds of whole tiles.
 // A tile cut between slots costs its later parts a partial write and its
 // first part's CTA the final add, both hidden behind the next mainloop;
-// with no whole tiles the add comes at the very end, after a copy of the
-// partials into the idle ring.
+// with no whole tiles the add comes at the very end.
 Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm, int bn, int64_t sk,
                      int num_sms) {
     const int64_t tiles = ceil_div(M, bm) * ceil_div(N, bn);
@@ -131,21 +129,17 @@ Estimate estimate_sk(int64_t M, int64_t N, int64_t K, int din, int dout, int bm,
     const double per_kb = std::max(mma, load);
     const double dp_rounds = static_cast<double>(ceil_div(tiles - sk, slots));
     const double sk_slices = std::ceil(static_cast<double>(sk) * kblocks / slots);
-    // contributors per owner; their partials fit the idle ring when each
-    // is no larger than the ring's share, else they are read from global
+    // contributors per owner, whose partials the owner reads from global
     // memory at the split-K rate
     const double owners_parts = std::ceil(kblocks / std::max(1.0, sk_slices));
     const double half_bytes = kBM * bn * 4.0;
-    const double ring_bytes = static_cast<double>(max_stages_for(bm, bn, dout)) *
-                              (kBM * kBK * 2.0 + (bm == 256 ? bn / 2 : bn) * kBK * 2.0);
-    const double fetch = owners_parts * half_bytes <= ring_bytes ? owners_parts * half_bytes / kStagedBytesPerCycle
-                                                                 : owners_parts * half_bytes / kReduceBytesPerCycle;
+    const double fetch = owners_parts * half_bytes / kReduceBytesPerCycle;
     const double tail = dp_rounds >= 1 ? std::max(kHiddenFixupCycles, kMidFixupCycles - kblocks * per_kb)
                                        : kFixupCycles + fetch;
     double compute = dp_rounds * (kblocks * per_kb + kUnitOverhead) + sk_slices * per_kb + 2 * kUnitOverhead + tail;
     double bytes = static_cast<double>(in_bytes(din)) * (M * K + K * N) +
                    static_cast<double>(out_bytes(dout)) * M * N +
-                   2.0 * 4.0 * static_cast<double>(slots) * bm * bn;
+                   3.0 * 4.0 * static_cast<double>(slots) * bm * bn;
     const double hbm = bytes / kHbmBytesPerCycle;
     return {std::max(compute, hbm) + 0.05 * compute, compute};
 }
@@ -161,7 +155,7 @@ int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages, int 
     // cluster split: a 128 x 32 fp32 exchange chunk per epilogue warpgroup
     // and four barriers
     const int64_t exchange = cluster_split == 2 ? 2 * 128 * 32 * 4 + 4 * 8 : 0;
-    return 1024 + stages * stage + staging + exchange + 8 * (2 * stages + 7) + 16;
+    return 1024 + stages * stage + staging + exchange + 8 * (2 * stages + 5) + 16;
 }
 
 int max_stages_for(int block_m, int block_n, int dtype_out, int cluster_split) {
@@ -365,17 +359,18 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
         }
         c.units = tiles - best_sk + segs;
         c.grid = static_cast<int32_t>(slots * ctas_per_slot);
-        // one fp32 partial slot per CTA half of each slot
-        c.workspace_bytes = slots * best_bm * static_cast<int64_t>(best_bn) * 4;
+        // two fp32 partial slots per CTA half of each slot: one for the
+        // segment that continues a tile, one for the owner of a tile (which
+        // writes its partial when a contributor is still to come)
+        c.workspace_bytes = 2 * slots * best_bm * static_cast<int64_t>(best_bn) * 4;
         c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
         c.debug_flags = f.debug_flags;
         *out = c;
         return TSGEMM_OK;
     }
+    // (the parts of a split tile never wait for one another, so S may
+    // exceed the grid's slots: the parts then run one after another)
     c.grid = static_cast<int32_t>(std::min<int64_t>(c.units, slots) * ctas_per_slot);
-    // part 0 of a split tile waits for parts 1..S-1, which must run on other
-    // CTAs (pairs) at the same time: S may not exceed the grid's slots
-    if (c.split_tiles > 0 && best_s > c.grid / ctas_per_slot) return TSGEMM_ERR_UNSUPPORTED;
     // S fp32 partial slots per split tile; each part fills the chunks it
     // does not own
     c.workspace_bytes = c.split_tiles * best_s * best_bm * static_cast<int64_t>(best_bn) * 4;

@@ -181,9 +181,9 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
             (void)cudaGetLastError();
             return TSGEMM_ERR_UNSUPPORTED;
         }
+        // (a smaller grid only makes each slot's stream-K range longer; the
+        // workspace sized for the larger one still covers it)
         if (cfg.grid > per_cluster * clusters) cfg.grid = per_cluster * clusters;
-        // the parts of a split unit must still run side by side
-        if (cfg.split_tiles > 0 && cfg.splits > cfg.grid / per_cluster) return TSGEMM_ERR_UNSUPPORTED;
     }
 
     // value-initialised; operator new honours the 64-byte alignment the
@@ -200,9 +200,10 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     p->device = dev;
     p->kernel = kern;
     p->smem = smem;
-    // split-K (stream-K) counters: one per 128-row half of each tile of a
-    // split (stream-K) unit (pairs reduce halves)
-    p->num_tiles = (cfg.stream_k_tiles > 0 ? cfg.stream_k_tiles : cfg.split_tiles) * (cfg.block_m / 128);
+    // split-K (stream-K) counters: per 128-row half of each split (stream-K)
+    // tile (pairs reduce halves), one per 32-column chunk and lane quarter
+    p->num_tiles = (cfg.stream_k_tiles > 0 ? cfg.stream_k_tiles : cfg.split_tiles) * (cfg.block_m / 128) *
+                   (cfg.block_n / 32) * 4;
 
     if (cudaMalloc(&p->status_d, sizeof(int)) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -246,6 +247,10 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n, layout);
     gp.C = nullptr;
     gp.ws = p->ws;
+    // stream-K: the owners' partials follow the contributors' (one 128 x
+    // block_n fp32 slot per CTA each)
+    gp.ws_own = (cfg.stream_k_tiles > 0 && p->ws) ? p->ws + static_cast<int64_t>(cfg.grid) * 128 * cfg.block_n
+                                                  : nullptr;
     gp.counters = p->counters;
     gp.status = p->status_d;
     gp.timeout_ns = static_cast<uint64_t>(cfg.timeout_ms) * 1000000ull;

@@ -142,9 +142,10 @@ TSGEMM_API tsgemm_status_t tsgemm_plan(tsgemm_plan_t* out, int64_t M, int64_t N,
 
 /* tsgemm_plan with some configuration fields forced (see tsgemm_config_t).
  * `force` may be NULL.  A forced value the kernel cannot run returns
- * TSGEMM_ERR_UNSUPPORTED; that includes a split factor larger than the number
- * of CTAs (CTA pairs) of the grid, since the parts of a split tile must run
- * side by side. */
+ * TSGEMM_ERR_UNSUPPORTED.  The parts of a split (or stream-K) tile never
+ * wait for one another: whichever part completes a chunk's set of partials
+ * adds them, so any split factor runs on any grid, and a run stays correct
+ * when some of its CTAs must wait for SMs held by other work. */
 TSGEMM_API tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t K,
                                tsgemm_dtype_t dtype_in, tsgemm_dtype_t dtype_out,
                                tsgemm_layout_t layout, const tsgemm_config_t* force);
@@ -194,7 +195,7 @@ TSGEMM_API const char* tsgemm_status_string(tsgemm_status_t s);
  * real-time loops that forbid cudaMalloc/cudaFree after start-up because
  * those calls can synchronise the whole device.  This entry point needs no
  * plan: the split-K scratch lives in one fixed device array inside the
- * library (TSGEMM_NOALLOC_SCRATCH_BYTES, about 32 MiB), which every GPU that
+ * library (TSGEMM_NOALLOC_SCRATCH_BYTES, about 34 MiB), which every GPU that
  * loads the library holds until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
  *
@@ -223,7 +224,8 @@ TSGEMM_API const char* tsgemm_status_string(tsgemm_status_t s);
  * capture.  Asynchronous otherwise: returns after the launch. */
 #define TSGEMM_NOALLOC_MAX_TILES 16384
 #define TSGEMM_NOALLOC_WS_BYTES (32u << 20)
-#define TSGEMM_NOALLOC_SCRATCH_BYTES (256u + TSGEMM_NOALLOC_MAX_TILES * 4u + TSGEMM_NOALLOC_WS_BYTES)
+/* status word, 32 counters per tile at most, the fp32 partials */
+#define TSGEMM_NOALLOC_SCRATCH_BYTES (256u + TSGEMM_NOALLOC_MAX_TILES * 128u + TSGEMM_NOALLOC_WS_BYTES)
 
 TSGEMM_API tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64_t K,
                                                      tsgemm_dtype_t dtype_in,
