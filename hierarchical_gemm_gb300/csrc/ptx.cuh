@@ -233,6 +233,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Hint: bring the 2-D box at (c0 = inner, c1 = outer) of the tensor into L2
+// (no shared memory, no completion to wait for).  Same coordinate rules as
+// the tiled load.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(m), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // 3-D tiled load of the box at (c0 = inner, c1, c2 = outer) into shared
 // memory, completing its bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,

@@ -47,7 +47,7 @@ class Config(ctypes.Structure):
                 ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("timeout_ms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
                 ("split_tiles", ctypes.c_int64), ("stream_k_tiles", ctypes.c_int64),
-                ("cluster_split", ctypes.c_int32)]
+                ("cluster_split", ctypes.c_int32), ("prefetch", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
