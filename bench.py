@@ -779,9 +779,153 @@ def run_attention(args):
     }
 
 
+# ----------------------------------------------------------- MLA decode --
+
+MLA_METRIC = "MLA decode HBM GB/s (Q, KV caches read once, O written once)"
+
+
+def mla_oracle_sample(w, bits, batch=0, heads=32):
+    """The oracle on the first `heads` heads of one batch."""
+    import oracle
+    q, qpe, kv, kpe = bits
+    sel = (q[batch:batch + 1, :heads], qpe[batch:batch + 1, :heads], kv[batch:batch + 1], kpe[batch:batch + 1])
+    return oracle.mla_decode(*sel, w["dtype"], w["scale"])
+
+
+def mla_sample_bytes(w, heads=32):
+    """Algorithmic bytes of the oracle sample: one batch's caches, `heads`
+    heads of its queries and outputs."""
+    return 2 * (w["Skv"] * (w["dim"] + w["pe_dim"]) + heads * (w["dim"] + w["pe_dim"] + w["dim"]))
+
+
+def run_mla_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import synth
+    w = synth.mla_workload(args.workload)
+    bits = synth.mla_inputs(w)
+    for _ in range(args.warmup):
+        mla_oracle_sample(w, bits)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        mla_oracle_sample(w, bits)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = mla_sample_bytes(w) / dt / 1e9
+    cfg = {"workload": w["name"], "B": w["B"], "H": w["H"], "Skv": w["Skv"], "dim": w["dim"],
+           "pe_dim": w["pe_dim"], "l2": "flushed between steps (read-only sweep of a 256 MB buffer)",
+           "parallelism": "1 GPU"}
+    return {
+        "impl": "reference", "metric": MLA_METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "32 heads of batch 0 against its whole cache per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def run_mla(args):
+    import torch
+
+    import oracle
+    import synth
+    from hierarchical_gemm_gb300 import tsgemm
+
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = synth.mla_workload(args.workload)
+    bits = synth.mla_inputs(w, rank_seed_offset(rank))
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w["dtype"]]
+    to = lambda x: torch.from_numpy(x.reshape(-1).view(np.int16)).to(dev).view(tdt).reshape(x.shape)  # noqa: E731
+    q, qpe, kv, kpe = (to(x) for x in bits)
+    O = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = L2Sweep(dev)
+    stream = torch.cuda.current_stream(dev)
+    force = {k: int(v) for k, v in (kv_.split("=") for kv_ in args.plan.split(",") if kv_)}
+    pf = force.get("prefetch_blocks", 0)
+
+    def launch():
+        tsgemm.mla_decode(q, qpe, kv, kpe, scale=w["scale"], O=O, status=status, stream=stream,
+                          prefetch_blocks=pf)
+    for _ in range(args.warmup):
+        flush()
+        launch()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local) if rank == 0 or world > 1 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(args.steps):
+        flush()
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t1 = time.time()
+    clocks = None
+    if sampler:
+        sampler.mark(t0, t1)
+        clocks = sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError("MLA decode device status %d" % int(status.item()))
+    ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends)) / args.steps
+    ms_max = max_over_ranks(ms, world, dev)
+    value = world * w["bytes"] / (ms_max * 1e-3) / 1e9
+    parity = None
+    if rank == 0:
+        ref, bound = mla_oracle_sample(w, bits)
+        got = O[:1, :32].cpu().reshape(-1).view(torch.int16).numpy().view(np.uint16).reshape(ref.shape)
+        ok, info = oracle.accept_attention(got, ref, bound, w["dtype"])
+        parity = {"sampled_outputs": int(ref.size), "ok": bool(ok),
+                  "max_err_over_bound": info.get("max_err_over_bound")}
+    peaks, kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    tensor_peak, tensor_desc = bf16_peak(clocks)
+    achieved = w["bytes"] / (ms * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t_c = time.perf_counter()
+        mla_oracle_sample(w, bits)
+        dt_c = time.perf_counter() - t_c
+        cpu = {"value": mla_sample_bytes(w) / dt_c / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "32 heads of batch 0 against its whole cache (%.2f s)" % dt_c}
+    if rank != 0:
+        return None
+    return {
+        "metric": MLA_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "Skv": w["Skv"], "dim": w["dim"],
+                   "pe_dim": w["pe_dim"], "l2": "flushed between steps (read-only sweep of a 256 MB buffer)",
+                   "parallelism": "independent replica per GPU" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": stored_traffic(w["name"]), "peak_kind": kind + " HBM copy bandwidth",
+                     "kernel": "mla_decode_sm103", "algorithmic_bytes_per_launch": w["bytes"],
+                     "algorithmic_flops_per_launch": w["flops"],
+                     "tensor_tflops": w["flops"] / (ms * 1e-3) / 1e12, "tensor_peak": tensor_peak,
+                     "tensor_peak_kind": tensor_desc},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clocks, "parity": parity,
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.workload.startswith("attn_"):
+    if args.workload.startswith("mla_"):
+        out = run_mla_reference(args) if args.impl == "reference" else run_mla(args)
+    elif args.workload.startswith("attn_"):
         out = run_attention_reference(args) if args.impl == "reference" else run_attention(args)
     else:
         out = run_reference(args) if args.impl == "reference" else run_ours(args)

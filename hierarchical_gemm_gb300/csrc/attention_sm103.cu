@@ -46,6 +46,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "attn_common.h"
 #include "ptx.cuh"
 #include "tsattn.h"
 
@@ -154,56 +155,39 @@ __device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar
         }
         tc_fence_after();
         uint32_t s[128];
-        auto ld_half = [&](int h) {
 #pragma unroll
-            for (int c = 2 * h; c < 2 * h + 2; ++c) {
-                uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c);
-                tmem_ld_32x32b_x32(trow + scol + 32u * c, part);
-            }
-        };
+        for (int c = 0; c < 4; ++c) {
+            uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c);
+            tmem_ld_32x32b_x32(trow + scol + 32u * c, part);
+        }
+        tmem_ld_wait();
         // keys past Sk or past the causal limit weigh nothing
         const int k0 = j * kBKV;
-        const bool ragged = !(k0 + kBKV - 1 <= kv_last && k0 + kBKV <= p.Sk);
-        auto mask_half = [&](int h) {
-            if (ragged) {
+        if (!(k0 + kBKV - 1 <= kv_last && k0 + kBKV <= p.Sk)) {
 #pragma unroll
-                for (int c = 64 * h; c < 64 * h + 64; ++c)
-                    if (k0 + c > kv_last || k0 + c >= p.Sk) s[c] = __float_as_uint(-INFINITY);
-            }
-        };
-        // p = 2^(c2 s - m) for the 64 keys of half h against the current
-        // maximum: one fused multiply-add per weight, two weights per packed
-        // instruction (before any visible key, m = +inf makes every weight
-        // 0); the half's weights go to the 32 score-buffer columns 32 h ..
-        // 32 h + 31, two per column, and into eight partial sums; `smax`
-        // collects the half's largest raw score.
-        float2 rsum[4];  // eight independent partial sums, added in a fixed order
-        auto weights_half = [&](int h, float& smax) {
-            const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
-            const float2 c22 = make_float2(c2, c2), mn2 = make_float2(mneg, mneg);
-            float mx[4];
+            for (int c = 0; c < 128; ++c)
+                if (k0 + c > kv_last || k0 + c >= p.Sk) s[c] = __float_as_uint(-INFINITY);
+        }
+        // row maximum: eight independent chains of three-input maxima, then
+        // a tree
+        float mx[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mx[i] = smax;
-            uint32_t w[32];
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = 64 * h + 2 * i;
-                const float a = __uint_as_float(s[c]), b = __uint_as_float(s[c + 1]);
-                asm("max.f32 %0, %1, %2, %3;" : "=f"(mx[i & 3]) : "f"(mx[i & 3]), "f"(a), "f"(b));
-                const float2 x = fma2(make_float2(a, b), c22, mn2);
-                const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                rsum[i & 3] = add2(rsum[i & 3], pw);
-                w[i] = kF16 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
-            }
-            smax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            tmem_st_32x32b_x32(trow + scol + 32u * h, w);
-        };
-        // Move every lane of the warp to its own new maximum (scaled `smax`
-        // of the block): rescale its row sum and, after the first block,
-        // its row of the output accumulator, which holds P_0 V_0 + ... +
-        // P_{j-1} V_{j-1}, complete (see above).
-        auto rescale = [&](float smax) {
-            const float m_new = fmaxf(m_used, smax * c2);  // (c2 > 0)
+        for (int c = 8; c < 128; c += 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                asm("max.f32 %0, %1, %2, %3;"
+                    : "=f"(mx[i])
+                    : "f"(mx[i]), "f"(__uint_as_float(s[c + i])), "f"(__uint_as_float(s[c + 8 + i])));
+        }
+        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_new = fmaxf(m_used, mb * c2);  // (c2 > 0)
+        const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+            // every lane of the warp moves to its own new maximum; O holds
+            // P_0 V_0 + ... + P_{j-1} V_{j-1}, complete (see above)
             const float alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m_new);
             if (m_new > -INFINITY) m_used = m_new;
             l *= alpha;
@@ -224,61 +208,28 @@ __device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar
                 }
                 tmem_st_wait();
             }
-        };
-        auto need_rescale = [&](float smax) {
-            const float m_new = fmaxf(m_used, smax * c2);
-            return m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
-        };
+        }
+        // p = 2^(c2 s - m): one fused multiply-add per weight, two weights
+        // per packed instruction; before any visible key, m = +inf makes
+        // every weight 0.  P_j goes back into the first 64 columns of the
+        // score buffer, two weights per column, 32 columns at a time.
+        const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
+        const float2 c22 = make_float2(c2, c2), mn2 = make_float2(mneg, mneg);
+        float2 rsum[4];  // eight independent partial sums, added in a fixed order
 #pragma unroll
         for (int i = 0; i < 4; ++i) rsum[i] = make_float2(0.0f, 0.0f);
-        ld_half(0);
-        tmem_ld_wait();
-        if (__all_sync(0xffffffffu, m_used != -INFINITY)) {
-            // The usual case: weights against the maximum already in use,
-            // the row's second half loading meanwhile; only if a score has
-            // outgrown that maximum by more than the lazy-rescale threshold
-            // are the weights taken again against the new one.
-            ld_half(1);
-            mask_half(0);
-            float smax = -INFINITY;
-            weights_half(0, smax);
-            tmem_ld_wait();
-            mask_half(1);
-            weights_half(1, smax);
-            if (__any_sync(0xffffffffu, need_rescale(smax))) {
-                tmem_st_wait();  // the first weights are written before they are replaced
-                rescale(smax);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) rsum[i] = make_float2(0.0f, 0.0f);
-                float unused = -INFINITY;
-                weights_half(0, unused);
-                weights_half(1, unused);
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = 64 * h + 2 * i;
+                const float2 x = fma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c22, mn2);
+                const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                rsum[i & 3] = add2(rsum[i & 3], pw);
+                w[i] = kF16 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
             }
-        } else {
-            // A lane has seen no key yet: its maximum comes first.
-            ld_half(1);
-            tmem_ld_wait();
-            mask_half(0);
-            mask_half(1);
-            // row maximum: eight independent chains of three-input maxima,
-            // then a tree
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
-#pragma unroll
-            for (int c = 8; c < 128; c += 16) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    asm("max.f32 %0, %1, %2, %3;"
-                        : "=f"(mx[i])
-                        : "f"(mx[i]), "f"(__uint_as_float(s[c + i])), "f"(__uint_as_float(s[c + 8 + i])));
-            }
-            const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            if (__any_sync(0xffffffffu, need_rescale(mb))) rescale(mb);
-            float unused = -INFINITY;
-            weights_half(0, unused);
-            weights_half(1, unused);
+            tmem_st_32x32b_x32(trow + scol + 32u * h, w);
         }
         l += ((rsum[0].x + rsum[0].y) + (rsum[1].x + rsum[1].y)) + ((rsum[2].x + rsum[2].y) + (rsum[3].x + rsum[3].y));
         tmem_st_wait();
@@ -528,7 +479,8 @@ EncodeTiledFn encode_fn() {
 }
 
 // The library's status word (one per device that loads the library), used
-// when the caller passes no status pointer.
+// when the caller passes no status pointer; the attention block and the MLA
+// decode kernel share it.
 __device__ int g_attn_status;
 
 struct DeviceState {
@@ -539,6 +491,28 @@ struct DeviceState {
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+
+// Device address of the status word on device `dev` (current), looked up
+// once per device; null on failure.  Call with g_mu held.
+int* status_word_locked(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceState& ds = g_dev[dev];
+    if (!ds.ready) {
+        void* sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_attn_status) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        ds.status = static_cast<int*>(sym);
+        ds.ready = true;
+    }
+    return ds.status;
+}
+
+int* library_status_word(int dev) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return status_word_locked(dev);
+}
 
 }  // namespace attn
 }  // namespace tsg
@@ -584,15 +558,7 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     {
         std::lock_guard<std::mutex> lock(g_mu);
         DeviceState& ds = g_dev[dev];
-        if (!ds.ready) {
-            void* sym = nullptr;
-            if (cudaGetSymbolAddress(&sym, g_attn_status) != cudaSuccess) {
-                (void)cudaGetLastError();
-                return TSGEMM_ERR_CUDA;
-            }
-            ds.status = static_cast<int*>(sym);
-            ds.ready = true;
-        }
+        if (!status_word_locked(dev)) return TSGEMM_ERR_CUDA;
         if (!ds.attr[f16 ? 1 : 0]) {
             // the warpgroups' register split must fit in what the CTA is
             // launched with, or the softmax warps would wait for registers

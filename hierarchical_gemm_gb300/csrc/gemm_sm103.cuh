@@ -84,13 +84,13 @@ struct GemmParams {
     int32_t kblocks;      // ceil(K / K-elements per slice)
     int32_t group_m;      // raster group height in tiles
     int32_t stages;
-    int32_t prefetch;     // L2 prefetch distance in K slices (0: none)
     int32_t debug_flags;
     int64_t full_tiles;   // tiles [0, full_tiles) of the schedule are not split
     int64_t units;        // full_tiles + (tiles - full_tiles) * S (split mode)
     int64_t sk_tiles;     // stream-K mode: the last sk_tiles tiles (0: split mode)
     int64_t sk_work;      // sk_tiles * kblocks K slices, spread over the slots
     uint32_t idesc;       // tcgen05 instruction descriptor
+    uint32_t pad_;
     void* C;
     float* ws;            // fp32 partials of the split tiles (S > 1), or of the
                           // stream-K segments that continue a tile (one per slot)
@@ -490,44 +490,6 @@ __device__ __forceinline__ void load_slice(uint32_t a_dst, uint32_t b_dst, const
     }
 }
 
-// L2 prefetch of the boxes load_slice would load for K-slice kb (the same
-// coordinates), issued some slices ahead of the load so that the operands a
-// tile's first pass reads from HBM are already in L2 when the ring asks.
-template <int kLayout, int kBCols, bool kF8 = false>
-__device__ __forceinline__ void prefetch_slice(const CUtensorMap* tmA, const CUtensorMap* tmB, int kb, int32_t row,
-                                               int32_t col) {
-    constexpr int kSK = slice_k<kF8>();
-    if constexpr (a_kmajor(kLayout)) {
-        tma_prefetch_2d(tmA, kb * kSK, row);
-    } else {
-        tma_prefetch_2d(tmA, row, kb * kBK);
-        tma_prefetch_2d(tmA, row + 64, kb * kBK);
-    }
-    if constexpr (b_kmajor(kLayout)) {
-        tma_prefetch_2d(tmB, kb * kSK, col);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBCols / 64; ++j) tma_prefetch_2d(tmB, col + j * 64, kb * kBK);
-    }
-}
-
-// Position `ahead` K-slices past slice kb of unit j in a slot's sequence of
-// units (which is what the producer loads next): false past the slot's
-// last unit.  `next` caches unit j + 1.
-__device__ __forceinline__ bool slice_ahead(const Unit& un, const Unit& next, bool has_next, int kb, int ahead,
-                                            const Unit*& at, int& at_kb) {
-    if (kb + ahead < un.kb1) {
-        at = &un;
-        at_kb = kb + ahead;
-        return true;
-    }
-    const int rest = kb + ahead - un.kb1;
-    if (!has_next || next.kb0 + rest >= next.kb1) return false;
-    at = &next;
-    at_kb = next.kb0 + rest;
-    return true;
-}
-
 // The four MMAs of one K-slice held at a_addr / b_addr: 16-deep kind::f16
 // steps, or 32-deep kind::f8f6f4 steps for 8-bit operands (32 bytes of a
 // K-major row either way, so the descriptor steps are the same).
@@ -710,21 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t outstanding = 0, out_parity = 0;  // loads issued, per slot
             bool skip = (p.debug_flags & 1) && blockIdx.x == 0;
             bool ok = true;
-            Unit un, nxt;
-            bool have = next_unit(0, un);
-            for (int64_t j = 0; ok && have; ++j) {
-                const bool has_next = next_unit(j + 1, nxt);
-                auto prefetch_ahead = [&](int kb, int ahead) {
-                    const Unit* at;
-                    int akb;
-                    if (slice_ahead(un, nxt, has_next, kb, ahead, at, akb))
-                        prefetch_slice<kLayout, BN, kF8>(&tmA, &tmB, akb, at->tm * kBM, at->tn * BN);
-                };
-                // the slot's first unit: the slices past the ring's first fill
-                if (j == 0)
-                    for (int d = S; d < p.prefetch; ++d) prefetch_ahead(un.kb0, d);
+            for (int64_t j = 0; ok; ++j) {
+                Unit un;
+                if (!next_unit(j, un)) break;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
-                    if (p.prefetch > 0) prefetch_ahead(kb, p.prefetch);
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, ctl)) {
                         ok = false;
                         break;
@@ -744,8 +695,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
-                un = nxt;
-                have = has_next;
             }
             // Let every copy this thread started land before the CTA exits.
             for (int s = 0; s < S; ++s)

@@ -111,23 +111,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // unannounced, so the MMA issuer's bounded wait runs out
             bool skip = (p.debug_flags & 1) && cluster_id == 0 && leader;
             bool ok = true;
-            Unit un, nxt;
-            bool have = unit_at(p, cluster_id, nclusters, 0, un);
-            for (int64_t j = 0; ok && have; ++j) {
-                const bool has_next = unit_at(p, cluster_id, nclusters, j + 1, nxt);
-                // L2 prefetch of this CTA's boxes `ahead` slices past kb
-                auto prefetch_ahead = [&](int kb, int ahead) {
-                    const Unit* at;
-                    int akb;
-                    if (slice_ahead(un, nxt, has_next, kb, ahead, at, akb))
-                        prefetch_slice<kLayout, PS::kBCols, kF8>(
-                            &tmA, &tmB, akb, at->tm * (2 * kBM) + static_cast<int32_t>(half) * kBM,
-                            at->tn * BN + static_cast<int32_t>(half) * PS::kBCols);
-                };
-                if (j == 0)
-                    for (int d = S; d < p.prefetch; ++d) prefetch_ahead(un.kb0, d);
+            for (int64_t j = 0; ok; ++j) {
+                Unit un;
+                if (!unit_at(p, cluster_id, nclusters, j, un)) break;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
-                    if (p.prefetch > 0) prefetch_ahead(kb, p.prefetch);
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, ctl)) {
                         ok = false;
                         break;
@@ -155,8 +142,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
-                un = nxt;
-                have = has_next;
             }
             for (int s = 0; s < S; ++s) {
                 if (!(outstanding & (1u << s))) continue;

@@ -258,7 +258,6 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     gp.kblocks = static_cast<int32_t>((K + 63) / 64);
     gp.group_m = cfg.group_m;
     gp.stages = cfg.stages;
-    gp.prefetch = cfg.prefetch > 0 ? cfg.prefetch : 0;
     gp.debug_flags = 0;
     gp.units = cfg.units;
     gp.full_tiles = tiles - cfg.split_tiles;

@@ -44,7 +44,6 @@ constexpr double kFixupCycles = 11000.0;      // stream-K: segment hand-overs an
 constexpr double kMidFixupCycles = 27000.0;
 constexpr double kHiddenFixupCycles = 1500.0;
 constexpr int kMaxSplits = 32;
-constexpr int kDefaultPrefetch = -1;          // L2 prefetch distance (K slices); -1: none
 constexpr int kDefaultTimeoutMs = 1000;
 
 bool dtype_pair_ok(int din, int dout) {
@@ -213,7 +212,6 @@ static tsgemm_status_t choose_cluster_split(int64_t M, int64_t N, int64_t K, int
     c.grid = static_cast<int32_t>(std::min<int64_t>(tiles, slots) * 2);
     c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
     c.debug_flags = f.debug_flags;
-    c.prefetch = f.prefetch ? f.prefetch : kDefaultPrefetch;
     (void)kblocks;
     *out = c;
     return TSGEMM_OK;
@@ -240,7 +238,6 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     if (f.split_tiles < 0 || (f.split_tiles > 0 && f.splits < 2)) return TSGEMM_ERR_INVALID_ARG;
     if (f.stream_k_tiles < -1) return TSGEMM_ERR_INVALID_ARG;
     if (f.cluster_split < 0 || f.cluster_split > 2) return TSGEMM_ERR_UNSUPPORTED;
-    if (f.prefetch < -1 || f.prefetch > 64) return TSGEMM_ERR_INVALID_ARG;
     if (f.cluster_split == 2) {
         // the DSMEM K split: one-SM tiles, each split in two between the
         // CTAs of a 2 x 1 cluster; RRR layout and 16-bit inputs
@@ -368,7 +365,6 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
         c.workspace_bytes = 2 * slots * best_bm * static_cast<int64_t>(best_bn) * 4;
         c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
         c.debug_flags = f.debug_flags;
-        c.prefetch = f.prefetch ? f.prefetch : kDefaultPrefetch;
         *out = c;
         return TSGEMM_OK;
     }
@@ -380,7 +376,6 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     c.workspace_bytes = c.split_tiles * best_s * best_bm * static_cast<int64_t>(best_bn) * 4;
     c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
     c.debug_flags = f.debug_flags;
-    c.prefetch = f.prefetch ? f.prefetch : kDefaultPrefetch;
     *out = c;
     return TSGEMM_OK;
 }

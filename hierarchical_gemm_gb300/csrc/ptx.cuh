@@ -233,11 +233,12 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Hint: bring the 2-D box at (c0 = inner, c1 = outer) of the tensor into L2
-// (no shared memory, no completion to wait for).  Same coordinate rules as
-// the tiled load.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t c0, int32_t c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(m), "r"(c0), "r"(c1)
+// Hint: bring the 3-D box at (c0 = inner, c1, c2 = outer) of the tensor into
+// L2 (no shared memory, no completion to wait for).  Same coordinate rules
+// as the tiled load.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m), "r"(c0), "r"(c1),
+                 "r"(c2)
                  : "memory");
 }
 

@@ -239,7 +239,6 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.kblocks = static_cast<int32_t>((K + tsg::slice_k(dtype_in) - 1) / tsg::slice_k(dtype_in));
     gp.group_m = cfg.group_m;
     gp.stages = cfg.stages;
-    gp.prefetch = cfg.prefetch > 0 ? cfg.prefetch : 0;
     gp.debug_flags = cfg.debug_flags;
     gp.units = cfg.units;
     gp.full_tiles = ((M + cfg.block_m - 1) / cfg.block_m) * gp.tiles_n - cfg.split_tiles - cfg.stream_k_tiles;

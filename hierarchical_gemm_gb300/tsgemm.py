@@ -36,7 +36,8 @@ _DTYPE_NAMES = {"f16": F16, "fp16": F16, "float16": F16, "half": F16,
 EXPORTS = ("tsgemm_plan", "tsgemm_plan_ex", "tsgemm_run", "tsgemm_destroy",
            "tsgemm_status", "tsgemm_get_config", "tsgemm_choose_config",
            "tsgemm_status_string", "tsgemm_run_splitk_noalloc",
-           "tsattn_forward", "tsattn_forward_ex", "tsattn_status")
+           "tsattn_forward", "tsattn_forward_ex", "tsattn_mla_decode", "tsattn_mla_decode_ex",
+           "tsattn_status")
 
 
 class Config(ctypes.Structure):
@@ -47,7 +48,7 @@ class Config(ctypes.Structure):
                 ("units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("timeout_ms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
                 ("split_tiles", ctypes.c_int64), ("stream_k_tiles", ctypes.c_int64),
-                ("cluster_split", ctypes.c_int32), ("prefetch", ctypes.c_int32)]
+                ("cluster_split", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -84,6 +85,10 @@ def _load():
     L.tsattn_forward.argtypes = [i64, i64, i64, i64, i32, i32, f32, i32, vp, vp, vp, vp, vp, vp]
     L.tsattn_forward_ex.restype = i32
     L.tsattn_forward_ex.argtypes = [i64, i64, i64, i64, i32, i32, f32, i32, vp, vp, vp, vp, vp, vp, i32, i32]
+    L.tsattn_mla_decode.restype = i32
+    L.tsattn_mla_decode.argtypes = [i64, i64, i64, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp]
+    L.tsattn_mla_decode_ex.restype = i32
+    L.tsattn_mla_decode_ex.argtypes = [i64, i64, i64, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32]
     L.tsattn_status.restype = i32
     L.tsattn_status.argtypes = []
     return L
@@ -286,6 +291,34 @@ def attention(Q, K, V, scale=None, causal=False, O=None, status=None, stream=Non
                                  _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(status), _stream_handle(stream),
                                  int(debug_flags), int(timeout_ms)),
            "tsattn_forward")
+    return O
+
+
+def mla_decode(Q, Q_pe, KV, K_pe, scale=None, O=None, status=None, stream=None, debug_flags=0, timeout_ms=0,
+               prefetch_blocks=0):
+    """MLA decode (tsattn_mla_decode): for CUDA tensors Q (B, H, 512), Q_pe
+    (B, H, 64), KV (B, Skv, 512) and K_pe (B, Skv, 64), contiguous, all
+    float16 or all bfloat16, O (B, H, 512) = softmax(scale * (Q KV^T +
+    Q_pe K_pe^T)) KV per batch.  scale defaults to 576 ** -0.5."""
+    import torch
+    if Q.dim() != 3 or Q_pe.dim() != 3 or KV.dim() != 3 or K_pe.dim() != 3:
+        raise ValueError("expected Q (B, H, 512), Q_pe (B, H, 64), KV (B, Skv, 512), K_pe (B, Skv, 64)")
+    B, H, dim = Q.shape
+    pe_dim = Q_pe.shape[2]
+    Skv = KV.shape[1]
+    if Q_pe.shape[:2] != (B, H) or KV.shape != (B, Skv, dim) or K_pe.shape != (B, Skv, pe_dim):
+        raise ValueError("inconsistent MLA shapes")
+    if not (Q.dtype == Q_pe.dtype == KV.dtype == K_pe.dtype) or \
+            not all(x.is_contiguous() for x in (Q, Q_pe, KV, K_pe)):
+        raise ValueError("Q, Q_pe, KV, K_pe must share a dtype and be contiguous")
+    if scale is None:
+        scale = float(dim + pe_dim) ** -0.5
+    if O is None:
+        O = torch.empty_like(Q)
+    _check(lib.tsattn_mla_decode_ex(B, H, Skv, dim, pe_dim, dtype_code(Q.dtype), float(scale), _ptr(Q), _ptr(Q_pe),
+                                    _ptr(KV), _ptr(K_pe), _ptr(O), _ptr(status), _stream_handle(stream),
+                                    int(debug_flags), int(timeout_ms), int(prefetch_blocks)),
+           "tsattn_mla_decode")
     return O
 
 

@@ -124,12 +124,6 @@ typedef struct {
                                CTA 0 through distributed shared memory, chunk
                                by chunk; no workspace.  Forced only; the
                                planner reports 1 otherwise. */
-    int32_t prefetch;       /* L2 prefetch distance in K slices: the producer
-                               asks for the operand boxes of the slice this
-                               many slices ahead of the one it loads into
-                               shared memory (a hint; no memory is written).
-                               Forced: > 0 a distance, -1 none; the planner
-                               reports -1 for none. */
 } tsgemm_config_t;
 
 /* Tests only: the first CTA (or CTA pair) skips the first operand load of

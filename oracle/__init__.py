@@ -250,6 +250,25 @@ def attention(Q_bits, K_bits, V_bits, dtype_in, scale, causal=False):
     return O, bound
 
 
+def mla_decode(Q_bits, Qpe_bits, KV_bits, Kpe_bits, dtype_in, scale):
+    """The MLA decode shape of the attention block (the FlashMLA example of
+    the TileScale README): per batch b and head h, scores over the latent
+    and rotary parts, s[t] = Q[b,h] . KV[b,t] + Q_pe[b,h] . K_pe[b,t], and
+    O[b,h] = softmax(scale s) KV[b] -- the latent cache is also the value.
+    That is the attention definition above with the query [Q Q_pe], the keys
+    [KV K_pe] (576 deep) and the values KV (512 wide), one query row per
+    head.  Q_bits (B, H, dim), Qpe_bits (B, H, pe), KV_bits (B, Skv, dim),
+    Kpe_bits (B, Skv, pe).  Returns (O, bound) of shape (B, H, dim)."""
+    Q_bits = np.asarray(Q_bits)
+    B, H, dim = Q_bits.shape
+    Skv = np.asarray(KV_bits).shape[1]
+    q = np.concatenate([Q_bits, np.asarray(Qpe_bits)], axis=2).reshape(B, 1, H, -1)
+    k = np.concatenate([np.asarray(KV_bits), np.asarray(Kpe_bits)], axis=2).reshape(B, 1, Skv, -1)
+    v = np.asarray(KV_bits).reshape(B, 1, Skv, dim)
+    O, bound = attention(q, k, v, dtype_in, scale, causal=False)
+    return O.reshape(B, H, dim), bound.reshape(B, H, dim)
+
+
 # Acceptance rule for an attention output (derived from the arithmetic of
 # the kernel's online softmax): the weights are computed in fp32 and
 # rounded once to the 16-bit input format before they multiply V, a

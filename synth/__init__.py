@@ -139,5 +139,5 @@ def matrix(rows, cols, dist, seed, dtype, out=None):
     return out
 
 
-from .workloads import (WORKLOADS, EXTRA_WORKLOADS, ATTN_WORKLOADS, workload, attn_workload,  # noqa: E402,F401
-                        inputs, stored)
+from .workloads import (WORKLOADS, EXTRA_WORKLOADS, ATTN_WORKLOADS, MLA_WORKLOADS, workload,  # noqa: E402,F401
+                        attn_workload, mla_workload, mla_inputs, inputs, stored)

@@ -65,6 +65,45 @@ ATTN_WORKLOADS = {
 }
 
 
+# The MLA decode shape (softmax(scale [Q Q_pe] [KV K_pe]^T) KV per batch):
+# one query token per sequence, H heads, a latent cache of Skv keys that is
+# both key (with its rotary part) and value; entries N(0, 1), scale
+# (512 + 64)^-1/2.  Seeds: Q 0x7E5A0000 + index, Q_pe that + 0x300, KV that
+# + 0x100, K_pe that + 0x400.
+MLA_WORKLOADS = {
+    "mla_decode_b64h128s4096_bf16": dict(
+        index=10, B=64, H=128, Skv=4096, dim=512, pe_dim=64, dtype="bf16"),
+}
+
+
+def mla_workload(name):
+    w = dict(MLA_WORKLOADS[name])
+    w["name"] = name
+    w["seed_q"] = _SEED_BASE + w["index"]
+    w["seed_qpe"] = _SEED_BASE + w["index"] + 0x300
+    w["seed_kv"] = _SEED_BASE + w["index"] + 0x100
+    w["seed_kpe"] = _SEED_BASE + w["index"] + 0x400
+    w["scale"] = float(w["dim"] + w["pe_dim"]) ** -0.5
+    # two products per key and head: 576-deep scores, 512-wide values
+    w["flops"] = 2 * w["B"] * w["H"] * w["Skv"] * (w["dim"] + w["pe_dim"] + w["dim"])
+    # Q, Q_pe, KV, K_pe read once, O written once (16-bit)
+    w["bytes"] = 2 * (w["B"] * w["H"] * (w["dim"] + w["pe_dim"]) + w["B"] * w["Skv"] * (w["dim"] + w["pe_dim"])
+                      + w["B"] * w["H"] * w["dim"])
+    return w
+
+
+def mla_inputs(w, off=0):
+    """Q (B, H, dim), Q_pe (B, H, pe_dim), KV (B, Skv, dim), K_pe (B, Skv,
+    pe_dim) bit patterns of an MLA workload, N(0, 1)."""
+    from . import matrix
+    B, H, S = w["B"], w["H"], w["Skv"]
+
+    def mk(rows, cols, seed):
+        return matrix(B * rows, cols, ("normal", 1.0), seed + off, w["dtype"]).reshape(B, rows, cols)
+    return (mk(H, w["dim"], w["seed_q"]), mk(H, w["pe_dim"], w["seed_qpe"]),
+            mk(S, w["dim"], w["seed_kv"]), mk(S, w["pe_dim"], w["seed_kpe"]))
+
+
 def attn_workload(name):
     w = dict(ATTN_WORKLOADS[name])
     w["name"] = name

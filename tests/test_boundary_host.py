@@ -428,15 +428,3 @@ def test_causal_launch_order_covers_every_tile_once(BH, nq, group):
     for c0 in range(0, BH * nq, span):
         qbs = [qb for _, qb in order[c0:c0 + span]]
         assert qbs == sorted(qbs, reverse=True)
-
-
-def test_prefetch_distance_field(ts):
-    # the L2 prefetch distance: -1 (none) unless forced; a forced distance
-    # is kept; out-of-range values are argument errors
-    c = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, prefetch=12)
-    assert c["prefetch"] == 12
-    assert ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, prefetch=-1)["prefetch"] == -1
-    for bad in (-2, 65):
-        with pytest.raises(ts.TsgemmError) as e:
-            ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, prefetch=bad)
-        assert e.value.status == ts.ERR_INVALID_ARG

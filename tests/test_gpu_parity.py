@@ -201,23 +201,6 @@ def test_persistent_loop_with_small_grid(block_m, grid):
     _check(C, A, B, "bf16", "bf16", exact=True)
 
 
-@pytest.mark.parametrize("layout", LAYOUTS)
-@pytest.mark.parametrize("force", [
-    dict(block_m=256, block_n=256, prefetch=3),
-    dict(block_m=128, block_n=192, prefetch=12, grid=5),
-    dict(block_m=256, block_n=128, splits=3, prefetch=9, grid=4),
-    dict(block_m=256, block_n=256, stream_k_tiles=9, prefetch=20, grid=6),
-])
-def test_l2_prefetch_ahead(layout, force):
-    # the producer's L2 prefetch of the boxes some slices ahead, across the
-    # boundaries of a slot's units; a hint only, so the result is exact
-    A = _ints(704, 1000, 91)
-    B = _ints(1000, 520, 92)
-    C, cfg = run_gemm(A, B, "bf16", "bf16", layout=layout, **force)
-    assert cfg["prefetch"] == force["prefetch"]
-    _check(C, A, B, "bf16", "bf16", exact=True)
-
-
 @pytest.mark.parametrize("M", [1, 128, 200, 257, 511])
 def test_pair_tiles_with_ragged_rows(M):
     # A pair tile whose second CTA has few or no valid rows.

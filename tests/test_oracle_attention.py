@@ -110,3 +110,30 @@ def test_acceptance_rule_catches_a_perturbation():
     bad[0, 0, 1, 2] += 0.02 * bound[0, 0, 1, 2] + 1e-3
     ok, info = oracle.accept_attention(bad.astype(np.float32), O, bound, "f32")
     assert not ok and info["first_bad"] == [0, 0, 1, 2]
+
+
+# ------------------------------------------------------------ MLA decode --
+
+def test_mla_decode_matches_float64_torch():
+    # The MLA decode shape against torch's float64 arithmetic written out
+    # from the definition: scores over the latent and rotary parts, the
+    # softmax over keys, and the latent cache as the values.
+    import torch
+    B, H, S, dim, pe = 2, 5, 37, 16, 8
+    r = np.random.default_rng(12)
+    q, qpe, kv, kpe = (synth.quantise(r.standard_normal(shape), "bf16")
+                       for shape in ((B, H, dim), (B, H, pe), (B, S, dim), (B, S, pe)))
+    scale = 0.37
+    O, bound = oracle.mla_decode(q, qpe, kv, kpe, "bf16", scale)
+
+    def t(x):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    s = scale * (t(q) @ t(kv).transpose(1, 2) + t(qpe) @ t(kpe).transpose(1, 2))  # (B, H, S)
+    w = torch.softmax(s, dim=-1)
+    ref = w @ t(kv)
+    mag = w @ t(kv).abs()
+    assert np.allclose(O, ref.numpy(), rtol=1e-12, atol=1e-13)
+    assert np.allclose(bound, mag.numpy(), rtol=1e-12, atol=1e-13)
+    # the rotary part counts: dropping it changes the result
+    O0, _ = oracle.mla_decode(q, np.zeros_like(qpe), kv, kpe, "bf16", scale)
+    assert not np.allclose(O0, O, rtol=1e-6, atol=1e-9)
