@@ -17,24 +17,29 @@
 //     latent columns of each key block that it loads for the scores;
 //   * the scores' 576-deep contraction is split between the pair: CTA 0 over
 //     latent dims [0, 256), CTA 1 over latent dims [256, 512) and the 64
-//     rotary dims; each holds only its part of Q and of every key block in
-//     shared memory;
+//     rotary dims; each holds only its part of every key block in shared
+//     memory, and its latent part of Q in tensor memory (the A operand of
+//     the score MMAs, written there once by the softmax threads, a row
+//     each); CTA 1's rotary part of Q stays in shared memory;
 //   * each CTA's softmax warpgroup (a thread per query head) reads its fp32
 //     partial scores from tensor memory, writes them into the partner's
 //     shared memory (distributed shared memory, st.shared::cluster), and adds
 //     the partner's partial to its own: both CTAs then hold the same full
 //     scores (the addition is commutative, so the sums agree bit for bit),
 //     keep the same running maximum and row sums, and form the same weights
-//     P, which each writes into its own tensor memory as the A operand of its
-//     P V (two weights per 32-bit column, like the attention block);
-//   * score buffers are double buffered, so the tensor cores compute the next
-//     block's partial scores while the softmax works on this one.
+//     P, which each writes into its own shared memory (128-byte swizzle) as
+//     the A operand of its P V;
+//   * the exchange runs a block ahead: while the softmax works on block j,
+//     block j + 1's partial is already on its way to the partner (two
+//     exchange buffers), and the tensor cores compute block j + 2's partial
+//     scores as soon as the softmax has read block j's (two score buffers).
 // Warps 0-3 run the softmax and epilogue (warp w reads tensor-memory lanes
-// 32 w .. 32 w + 31), warp 4 lane 0 loads Q once and streams key blocks
-// through a two-slot ring (optionally asking for later blocks in L2 ahead),
-// warp 5 lane 0 issues the MMAs.  Every wait is bounded in time; a CTA that
-// gives up records a timeout, sets its partner's abort flag, lets its copies
-// and MMAs finish, frees tensor memory and returns.
+// 32 w .. 32 w + 31), warp 4 lane 0 loads CTA 1's rotary part of Q once and
+// streams key blocks through a three-slot ring (optionally asking for later
+// blocks in L2 ahead), warp 5 lane 0 issues the MMAs.  Every wait is
+// bounded in time; a CTA that gives up records a timeout, sets its
+// partner's abort flag, lets its copies and MMAs finish, frees tensor
+// memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,28 +59,32 @@ constexpr int kDR = 64;                 // rotary dims
 constexpr int kVHalf = kDL / 2;         // value columns per CTA
 constexpr int kThreads = 192;           // warps 0-3 softmax, 4 loads, 5 MMAs
 constexpr int kWarpLoad = 4, kWarpMma = 5;
-constexpr int kSlots = 2;               // key block ring depth
+constexpr int kSlots = 3;               // key block ring depth
 // a 64-dim column of the 128-byte swizzle: 128 heads or 64 keys x 128 bytes
 constexpr uint32_t kQAtom = kH * 128u;  // 16 KiB
 constexpr uint32_t kKAtom = kN * 128u;  // 8 KiB
 constexpr int kMaxAtoms = 5;            // CTA 0: 4 latent atoms; CTA 1: 4 latent + 1 rotary
-constexpr uint32_t kQOff = 0;
-constexpr uint32_t kKOff = kMaxAtoms * kQAtom;                 // 80 KiB
-constexpr uint32_t kXOff = kKOff + kSlots * kMaxAtoms * kKAtom;  // +80 KiB
-constexpr uint32_t kXBytes = kH * kN * 4u;                     // the partner's fp32 partial scores
-constexpr uint32_t kBarOff = kXOff + kXBytes;
-// barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], o_ready,
-// x_full, x_free, drain
-constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 1 + 2 + 1;
+constexpr uint32_t kSlotBytes = kMaxAtoms * kKAtom;          // 40 KiB
+constexpr uint32_t kXBytes = kH * kN * 4u;                   // a partner's fp32 partial scores
+constexpr uint32_t kQOff = 0;                                // CTA 1: the rotary part of Q
+constexpr uint32_t kPOff = kQOff + kQAtom;                   // the weights P (128 x 64, 16 KiB)
+constexpr uint32_t kKOff = kPOff + kQAtom;
+constexpr uint32_t kXOff = kKOff + kSlots * kSlotBytes;      // two exchange buffers
+constexpr uint32_t kBarOff = kXOff + 2 * kXBytes;
+// barriers: q_full, qt_full, kv_full[3], kv_empty[3], s_full[2], s_free[2],
+// p_full, pv_done, x_full[2], x_free[2], drain
+constexpr int kNumBars = 2 + 2 * kSlots + 4 + 2 + 4 + 1;
 constexpr uint32_t kMiscOff = kBarOff + 8u * kNumBars;
 constexpr uint32_t kSmemBytes = 1024u + kMiscOff + 16u;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kTmemCols = 512;     // O at 0 (256 columns), score buffer b at 256 + 64 b
-constexpr uint32_t kSCol = 256;
+constexpr uint32_t kTmemCols = 512;     // O at 0 (256 columns), score buffer i at 256 + 64 i,
+constexpr uint32_t kSCol = 256;         // the latent part of Q at 384 (two elements per column)
+constexpr uint32_t kQCol = 384;
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
 constexpr int kDefaultPrefetch = 0;     // key blocks asked for in L2 ahead of the ring
 
 struct MlaParams {
+    const void* Q;        // [B][H][512]: each softmax thread copies its head's part into tensor memory
     int32_t B, H, Skv;
     int32_t nblk;         // key blocks: ceil(Skv / 64)
     float scale_log2;     // scale * log2(e)
@@ -95,21 +104,23 @@ __host__ __device__ constexpr uint32_t idesc(bool f16, uint32_t n, bool b_nmajor
 
 struct Bars {
     uint32_t b;
-    __device__ uint32_t q_full() const { return b; }
-    __device__ uint32_t kv_full(int s) const { return b + 8u * (1 + s); }
-    __device__ uint32_t kv_empty(int s) const { return b + 8u * (1 + kSlots + s); }
-    __device__ uint32_t s_full(int i) const { return b + 8u * (1 + 2 * kSlots + i); }
-    __device__ uint32_t p_full(int i) const { return b + 8u * (3 + 2 * kSlots + i); }
-    __device__ uint32_t o_ready() const { return b + 8u * (5 + 2 * kSlots); }    // a P V complete
-    __device__ uint32_t x_full() const { return b + 8u * (6 + 2 * kSlots); }     // partner's partial written here
-    __device__ uint32_t x_free() const { return b + 8u * (7 + 2 * kSlots); }     // partner read what we wrote
-    __device__ uint32_t drain() const { return b + 8u * (8 + 2 * kSlots); }
+    __device__ uint32_t q_full() const { return b; }                                   // rotary Q (TMA)
+    __device__ uint32_t qt_full() const { return b + 8u; }                             // latent Q in tensor memory
+    __device__ uint32_t kv_full(int s) const { return b + 8u * (2 + s); }
+    __device__ uint32_t kv_empty(int s) const { return b + 8u * (2 + kSlots + s); }
+    __device__ uint32_t s_full(int i) const { return b + 8u * (2 + 2 * kSlots + i); }  // partial scores ready
+    __device__ uint32_t s_free(int i) const { return b + 8u * (4 + 2 * kSlots + i); }  // ... read by the softmax
+    __device__ uint32_t p_full() const { return b + 8u * (6 + 2 * kSlots); }           // P written
+    __device__ uint32_t pv_done() const { return b + 8u * (7 + 2 * kSlots); }          // a P V complete
+    __device__ uint32_t x_full(int i) const { return b + 8u * (8 + 2 * kSlots + i); }  // partner's partial here
+    __device__ uint32_t x_free(int i) const { return b + 8u * (10 + 2 * kSlots + i); } // partner read ours
+    __device__ uint32_t drain() const { return b + 8u * (12 + 2 * kSlots); }
 };
 
-// One softmax thread: query head row (lane quarter `quarter`, lane `lane`)
-// of the CTA's 128 heads.  Returns false if the CTA is aborting.
+// One softmax thread: query head row r = 32 quarter + lane of the CTA's 128
+// heads.
 template <bool kF16>
-__device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar, uint32_t tmem, uint32_t xbuf,
+__device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar, uint32_t tmem, uint32_t base,
                                              uint32_t peer, int b, int h0, int quarter, int lane,
                                              const WaitCtl& ctl) {
     const int r = quarter * 32 + lane;  // head within the block
@@ -118,45 +129,92 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
     // every thread waits itself: each then reads or overwrites only its own
     // row, after the barrier's acquire
     auto wait_cluster = [&](uint32_t bb, uint32_t parity) { return wait_bounded<true>(bb, parity, ctl); };
-    const uint32_t xmine = xbuf + static_cast<uint32_t>(r) * 16u;  // row r: 16-byte chunk c at + c * 2 KiB
-    const uint32_t xpeer = mapa_shared(xmine, peer);
-    float m_used = -INFINITY;  // base-2 maximum the weights are taken against
-    float l = 0.0f;
-    bool ok = true;
-    for (int j = 0; j < p.nblk; ++j) {
+    auto warp_wait = [&](uint32_t bb, uint32_t parity) -> bool {
+        int good = 1;
+        if (lane == 0) good = wait_bounded(bb, parity, ctl) ? 1 : 0;
+        return __shfl_sync(0xffffffffu, good, 0) != 0;
+    };
+    // exchange buffer i, row r: 16-byte chunk c at + c * 2 KiB
+    auto xaddr = [&](int i) { return base + kXOff + static_cast<uint32_t>(i) * kXBytes + static_cast<uint32_t>(r) * 16u; };
+    // This head's latent part of Q (256 dims, two per 32-bit column, as
+    // they lie in memory) into tensor memory, the score MMAs' A operand;
+    // heads past H are zero.
+    {
+        const uint32_t rank = cluster_ctarank();
+        const int head = h0 + r;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.Q) +
+                               ((static_cast<int64_t>(b) * p.H + head) * kDL + rank * kVHalf) / 2;
+#pragma unroll 1
+        for (int c = 0; c < kVHalf / 2; c += 32) {
+            uint32_t v[32];
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {
+                uint4 x4 = make_uint4(0u, 0u, 0u, 0u);
+                if (head < p.H) x4 = __ldg(reinterpret_cast<const uint4*>(qrow + c + q));
+                v[q] = x4.x;
+                v[q + 1] = x4.y;
+                v[q + 2] = x4.z;
+                v[q + 3] = x4.w;
+            }
+            tmem_st_32x32b_x32(trow + kQCol + c, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.qt_full());
+    }
+    // Block j's partial scores: read them from score buffer j & 1 (and free
+    // it for block j + 2), keep them in `own`, and write them into the
+    // partner's exchange buffer j & 1 once it has read block j - 2 there.
+    uint32_t own[64];
+    auto send = [&](int j) -> bool {
         const int i = j & 1;
-        if (!wait_bounded(bar.s_full(i), static_cast<uint32_t>(j >> 1) & 1u, ctl)) {
-            ok = false;
-            break;
-        }
+        if (!warp_wait(bar.s_full(i), static_cast<uint32_t>(j >> 1) & 1u)) return false;
         tc_fence_after();
-        uint32_t s[64];
-        tmem_ld_32x32b_x32(trow + kSCol + 64u * i, *reinterpret_cast<uint32_t(*)[32]>(s));
-        tmem_ld_32x32b_x32(trow + kSCol + 64u * i + 32u, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+        tmem_ld_32x32b_x32(trow + kSCol + 64u * i, *reinterpret_cast<uint32_t(*)[32]>(own));
+        tmem_ld_32x32b_x32(trow + kSCol + 64u * i + 32u, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
         tmem_ld_wait();
-        // this CTA's partial goes to the partner, once it has read the last one
-        if (j > 0 && !wait_cluster(bar.x_free(), static_cast<uint32_t>(j - 1) & 1u)) {
-            ok = false;
-            break;
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.s_free(i));
+        if (j >= 2 && !wait_cluster(bar.x_free(i), static_cast<uint32_t>((j - 2) >> 1) & 1u)) return false;
+        const uint32_t dst = mapa_shared(xaddr(i), peer);
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-            st_shared_cluster_v4(xpeer + c * 2048u, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-        mbar_arrive_cluster(bar.x_full(), peer);
-        if (!wait_cluster(bar.x_full(), static_cast<uint32_t>(j) & 1u)) {
+            st_shared_cluster_v4(dst + c * 2048u, own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
+        mbar_arrive_cluster(bar.x_full(i), peer);
+        return true;
+    };
+    float m_used = -INFINITY;  // base-2 maximum the weights are taken against
+    float l = 0.0f;
+    bool ok = send(0);
+    // the weights' row in the 128-byte swizzle: 16-byte chunk c of row r at
+    // r * 128 + ((c ^ (r mod 8)) * 16)
+    const uint32_t prow = base + kPOff + static_cast<uint32_t>(r) * 128u;
+    for (int j = 0; ok && j < p.nblk; ++j) {
+        const int i = j & 1;
+        float f[64];
+        // this block's full scores: own partial + the partner's
+#pragma unroll
+        for (int c = 0; c < 64; ++c) f[c] = __uint_as_float(own[c]);
+        if (!wait_cluster(bar.x_full(i), static_cast<uint32_t>(j >> 1) & 1u)) {
             ok = false;
             break;
         }
-        float f[64];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-            const float4 v = ld_shared_f4(xmine + c * 2048u);
-            f[4 * c] = __uint_as_float(s[4 * c]) + v.x;
-            f[4 * c + 1] = __uint_as_float(s[4 * c + 1]) + v.y;
-            f[4 * c + 2] = __uint_as_float(s[4 * c + 2]) + v.z;
-            f[4 * c + 3] = __uint_as_float(s[4 * c + 3]) + v.w;
+            const float4 v = ld_shared_f4(xaddr(i) + c * 2048u);
+            f[4 * c] += v.x;
+            f[4 * c + 1] += v.y;
+            f[4 * c + 2] += v.z;
+            f[4 * c + 3] += v.w;
         }
-        mbar_arrive_cluster(bar.x_free(), peer);  // the partner may write the next partial
+        mbar_arrive_cluster(bar.x_free(i), peer);  // the partner may write block j + 2 here
+        // the next block's partial goes out before this block's softmax
+        if (j + 1 < p.nblk && !send(j + 1)) {
+            ok = false;
+            break;
+        }
         // keys past Skv weigh nothing
         const int k0 = j * kN;
         if (k0 + kN > p.Skv) {
@@ -176,19 +234,18 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
         const float mb = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         const float m_new = fmaxf(m_used, mb * c2);  // (c2 > 0)
         const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
+        // P V of block j - 1 complete: its weights may be overwritten, and the
+        // output accumulator holds P_0 V + ... + P_{j-1} V
+        if (j >= 1 && !warp_wait(bar.pv_done(), static_cast<uint32_t>(j - 1) & 1u)) {
+            ok = false;
+            break;
+        }
         if (__any_sync(0xffffffffu, need)) {
-            // every lane of the warp moves to its own new maximum; the output
-            // accumulator must hold P_0 V + ... + P_{j-1} V, complete
+            // every lane of the warp moves to its own new maximum
             const float alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m_new);
             if (m_new > -INFINITY) m_used = m_new;
             l *= alpha;
             if (j >= 1) {
-                int good = 1;
-                if (lane == 0) good = wait_bounded(bar.o_ready(), static_cast<uint32_t>(j - 1) & 1u, ctl) ? 1 : 0;
-                if (!__shfl_sync(0xffffffffu, good, 0)) {
-                    ok = false;
-                    break;
-                }
                 tc_fence_after();
                 const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
@@ -205,36 +262,37 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
                     tmem_st_32x32b_x32(trow + c, o);
                 }
                 tmem_st_wait();
+                tc_fence_before();
             }
         }
-        // p = 2^(c2 s - m), two weights per packed fused multiply-add; P
-        // goes to the first 32 columns of this score buffer
+        // p = 2^(c2 s - m), two weights per packed fused multiply-add, into
+        // this row of P in shared memory
         const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
         const float2 c22 = make_float2(c2, c2), mn2 = make_float2(mneg, mneg);
         float2 rsum[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) rsum[q] = make_float2(0.0f, 0.0f);
-        uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const float2 x = fma2(make_float2(f[2 * q], f[2 * q + 1]), c22, mn2);
-            const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            rsum[q & 3] = add2(rsum[q & 3], pw);
-            w[q] = kF16 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
+        for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = 8 * c + 2 * q;
+                const float2 x = fma2(make_float2(f[e], f[e + 1]), c22, mn2);
+                const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                rsum[q] = add2(rsum[q], pw);
+                w[q] = kF16 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
+            }
+            st_shared_v4(prow + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1], w[2],
+                         w[3]);
         }
-        tmem_st_32x32b_x32(trow + kSCol + 64u * i, w);
         l += ((rsum[0].x + rsum[0].y) + (rsum[1].x + rsum[1].y)) + ((rsum[2].x + rsum[2].y) + (rsum[3].x + rsum[3].y));
-        tmem_st_wait();
-        tc_fence_before();
+        fence_proxy_async_shared();  // the MMA reads P through the async proxy
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar.p_full(i));
+        if (lane == 0) mbar_arrive(bar.p_full());
     }
     // ---------------------------------------------------- epilogue --
-    if (ok) {
-        int good = 1;
-        if (lane == 0) good = wait_bounded(bar.o_ready(), static_cast<uint32_t>(p.nblk - 1) & 1u, ctl) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, good, 0) != 0;
-    }
+    if (ok && !warp_wait(bar.pv_done(), static_cast<uint32_t>(p.nblk - 1) & 1u)) ok = false;
     if (!ok) return;
     tc_fence_after();
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
@@ -263,9 +321,8 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
 
 template <bool kF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_sm103(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQpe,
-                     const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmKpe,
-                     const MlaParams p) {
+    mla_decode_sm103(const __grid_constant__ CUtensorMap tmQpe, const __grid_constant__ CUtensorMap tmKV,
+                     const __grid_constant__ CUtensorMap tmKpe, const MlaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -287,21 +344,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar.q_full(), 1);
+        mbar_init(bar.qt_full(), 4);  // every softmax warp
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar.kv_full(s), 1);
             mbar_init(bar.kv_empty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar.s_full(i), 1);
-            mbar_init(bar.p_full(i), 4);  // every softmax warp
+            mbar_init(bar.s_free(i), 4);    // every softmax warp
+            mbar_init(bar.x_full(i), 128);  // every softmax thread of the partner
+            mbar_init(bar.x_free(i), 128);
         }
-        mbar_init(bar.o_ready(), 1);
-        mbar_init(bar.x_full(), 128);  // every softmax thread of the partner
-        mbar_init(bar.x_free(), 128);
+        mbar_init(bar.p_full(), 4);
+        mbar_init(bar.pv_done(), 1);
         mbar_init(bar.drain(), 1);
         *abort_flag = 0;
         fence_barrier_init();
-        prefetch_tmap(&tmQ);
         prefetch_tmap(&tmQpe);
         prefetch_tmap(&tmKV);
         prefetch_tmap(&tmKpe);
@@ -317,21 +375,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
         // ---------------------------------------- softmax and epilogue --
-        softmax_rows<kF16>(p, bar, tmem, base + kXOff, peer, b, h0, warp, lane, ctl);
+        softmax_rows<kF16>(p, bar, tmem, base, peer, b, h0, warp, lane, ctl);
     } else if (warp == kWarpLoad) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            // CTA r's columns: latent dims 256 r + 64 a for a < 4; CTA 1's
-            // fifth column is the rotary part
-            auto atom_map = [&](int a, bool q) -> const CUtensorMap* {
-                return a < 4 ? (q ? &tmQ : &tmKV) : (q ? &tmQpe : &tmKpe);
-            };
+            // CTA r's columns of a key block: latent dims 256 r + 64 a for
+            // a < 4; CTA 1's fifth column is the rotary part
+            auto atom_map = [&](int a) -> const CUtensorMap* { return a < 4 ? &tmKV : &tmKpe; };
             auto atom_x = [&](int a) { return a < 4 ? static_cast<int32_t>(rank) * kVHalf + 64 * a : 0; };
-            mbar_arrive_expect_tx(bar.q_full(), natoms * kQAtom);
-            for (int a = 0; a < natoms; ++a)
-                tma_load_3d(base + kQOff + a * kQAtom, atom_map(a, true), bar.q_full(), atom_x(a), h0, b);
+            if (rank == 1) {
+                mbar_arrive_expect_tx(bar.q_full(), kQAtom);
+                tma_load_3d(base + kQOff, &tmQpe, bar.q_full(), 0, h0, b);
+            } else {
+                mbar_arrive(bar.q_full());
+            }
             for (int j = kSlots; j < p.prefetch && j < p.nblk; ++j)
-                for (int a = 0; a < natoms; ++a) tma_prefetch_3d(atom_map(a, false), atom_x(a), j * kN, b);
+                for (int a = 0; a < natoms; ++a) tma_prefetch_3d(atom_map(a), atom_x(a), j * kN, b);
             uint32_t outstanding = 0, out_par = 0;
             for (int j = 0; j < p.nblk; ++j) {
                 const int st = j % kSlots;
@@ -339,13 +398,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!wait_bounded(bar.kv_empty(st), ph ^ 1u, ctl)) break;
                 if (p.prefetch > 0 && j + p.prefetch < p.nblk)
                     for (int a = 0; a < natoms; ++a)
-                        tma_prefetch_3d(atom_map(a, false), atom_x(a), (j + p.prefetch) * kN, b);
+                        tma_prefetch_3d(atom_map(a), atom_x(a), (j + p.prefetch) * kN, b);
                 // tests only: the first pair's first CTA leaves its first block unloaded
                 if ((p.debug_flags & 1) && cluster == 0 && rank == 0 && j == 0) continue;
-                const uint32_t dst = base + kKOff + st * (kMaxAtoms * kKAtom);
+                const uint32_t dst = base + kKOff + st * kSlotBytes;
                 mbar_arrive_expect_tx(bar.kv_full(st), natoms * kKAtom);
                 for (int a = 0; a < natoms; ++a)
-                    tma_load_3d(dst + a * kKAtom, atom_map(a, false), bar.kv_full(st), atom_x(a), j * kN, b);
+                    tma_load_3d(dst + a * kKAtom, atom_map(a), bar.kv_full(st), atom_x(a), j * kN, b);
                 outstanding |= 1u << st;
                 out_par = (out_par & ~(1u << st)) | (ph << st);
             }
@@ -359,47 +418,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc(kF16, kN, false), kIdPV = idesc(kF16, kVHalf, true);
-            bool ok = wait_bounded(bar.q_full(), 0u, ctl);
-            // partial S_j = Q_r K_{j,r}^T into score buffer j & 1: both
-            // operands K-major, 16 dims per step (32 bytes along a row of a
-            // 64-dim column).  The buffer held P_{j-2}, which P V of block
-            // j - 2 (issued before) has read.
+            bool ok = wait_bounded(bar.q_full(), 0u, ctl) && wait_bounded(bar.qt_full(), 0u, ctl);
+            // partial S_j = Q_r K_{j,r}^T into score buffer j & 1, 16 dims
+            // per step: the latent part with Q from tensor memory (8
+            // columns a step), CTA 1's rotary part with Q from shared
+            // memory; K K-major (32 bytes along a row of a 64-dim column a
+            // step).  For j >= 2 the softmax has read block j - 2 out of the
+            // buffer first.
             auto issue_s = [&](int j) -> bool {
                 const int st = j % kSlots;
+                if (j >= 2 && !wait_bounded(bar.s_free(j & 1), static_cast<uint32_t>((j - 2) >> 1) & 1u, ctl))
+                    return false;
                 if (!wait_bounded(bar.kv_full(st), static_cast<uint32_t>(j / kSlots) & 1u, ctl)) return false;
                 tc_fence_after();
-                const uint32_t ks = base + kKOff + st * (kMaxAtoms * kKAtom);
-                for (int k = 0; k < natoms * 4; ++k) {
-                    const uint64_t ad = smem_desc_sw128(base + kQOff + (k >> 2) * kQAtom + (k & 3) * 32u, 16u, 1024u);
+                const uint32_t ks = base + kKOff + st * kSlotBytes;
+                const uint32_t d = tmem + kSCol + 64u * (j & 1);
+                for (int k = 0; k < 16; ++k) {
                     const uint64_t bd = smem_desc_sw128(ks + (k >> 2) * kKAtom + (k & 3) * 32u, 16u, 1024u);
-                    umma_f16<1>(tmem + kSCol + 64u * (j & 1), ad, bd, kIdS, k > 0 ? 1u : 0u);
+                    umma_f16_ta(d, tmem + kQCol + 8u * k, bd, kIdS, k > 0 ? 1u : 0u);
+                }
+                if (natoms == 5) {
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = smem_desc_sw128(base + kQOff + k * 32u, 16u, 1024u);
+                        const uint64_t bd = smem_desc_sw128(ks + 4 * kKAtom + k * 32u, 16u, 1024u);
+                        umma_f16<1>(d, ad, bd, kIdS, 1u);
+                    }
                 }
                 umma_commit(bar.s_full(j & 1));
                 return true;
             };
-            // O_r += P_j V_{j,r}: P (128 heads x 64 keys, two per 32-bit
-            // column) is the tensor-memory A operand; V the N-major B
-            // operand over the CTA's four latent columns of the block
-            // (64-dim columns 8 KiB apart, 8-key groups 1 KiB apart, the
-            // k-th 16-key step 2 KiB on).
+            // O_r += P_j V_{j,r}: P (128 heads x 64 keys, K-major in the
+            // 128-byte swizzle) from shared memory; V the N-major B operand
+            // over the CTA's four latent columns of the block (64-dim
+            // columns 8 KiB apart, 8-key groups 1 KiB apart, the k-th 16-key
+            // step 2 KiB on).
             auto issue_pv = [&](int j) -> bool {
-                if (!wait_bounded(bar.p_full(j & 1), static_cast<uint32_t>(j >> 1) & 1u, ctl)) return false;
+                if (!wait_bounded(bar.p_full(), static_cast<uint32_t>(j) & 1u, ctl)) return false;
                 tc_fence_after();
-                const uint32_t vs = base + kKOff + (j % kSlots) * (kMaxAtoms * kKAtom);
+                const uint32_t vs = base + kKOff + (j % kSlots) * kSlotBytes;
 #pragma unroll
                 for (int k = 0; k < kN / 16; ++k) {
+                    const uint64_t ad = smem_desc_sw128(base + kPOff + k * 32u, 16u, 1024u);
                     const uint64_t bd = smem_desc_sw128(vs + k * 2048u, kKAtom, 1024u);
-                    umma_f16_ta(tmem, tmem + kSCol + 64u * (j & 1) + 8u * k, bd, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+                    umma_f16<1>(tmem, ad, bd, kIdPV, (j > 0 || k > 0) ? 1u : 0u);
                 }
-                umma_commit(bar.o_ready());
+                umma_commit(bar.pv_done());
                 umma_commit(bar.kv_empty(j % kSlots));  // the block's scores and values are read
                 return true;
             };
+            // S_0, S_1; then per block j: S_{j+2} (once the softmax has read
+            // S_j), P V_j (once it has written P_j)
             if (ok) ok = issue_s(0);
             if (ok && p.nblk > 1) ok = issue_s(1);
             for (int j = 0; ok && j < p.nblk; ++j) {
-                ok = issue_pv(j);
-                if (ok && j + 2 < p.nblk) ok = issue_s(j + 2);
+                if (j + 2 < p.nblk) ok = issue_s(j + 2);
+                if (ok) ok = issue_pv(j);
             }
             // every MMA issued above completes before tensor memory is freed
             umma_commit(bar.drain());
@@ -520,12 +593,13 @@ extern "C" tsgemm_status_t tsattn_mla_decode_ex(int64_t B, int64_t H, int64_t Sk
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    alignas(64) CUtensorMap tmQ, tmQpe, tmKV, tmKpe;
-    if (!map3(&tmQ, Q, kDL, H, kH) || !map3(&tmQpe, Q_pe, kDR, H, kH) || !map3(&tmKV, KV, kDL, Skv, kN) ||
+    alignas(64) CUtensorMap tmQpe, tmKV, tmKpe;
+    if (!map3(&tmQpe, Q_pe, kDR, H, kH) || !map3(&tmKV, KV, kDL, Skv, kN) ||
         !map3(&tmKpe, K_pe, kDR, Skv, kN))
         return TSGEMM_ERR_CUDA;
 
     MlaParams prm{};
+    prm.Q = Q;
     prm.B = static_cast<int32_t>(B);
     prm.H = static_cast<int32_t>(H);
     prm.Skv = static_cast<int32_t>(Skv);
@@ -547,7 +621,7 @@ extern "C" tsgemm_status_t tsattn_mla_decode_ex(int64_t B, int64_t H, int64_t Sk
     lc.blockDim = dim3(kThreads, 1, 1);
     lc.dynamicSmemBytes = kSmemBytes;
     lc.stream = s;
-    void* args[5] = {&tmQ, &tmQpe, &tmKV, &tmKpe, &prm};
+    void* args[4] = {&tmQpe, &tmKV, &tmKpe, &prm};
     if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;
