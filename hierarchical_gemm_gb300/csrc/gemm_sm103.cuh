@@ -90,7 +90,8 @@ struct GemmParams {
     int64_t sk_tiles;     // stream-K mode: the last sk_tiles tiles (0: split mode)
     int64_t sk_work;      // sk_tiles * kblocks K slices, spread over the slots
     uint32_t idesc;       // tcgen05 instruction descriptor
-    uint32_t pad_;
+    int32_t csplit;       // cluster split: CTAs of a cluster sharing each
+                          // tile's K range (2, 4 or 8), else 1
     void* C;
     float* ws;            // fp32 partials of the split tiles (S > 1), or of the
                           // stream-K segments that continue a tile (one per slot)
@@ -536,16 +537,21 @@ __host__ __device__ constexpr uint32_t smem_bytes_1sm(int stages) {
            (kCS ? kCsBytes : 0u) + 8u * (2 * stages + 5) /* barriers */ + 16u /* tmem holder, abort flag */;
 }
 
-// Cluster split (a 2 x 1 cluster of one-SM CTAs per tile): CTA 1 computes
-// the tile's second half of K and hands its accumulator, chunk by chunk, to
-// CTA 0 through distributed shared memory; CTA 0 adds it after its own
-// (the K order) and stores C.  Per epilogue warp and 32-column chunk: the
-// sender waits until the receiver's buffer is free, writes its 32 rows into
-// it with st.shared::cluster and arrives (release, cluster scope) on the
-// receiver's full barrier; the receiver waits for it (acquire), adds, and
-// arrives on the sender's empty barrier.  Every lane arrives, so each
-// lane's own writes (reads) are ordered before its arrival.  `buf` is this
-// warp's 4 KiB of its warpgroup's buffer in CTA 0; `phase` counts chunks.
+// Cluster split (a cs x 1 cluster of one-SM CTAs per tile, cs = 2, 4 or
+// 8): CTA r computes the r-th of cs consecutive parts of the tile's K
+// range, and the partial sums travel down the cluster as a chain: CTA r
+// receives 0 + p_0 + ... + p_{r-1} from CTA r - 1 through distributed
+// shared memory, adds its own p_r (so the parts are summed in K order) and
+// passes the sum to CTA r + 1; the last CTA stores C.  Per epilogue warp
+// and 32-column chunk: a sender waits until its successor's buffer is free
+// (the successor arrives on the sender's empty barrier), writes its 32 rows
+// there with st.shared::cluster and arrives (release, cluster scope) on
+// the successor's full barrier; a receiver waits for that (acquire), adds,
+// and arrives on its predecessor's empty barrier.  Every lane arrives, so
+// each lane's own writes (reads) are ordered before its arrival.  `buf` is
+// this warp's 4 KiB of its warpgroup's receive buffer; `phase` counts
+// chunks.  No CTA waits for one outside its cluster, whose CTAs the
+// hardware runs together.
 template <int BN, int kOut, class Release>
 __device__ __forceinline__ bool drain_cs(const GemmParams& p, const CUtensorMap* tmC, CStager<kOut>& out,
                                          const Unit& un, uint32_t tbase, int row0, int lane, int c_begin,
@@ -553,37 +559,39 @@ __device__ __forceinline__ bool drain_cs(const GemmParams& p, const CUtensorMap*
                                          uint32_t& phase, const WaitCtl& ctl, Release&& release) {
     const int col0 = un.tn * BN;
     const int c_end = c_begin + BN / 2;
+    const uint32_t last = static_cast<uint32_t>(p.csplit) - 1u;
 #pragma unroll 1
     for (int c = c_begin; c < c_end; c += 32) {
         uint32_t r[32];
-        if (rank != 0) {
-            if (!wait_bounded<true>(empty_bar, phase ^ 1u, ctl)) return false;  // the receiver read the last chunk
-            tmem_ld_32x32b_x32(tbase + c, r);
-            tmem_ld_wait();
-            if (c + 32 >= c_end) release();
-            const uint32_t dst = mapa_shared(buf + lane * 16u, 0u);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-                st_shared_cluster_v4(dst + v * 512u, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-            mbar_arrive_cluster(full_bar, 0u);
-        } else {
-            if (!wait_bounded<true>(full_bar, phase, ctl)) return false;
-            tmem_ld_32x32b_x32(tbase + c, r);
-            tmem_ld_wait();
-            if (c + 32 >= c_end) release();
-            float acc[32];
-            // the sum starts from a cleared (+0) accumulator: 0 + own + partner
+        tmem_ld_32x32b_x32(tbase + c, r);
+        tmem_ld_wait();
+        if (c + 32 >= c_end) release();
+        float acc[32];
+        if (rank == 0) {
+            // the sum starts from a cleared (+0) accumulator
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[j] = __fadd_rn(0.0f, __uint_as_float(r[j]));
+        } else {
+            if (!wait_bounded<true>(full_bar, phase, ctl)) return false;
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
                 const float4 x = ld_shared_f4(buf + lane * 16u + v * 512u);
-                acc[4 * v] = __fadd_rn(acc[4 * v], x.x);
-                acc[4 * v + 1] = __fadd_rn(acc[4 * v + 1], x.y);
-                acc[4 * v + 2] = __fadd_rn(acc[4 * v + 2], x.z);
-                acc[4 * v + 3] = __fadd_rn(acc[4 * v + 3], x.w);
+                acc[4 * v] = __fadd_rn(x.x, __uint_as_float(r[4 * v]));
+                acc[4 * v + 1] = __fadd_rn(x.y, __uint_as_float(r[4 * v + 1]));
+                acc[4 * v + 2] = __fadd_rn(x.z, __uint_as_float(r[4 * v + 2]));
+                acc[4 * v + 3] = __fadd_rn(x.w, __uint_as_float(r[4 * v + 3]));
             }
-            mbar_arrive_cluster(empty_bar, 1u);  // the buffer may be refilled
+            mbar_arrive_cluster(empty_bar, rank - 1u);  // the predecessor may refill this buffer
+        }
+        if (rank < last) {
+            if (!wait_bounded<true>(empty_bar, phase ^ 1u, ctl)) return false;  // the successor read the last chunk
+            const uint32_t dst = mapa_shared(buf + lane * 16u, rank + 1u);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                st_shared_cluster_v4(dst + v * 512u, __float_as_uint(acc[4 * v]), __float_as_uint(acc[4 * v + 1]),
+                                     __float_as_uint(acc[4 * v + 2]), __float_as_uint(acc[4 * v + 3]));
+            mbar_arrive_cluster(full_bar, rank + 1u);
+        } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
             out.put(p, tmC, row0, col0 + c, r);
@@ -593,9 +601,10 @@ __device__ __forceinline__ bool drain_cs(const GemmParams& p, const CUtensorMap*
     return true;
 }
 
-// kCS: launched as 2 x 1 clusters (a runtime launch attribute), the two
-// CTAs splitting each tile's K range and exchanging through distributed
-// shared memory (drain_cs).
+// kCS: launched as cs x 1 clusters (a runtime launch attribute, cs =
+// p.csplit), the CTAs of a cluster splitting each tile's K range and
+// chaining their partial sums through distributed shared memory
+// (drain_cs).
 template <int BN, int kOut, int kLayout, bool kF8 = false, bool kCS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_sm103_1sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -645,20 +654,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_alloc<1>(smem_u32(tmem_holder), TS::kTmemCols);
     tc_fence_before();
     __syncthreads();
-    if constexpr (kCS) cluster_sync();  // both CTAs' barriers initialised before either uses them
+    if constexpr (kCS) cluster_sync();  // every CTA's barriers initialised before any uses them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     // work slot and, for the cluster split, this CTA's half of every tile's K
     const uint32_t cs_rank = kCS ? cluster_ctarank() : 0u;
-    if constexpr (kCS) ctl.peer_abort[ctl.npeers++] = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), cs_rank ^ 1u);
-    const int64_t slot = kCS ? blockIdx.x >> 1 : blockIdx.x;
-    const int64_t nslots = kCS ? gridDim.x >> 1 : gridDim.x;
+    const int cs = kCS ? p.csplit : 1;
+    if constexpr (kCS) {
+        // a CTA that gives up sets its chain neighbours' abort flags
+        const uint32_t me = smem_u32(const_cast<int*>(abort_flag));
+        const bool has_prev = cs_rank > 0, has_next = static_cast<int>(cs_rank) + 1 < cs;
+        const uint32_t next = has_next ? mapa_shared(me, cs_rank + 1u) : 0u;
+        ctl.peer_abort[0] = has_prev ? mapa_shared(me, cs_rank - 1u) : next;
+        ctl.peer_abort[1] = next;
+        ctl.npeers = (has_prev ? 1 : 0) + (has_next ? 1 : 0);
+    }
+    const int64_t slot = blockIdx.x / cs;
+    const int64_t nslots = gridDim.x / cs;
     auto next_unit = [&](int64_t j, Unit& un) -> bool {
         if (!unit_at(p, slot, nslots, j, un)) return false;
         if constexpr (kCS) {
-            un.kb0 = static_cast<int>(cs_rank * p.kblocks / 2);
-            un.kb1 = static_cast<int>((cs_rank + 1) * p.kblocks / 2);
+            un.kb0 = static_cast<int>(static_cast<int64_t>(cs_rank) * p.kblocks / cs);
+            un.kb1 = static_cast<int>(static_cast<int64_t>(cs_rank + 1) * p.kblocks / cs);
         }
         return true;
     };
@@ -793,8 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane 0 ran a role loop alone may arrive in any convergence state.
     tc_fence_before();
     cta_barrier_any();
-    // (cluster split: neither CTA leaves while the other may still write
-    // into or read its shared memory)
+    // (cluster split: no CTA leaves while another may still write into or
+    // read its shared memory)
     if constexpr (kCS) cluster_barrier_any();
     if (warp == 1) {
         __syncwarp();

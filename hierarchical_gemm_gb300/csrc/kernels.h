@@ -7,9 +7,9 @@ namespace tsg {
 
 // Kernel entry for a tile width (64/128/192/256), output kind (0 fp16,
 // 1 bf16, 2 fp32), operand layout (tsgemm_layout_t), input width (in8:
-// 8-bit float inputs, RCR layout only) and cluster split (cs = 2: launched
-// as 2 x 1 clusters splitting each tile's K; RRR, 16-bit inputs); null for
-// an unsupported combination.
+// 8-bit float inputs, RCR layout only) and cluster split (cs = 2, 4 or 8:
+// launched as cs x 1 clusters splitting each tile's K; RRR, 16-bit
+// inputs); null for an unsupported combination.
 const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8, int cs);
 
 // Dynamic shared memory the kernel above uses with `stages` ring slots.

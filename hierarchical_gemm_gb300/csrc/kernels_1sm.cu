@@ -9,7 +9,7 @@
 namespace tsg {
 
 const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8, int cs) {
-    if (cs == 2) return layout == 0 && !in8 ? kernel_1sm_cs(block_n, out_kind) : nullptr;
+    if (cs >= 2) return layout == 0 && !in8 ? kernel_1sm_cs(block_n, out_kind) : nullptr;
     if (cs > 1) return nullptr;
     if (in8) return layout == 1 ? kernel_1sm_f8(block_n, out_kind) : nullptr;
     switch (layout) {
@@ -24,7 +24,7 @@ const void* kernel_1sm(int block_n, int out_kind, int layout, bool in8, int cs) 
 int64_t kernel_1sm_smem_bytes(int block_n, int out_kind, int stages, int cs) {
     auto pick = [&](auto bn) -> int64_t {
         constexpr int BN = decltype(bn)::value;
-        if (cs == 2) {
+        if (cs >= 2) {
             switch (out_kind) {
                 case kOutF16: return smem_bytes_1sm<BN, kOutF16, true>(stages);
                 case kOutBF16: return smem_bytes_1sm<BN, kOutBF16, true>(stages);

@@ -262,6 +262,7 @@ extern "C" tsgemm_status_t tsgemm_run_splitk_noalloc(int64_t M, int64_t N, int64
     gp.units = cfg.units;
     gp.full_tiles = tiles - cfg.split_tiles;
     gp.idesc = idesc_for(dtype_in, cfg.block_n);
+    gp.csplit = 1;
     gp.C = C;
     gp.ws = ws;
     gp.ws_own = nullptr;  // (stream-K only)

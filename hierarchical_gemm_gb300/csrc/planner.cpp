@@ -154,7 +154,7 @@ int64_t smem_bytes_for(int block_m, int block_n, int dtype_out, int stages, int 
     const int64_t staging = dtype_out == TSGEMM_F32 ? 0 : kEpiWarps * 2 * 32 * 32 * out_bytes(dtype_out);
     // cluster split: a 128 x 32 fp32 exchange chunk per epilogue warpgroup
     // and four barriers
-    const int64_t exchange = cluster_split == 2 ? 2 * 128 * 32 * 4 + 4 * 8 : 0;
+    const int64_t exchange = cluster_split >= 2 ? 2 * 128 * 32 * 4 + 4 * 8 : 0;
     return 1024 + stages * stage + staging + exchange + 8 * (2 * stages + 5) + 16;
 }
 
@@ -185,14 +185,12 @@ tsgemm_status_t validate_problem(int64_t M, int64_t N, int64_t K, int dtype_in, 
     return TSGEMM_OK;
 }
 
-// The DSMEM cluster-split plan (forced by cluster_split = 2): one-SM tiles
-// of the widest width up to N, every tile's K range split between the two
-// CTAs of a 2 x 1 cluster, one tile per cluster at a time.
-static tsgemm_status_t choose_cluster_split(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out,
-                                            int num_sms, const tsgemm_config_t& f, int64_t kblocks,
-                                            tsgemm_config_t* out) {
-    (void)K;
-    (void)dtype_in;
+// The DSMEM cluster-split plan (forced by cluster_split = 2, 4 or 8):
+// one-SM tiles of the widest width up to N, every tile's K range split
+// between the cs CTAs of a cs x 1 cluster, one tile per cluster at a time.
+static tsgemm_status_t choose_cluster_split(int64_t M, int64_t N, int num_sms, const tsgemm_config_t& f,
+                                            int dtype_out, tsgemm_config_t* out) {
+    const int cs = f.cluster_split;
     const int64_t n_pad = ceil_div(N, 64) * 64;
     int bn = f.block_n;
     if (!bn) bn = n_pad >= 256 ? 256 : (n_pad >= 192 ? 192 : (n_pad >= 128 ? 128 : 64));
@@ -200,19 +198,18 @@ static tsgemm_status_t choose_cluster_split(int64_t M, int64_t N, int64_t K, int
     c.block_m = 128;
     c.block_n = bn;
     c.splits = 1;
-    const int smax_fit = max_stages_for(128, bn, dtype_out, 2);
+    const int smax_fit = max_stages_for(128, bn, dtype_out, cs);
     if (f.stages > smax_fit || (f.stages != 0 && f.stages < 2)) return TSGEMM_ERR_UNSUPPORTED;
     c.stages = f.stages ? f.stages : smax_fit;
     c.group_m = f.group_m ? f.group_m : 8;
-    c.cluster_split = 2;
+    c.cluster_split = cs;
     const int64_t tiles = ceil_div(M, 128) * ceil_div(N, bn);
     c.units = tiles;
-    const int64_t slots = (f.grid ? f.grid : num_sms) / 2;
+    const int64_t slots = (f.grid ? f.grid : num_sms) / cs;
     if (slots < 1) return TSGEMM_ERR_UNSUPPORTED;
-    c.grid = static_cast<int32_t>(std::min<int64_t>(tiles, slots) * 2);
+    c.grid = static_cast<int32_t>(std::min<int64_t>(tiles, slots) * cs);
     c.timeout_ms = f.timeout_ms ? f.timeout_ms : kDefaultTimeoutMs;
     c.debug_flags = f.debug_flags;
-    (void)kblocks;
     *out = c;
     return TSGEMM_OK;
 }
@@ -237,21 +234,25 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     if (f.units != 0 || f.workspace_bytes != 0) return TSGEMM_ERR_INVALID_ARG;  // derived fields
     if (f.split_tiles < 0 || (f.split_tiles > 0 && f.splits < 2)) return TSGEMM_ERR_INVALID_ARG;
     if (f.stream_k_tiles < -1) return TSGEMM_ERR_INVALID_ARG;
-    if (f.cluster_split < 0 || f.cluster_split > 2) return TSGEMM_ERR_UNSUPPORTED;
-    if (f.cluster_split == 2) {
-        // the DSMEM K split: one-SM tiles, each split in two between the
-        // CTAs of a 2 x 1 cluster; RRR layout and 16-bit inputs
+    if (f.cluster_split < 0 || f.cluster_split > 8 || (f.cluster_split > 2 && f.cluster_split != 4 &&
+                                                        f.cluster_split != 8))
+        return TSGEMM_ERR_UNSUPPORTED;
+    const bool csplit = f.cluster_split >= 2;
+    if (csplit) {
+        // the DSMEM K split: one-SM tiles, each split into cs parts between
+        // the CTAs of a cs x 1 cluster; RRR layout and 16-bit inputs
         if (f.block_m == 256 || f.splits > 1 || f.split_tiles > 0 || f.stream_k_tiles > 0)
             return TSGEMM_ERR_INVALID_ARG;
-        if (layout != TSGEMM_LAYOUT_RRR || is_8bit(dtype_in) || num_sms < 2) return TSGEMM_ERR_UNSUPPORTED;
+        if (layout != TSGEMM_LAYOUT_RRR || is_8bit(dtype_in) || num_sms < f.cluster_split)
+            return TSGEMM_ERR_UNSUPPORTED;
     }
     if (f.stream_k_tiles > 0 && (f.splits > 1 || f.split_tiles > 0)) return TSGEMM_ERR_INVALID_ARG;
 
     const int64_t kblocks = ceil_div(K, slice_k(dtype_in));
     if (f.splits > kblocks || f.splits > 4096) return TSGEMM_ERR_UNSUPPORTED;
-    if (f.cluster_split == 2) {
-        if (kblocks < 2) return TSGEMM_ERR_UNSUPPORTED;
-        return choose_cluster_split(M, N, K, dtype_in, dtype_out, num_sms, f, kblocks, out);
+    if (csplit) {
+        if (kblocks < f.cluster_split) return TSGEMM_ERR_UNSUPPORTED;  // every CTA needs a K slice
+        return choose_cluster_split(M, N, num_sms, f, dtype_out, out);
     }
 
     // Candidate tile widths: never wider than N rounded up to 64.

@@ -129,9 +129,10 @@ struct WaitCtl {
     volatile int* abort;   // shared memory
     int* status;           // global status word of the plan
     uint64_t timeout_ns;
-    // shared::cluster address of the abort flag of the other CTA of a 2 x 1
-    // cluster, which a CTA that gives up sets too
-    uint32_t peer_abort[1] = {0u};
+    // shared::cluster addresses of the abort flags of other CTAs of the
+    // cluster (the pair's other CTA, or a cluster split's chain
+    // neighbours), which a CTA that gives up sets too
+    uint32_t peer_abort[2] = {0u, 0u};
     int npeers = 0;
 };
 
@@ -139,7 +140,8 @@ struct WaitCtl {
 // plan's status word.
 __device__ __forceinline__ void record_timeout(const WaitCtl& ctl) {
     *ctl.abort = 1;
-    for (int i = 0; i < ctl.npeers; ++i) st_shared_cluster_u32(ctl.peer_abort[i], 1u);
+    if (ctl.npeers > 0) st_shared_cluster_u32(ctl.peer_abort[0], 1u);
+    if (ctl.npeers > 1) st_shared_cluster_u32(ctl.peer_abort[1], 1u);
     atomicExch(ctl.status, 5 /* TSGEMM_ERR_TIMEOUT */);
     __threadfence();
 }

@@ -140,7 +140,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
 
     const bool pair = cfg.block_m == 256;
     const bool in8 = tsg::is_8bit(dtype_in);
-    const int cs = cfg.cluster_split == 2 ? 2 : 1;
+    const int cs = cfg.cluster_split >= 2 ? cfg.cluster_split : 1;
     const void* kern = pair ? tsg::kernel_2sm(cfg.block_n, out_kind(dtype_out), layout, in8)
                             : tsg::kernel_1sm(cfg.block_n, out_kind(dtype_out), layout, in8, cs);
     const int64_t need = pair ? tsg::kernel_2sm_smem_bytes(cfg.block_n, out_kind(dtype_out), cfg.stages)
@@ -158,18 +158,18 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;
     }
-    if (pair || cs == 2) {
+    if (pair || cs >= 2) {
         // Persistent clusters: launch no more than can be resident at once
         // (a cluster's CTAs must share a GPC).
-        const int per_cluster = 2;
+        const int per_cluster = pair ? 2 : cs;
         cudaLaunchConfig_t lc{};
         lc.gridDim = dim3(static_cast<unsigned>(cfg.grid), 1, 1);
         lc.blockDim = dim3(tsg::kThreads, 1, 1);
         lc.dynamicSmemBytes = static_cast<size_t>(smem);
-        // the cluster-split kernel takes its 2 x 1 cluster shape at launch
+        // the cluster-split kernel takes its cs x 1 cluster shape at launch
         cudaLaunchAttribute cattr{};
         cattr.id = cudaLaunchAttributeClusterDimension;
-        cattr.val.clusterDim.x = 2;
+        cattr.val.clusterDim.x = static_cast<unsigned>(per_cluster);
         cattr.val.clusterDim.y = 1;
         cattr.val.clusterDim.z = 1;
         if (!pair) {
@@ -245,6 +245,7 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.sk_tiles = cfg.stream_k_tiles;
     gp.sk_work = cfg.stream_k_tiles * gp.kblocks;
     gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n, layout);
+    gp.csplit = cs;
     gp.C = nullptr;
     gp.ws = p->ws;
     // stream-K: the owners' partials follow the contributors' (one 128 x
@@ -385,9 +386,9 @@ tsgemm_status_t tsgemm_run(tsgemm_plan_t plan, const void* A, const void* B, voi
     lc.attrs = nullptr;
     lc.numAttrs = 0;
     cudaLaunchAttribute cattr{};
-    if (plan->cfg.cluster_split == 2) {
+    if (plan->cfg.cluster_split >= 2) {
         cattr.id = cudaLaunchAttributeClusterDimension;
-        cattr.val.clusterDim.x = 2;
+        cattr.val.clusterDim.x = static_cast<unsigned>(plan->cfg.cluster_split);
         cattr.val.clusterDim.y = 1;
         cattr.val.clusterDim.z = 1;
         lc.attrs = &cattr;

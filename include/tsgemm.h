@@ -117,13 +117,17 @@ typedef struct {
                                none, 0 the planner's choice. The workspace is
                                then one block_m x block_n fp32 partial per
                                slot. */
-    int32_t cluster_split;  /* 2: the DSMEM split of K (block_m 128, RRR
-                               layout, 16-bit inputs): the two CTAs of a 2 x 1
-                               cluster compute the two halves of every tile's
-                               K range and CTA 1 hands its fp32 accumulator to
-                               CTA 0 through distributed shared memory, chunk
-                               by chunk; no workspace.  Forced only; the
-                               planner reports 1 otherwise. */
+    int32_t cluster_split;  /* 2, 4 or 8: the DSMEM split of K (block_m 128,
+                               RRR layout, 16-bit inputs, at least that many
+                               K slices): the cs CTAs of a cs x 1 cluster
+                               compute cs consecutive parts of every tile's
+                               K range; CTA r receives the fp32 sum of parts
+                               0..r-1 from CTA r - 1 through distributed
+                               shared memory, chunk by chunk, adds its own
+                               and passes it on, and the last CTA stores C
+                               (parts summed in K order); no workspace.
+                               Forced only; the planner reports 1
+                               otherwise. */
 } tsgemm_config_t;
 
 /* Tests only: the first CTA (or CTA pair) skips the first operand load of

@@ -376,7 +376,8 @@ def test_cluster_split_rules(ts):
     # the planner never proposes it by itself
     assert ts.choose_config(1024, 2048, 8192, "bf16", "bf16", 152)["cluster_split"] == 1
     for force, code in [(dict(cluster_split=2, block_m=256), 1), (dict(cluster_split=2, splits=2), 1),
-                        (dict(cluster_split=2, stream_k_tiles=4), 1), (dict(cluster_split=3), 2)]:
+                        (dict(cluster_split=4, stream_k_tiles=4), 1), (dict(cluster_split=3), 2),
+                        (dict(cluster_split=6), 2), (dict(cluster_split=16), 2)]:
         with pytest.raises(ts.TsgemmError) as e:
             ts.choose_config(1024, 2048, 8192, "bf16", "bf16", 152, **force)
         assert e.value.status == code, force
@@ -385,6 +386,23 @@ def test_cluster_split_rules(ts):
         with pytest.raises(ts.TsgemmError) as e:
             ts.choose_config(*args[:6], layout=args[6], cluster_split=2)
         assert e.value.status == code, args
+
+
+@pytest.mark.parametrize("cs", [2, 4, 8])
+def test_cluster_split_sizes(ts, cs):
+    # cs CTAs per cluster, one tile per cluster at a time; every CTA needs a
+    # K slice of its own
+    c = ts.choose_config(1024, 2048, 8192, "bf16", "f32", 152, cluster_split=cs)
+    assert c["cluster_split"] == cs and c["grid"] % cs == 0
+    assert c["grid"] == min(64, 152 // cs) * cs
+    c = ts.choose_config(128, 256, 64 * cs, "bf16", "f32", 152, cluster_split=cs)
+    assert c["grid"] == cs and c["units"] == 1
+    with pytest.raises(ts.TsgemmError) as e:
+        ts.choose_config(128, 256, 64 * cs - 64, "bf16", "f32", 152, cluster_split=cs)
+    assert e.value.status == 2
+    with pytest.raises(ts.TsgemmError) as e:
+        ts.choose_config(128, 256, 8192, "bf16", "f32", cs - 1, cluster_split=cs)
+    assert e.value.status == 2
 
 
 # ---------------------------------------------------------- attention --
