@@ -52,6 +52,15 @@ def test_shapes(dt, causal, B, H, Sq, Sk):
     _check((B, H, Sq, D), (B, H, Sk, D), dt, causal)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Sq,Sk", [(600, 600), (1000, 777), (641, 1024), (700, 650), (513, 1)])
+def test_query_ranges_across_tiles(causal, Sq, Sk):
+    # query ranges that end inside a 128-row tile, inside the second tile
+    # of a CTA, or with a CTA's second tile wholly past the last row; more
+    # queries than keys; a single key
+    _check((1, 2, Sq, D), (1, 2, Sk, D), "bf16", causal, seed=50 + Sq + Sk)
+
+
 def test_causal_rows_without_keys():
     # more queries than keys: the first Sq - Sk rows see no key and are zero
     O, ref = _check((1, 1, 300, D), (1, 1, 200, D), "bf16", True)
