@@ -29,14 +29,17 @@
 //     keep the same running maximum and row sums, and form the same weights
 //     P, which each writes into its own shared memory (128-byte swizzle) as
 //     the A operand of its P V;
-//   * the exchange runs a block ahead: while the softmax works on block j,
-//     block j + 1's partial is already on its way to the partner (two
-//     exchange buffers), and the tensor cores compute block j + 2's partial
-//     scores as soon as the softmax has read block j's (two score buffers).
-// Warps 0-3 run the softmax and epilogue (warp w reads tensor-memory lanes
-// 32 w .. 32 w + 31), warp 4 lane 0 loads CTA 1's rotary part of Q once and
-// streams key blocks through a three-slot ring (optionally asking for later
-// blocks in L2 ahead), warp 5 lane 0 issues the MMAs.  Every wait is
+//   * the exchange has a warpgroup of its own, a thread per head: it reads
+//     each block's partial from tensor memory and writes it into the
+//     partner's exchange buffer (two buffers) while the softmax warpgroup
+//     is still on an earlier block, so the exchange and the softmax overlap;
+//     the tensor cores compute block j + 2's partial scores as soon as both
+//     warpgroups have read block j's (two score buffers).
+// Warps 0-3 run the softmax and epilogue and warps 4-7 the exchange (warp w
+// reads tensor-memory lanes 32 (w mod 4) .. +31), warp 8 lane 0 loads CTA
+// 1's rotary part of Q once and streams key blocks through a three-slot
+// ring (optionally asking for later blocks in L2 ahead), warp 9 lane 0
+// issues the MMAs.  Every wait is
 // bounded in time; a CTA that gives up records a timeout, sets its
 // partner's abort flag, lets its copies and MMAs finish, frees tensor
 // memory and returns.
@@ -57,8 +60,8 @@ constexpr int kN = 64;                  // keys per block
 constexpr int kDL = 512;                // latent (= value) dims
 constexpr int kDR = 64;                 // rotary dims
 constexpr int kVHalf = kDL / 2;         // value columns per CTA
-constexpr int kThreads = 192;           // warps 0-3 softmax, 4 loads, 5 MMAs
-constexpr int kWarpLoad = 4, kWarpMma = 5;
+constexpr int kThreads = 320;           // warps 0-3 softmax, 4-7 exchange, 8 loads, 9 MMAs
+constexpr int kWarpSend = 4, kWarpLoad = 8, kWarpMma = 9;
 constexpr int kSlots = 3;               // key block ring depth
 // a 64-dim column of the 128-byte swizzle: 128 heads or 64 keys x 128 bytes
 constexpr uint32_t kQAtom = kH * 128u;  // 16 KiB
@@ -109,7 +112,7 @@ struct Bars {
     __device__ uint32_t kv_full(int s) const { return b + 8u * (2 + s); }
     __device__ uint32_t kv_empty(int s) const { return b + 8u * (2 + kSlots + s); }
     __device__ uint32_t s_full(int i) const { return b + 8u * (2 + 2 * kSlots + i); }  // partial scores ready
-    __device__ uint32_t s_free(int i) const { return b + 8u * (4 + 2 * kSlots + i); }  // ... read by the softmax
+    __device__ uint32_t s_free(int i) const { return b + 8u * (4 + 2 * kSlots + i); }  // ... read by both warpgroups
     __device__ uint32_t p_full() const { return b + 8u * (6 + 2 * kSlots); }           // P written
     __device__ uint32_t pv_done() const { return b + 8u * (7 + 2 * kSlots); }          // a P V complete
     __device__ uint32_t x_full(int i) const { return b + 8u * (8 + 2 * kSlots + i); }  // partner's partial here
@@ -163,40 +166,38 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
         __syncwarp();
         if (lane == 0) mbar_arrive(bar.qt_full());
     }
-    // Block j's partial scores: read them from score buffer j & 1 (and free
-    // it for block j + 2), keep them in `own`, and write them into the
-    // partner's exchange buffer j & 1 once it has read block j - 2 there.
-    uint32_t own[64];
-    auto send = [&](int j) -> bool {
-        const int i = j & 1;
-        if (!warp_wait(bar.s_full(i), static_cast<uint32_t>(j >> 1) & 1u)) return false;
-        tc_fence_after();
-        tmem_ld_32x32b_x32(trow + kSCol + 64u * i, *reinterpret_cast<uint32_t(*)[32]>(own));
-        tmem_ld_32x32b_x32(trow + kSCol + 64u * i + 32u, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar.s_free(i));
-        if (j >= 2 && !wait_cluster(bar.x_free(i), static_cast<uint32_t>((j - 2) >> 1) & 1u)) return false;
-        const uint32_t dst = mapa_shared(xaddr(i), peer);
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-            st_shared_cluster_v4(dst + c * 2048u, own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
-        mbar_arrive_cluster(bar.x_full(i), peer);
-        return true;
-    };
+    // x_full(i) completes once the partner's kXBytes of block j (i = j & 1)
+    // have landed and this CTA has armed it for that block: blocks 0 and 1
+    // now, block j + 2 once block j has been read out of the buffer
+    if (r == 0) {
+        mbar_arrive_expect_tx(bar.x_full(0), kXBytes);
+        if (p.nblk > 1) mbar_arrive_expect_tx(bar.x_full(1), kXBytes);
+    }
     float m_used = -INFINITY;  // base-2 maximum the weights are taken against
     float l = 0.0f;
-    bool ok = send(0);
+    bool ok = true;
     // the weights' row in the 128-byte swizzle: 16-byte chunk c of row r at
     // r * 128 + ((c ^ (r mod 8)) * 16)
     const uint32_t prow = base + kPOff + static_cast<uint32_t>(r) * 128u;
     for (int j = 0; ok && j < p.nblk; ++j) {
         const int i = j & 1;
+        // this block's own partial (the exchange warpgroup reads it too),
+        // then the partner's, added in
+        if (!warp_wait(bar.s_full(i), static_cast<uint32_t>(j >> 1) & 1u)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        uint32_t own[64];
+        tmem_ld_32x32b_x32(trow + kSCol + 64u * i, *reinterpret_cast<uint32_t(*)[32]>(own));
+        tmem_ld_32x32b_x32(trow + kSCol + 64u * i + 32u, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
+        tmem_ld_wait();
         float f[64];
-        // this block's full scores: own partial + the partner's
 #pragma unroll
         for (int c = 0; c < 64; ++c) f[c] = __uint_as_float(own[c]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.s_free(i));
         if (!wait_cluster(bar.x_full(i), static_cast<uint32_t>(j >> 1) & 1u)) {
             ok = false;
             break;
@@ -209,12 +210,8 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
             f[4 * c + 2] += v.z;
             f[4 * c + 3] += v.w;
         }
+        if (r == 0 && j + 2 < p.nblk) mbar_arrive_expect_tx(bar.x_full(i), kXBytes);  // for block j + 2
         mbar_arrive_cluster(bar.x_free(i), peer);  // the partner may write block j + 2 here
-        // the next block's partial goes out before this block's softmax
-        if (j + 1 < p.nblk && !send(j + 1)) {
-            ok = false;
-            break;
-        }
         // keys past Skv weigh nothing
         const int k0 = j * kN;
         if (k0 + kN > p.Skv) {
@@ -319,6 +316,41 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
     }
 }
 
+// One exchange thread, head row r = 32 quarter + lane: block j's partial
+// scores from score buffer j & 1 into the partner's exchange buffer j & 1,
+// once the partner's softmax has read block j - 2 there.  The stores are
+// asynchronous and complete as transaction bytes on the partner's x_full
+// barrier, which the partner arms (expects kXBytes) once per block.
+__device__ __forceinline__ void send_rows(const MlaParams& p, const Bars& bar, uint32_t tmem, uint32_t base,
+                                          uint32_t peer, int quarter, int lane, const WaitCtl& ctl) {
+    const int r = quarter * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    // exchange buffer i, row r: 16-byte chunk c at + c * 2 KiB
+    const uint32_t xrow = base + kXOff + static_cast<uint32_t>(r) * 16u;
+    for (int j = 0; j < p.nblk; ++j) {
+        const int i = j & 1;
+        int good = 1;
+        if (lane == 0) good = wait_bounded(bar.s_full(i), static_cast<uint32_t>(j >> 1) & 1u, ctl) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, good, 0)) return;
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(trow + kSCol + 64u * i, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld_32x32b_x32(trow + kSCol + 64u * i + 32u, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.s_free(i));
+        // every thread waits itself: it then overwrites only its own row
+        if (j >= 2 && !wait_bounded<true>(bar.x_free(i), static_cast<uint32_t>((j - 2) >> 1) & 1u, ctl)) return;
+        // asynchronous stores that complete as transaction bytes on the
+        // partner's x_full barrier, which the partner arms for every block
+        const uint32_t dst = mapa_shared(xrow + static_cast<uint32_t>(i) * kXBytes, peer);
+        const uint32_t fb = mapa_shared(bar.x_full(i), peer);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) st_async_v4(dst + c * 2048u, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3], fb);
+    }
+}
+
 template <bool kF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_sm103(const __grid_constant__ CUtensorMap tmQpe, const __grid_constant__ CUtensorMap tmKV,
@@ -351,8 +383,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar.s_full(i), 1);
-            mbar_init(bar.s_free(i), 4);    // every softmax warp
-            mbar_init(bar.x_full(i), 128);  // every softmax thread of the partner
+            mbar_init(bar.s_free(i), 8);    // every softmax and exchange warp
+            mbar_init(bar.x_full(i), 1);    // armed by this CTA; the partner's bytes complete it
             mbar_init(bar.x_free(i), 128);
         }
         mbar_init(bar.p_full(), 4);
@@ -373,9 +405,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     ctl.peer_abort[ctl.npeers++] = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), peer);
 
-    if (warp < 4) {
+    if (warp < kWarpSend) {
         // ---------------------------------------- softmax and epilogue --
         softmax_rows<kF16>(p, bar, tmem, base, peer, b, h0, warp, lane, ctl);
+    } else if (warp < kWarpLoad) {
+        // ---------------------------------------------------- exchange --
+        send_rows(p, bar, tmem, base, peer, warp - kWarpSend, lane, ctl);
     } else if (warp == kWarpLoad) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
@@ -466,13 +501,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 umma_commit(bar.kv_empty(j % kSlots));  // the block's scores and values are read
                 return true;
             };
-            // S_0, S_1; then per block j: S_{j+2} (once the softmax has read
-            // S_j), P V_j (once it has written P_j)
+            // S_0, S_1; then per block j: P V_j (once the softmax has written
+            // P_j), which frees the block's ring slot for block j + 3, then
+            // S_{j+2} (once both warpgroups have read S_j and block j + 2 is
+            // in) -- P V_j never waits for a later block's copy
             if (ok) ok = issue_s(0);
             if (ok && p.nblk > 1) ok = issue_s(1);
             for (int j = 0; ok && j < p.nblk; ++j) {
-                if (j + 2 < p.nblk) ok = issue_s(j + 2);
-                if (ok) ok = issue_pv(j);
+                ok = issue_pv(j);
+                if (ok && j + 2 < p.nblk) ok = issue_s(j + 2);
             }
             // every MMA issued above completes before tensor memory is freed
             umma_commit(bar.drain());

@@ -44,6 +44,17 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr_cluster, uint
                  : "memory");
 }
 
+// 16 bytes into (possibly another CTA's) shared memory at a shared::cluster
+// address, completing as 16 transaction bytes on the mbarrier at
+// `bar_cluster` (in the same CTA as the data): no release, no arrival.
+__device__ __forceinline__ void st_async_v4(uint32_t addr_cluster, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr_cluster),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr_cluster, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
 }
