@@ -39,7 +39,9 @@
 // reads tensor-memory lanes 32 (w mod 4) .. +31), warp 8 lane 0 loads CTA
 // 1's rotary part of Q once and streams key blocks through a three-slot
 // ring (optionally asking for later blocks in L2 ahead), warp 9 lane 0
-// issues the MMAs.  Every wait is
+// issues the MMAs, and warp 10 lane 0 relays to the partner that the
+// softmax warps have read its partial (the one cross-CTA release of the
+// exchange).  Every wait is
 // bounded in time; a CTA that gives up records a timeout, sets its
 // partner's abort flag, lets its copies and MMAs finish, frees tensor
 // memory and returns.
@@ -60,8 +62,8 @@ constexpr int kN = 64;                  // keys per block
 constexpr int kDL = 512;                // latent (= value) dims
 constexpr int kDR = 64;                 // rotary dims
 constexpr int kVHalf = kDL / 2;         // value columns per CTA
-constexpr int kThreads = 320;           // warps 0-3 softmax, 4-7 exchange, 8 loads, 9 MMAs
-constexpr int kWarpSend = 4, kWarpLoad = 8, kWarpMma = 9;
+constexpr int kThreads = 352;           // warps 0-3 softmax, 4-7 exchange, 8 loads, 9 MMAs, 10 relay
+constexpr int kWarpSend = 4, kWarpLoad = 8, kWarpMma = 9, kWarpRelay = 10;
 constexpr int kSlots = 3;               // key block ring depth
 // a 64-dim column of the 128-byte swizzle: 128 heads or 64 keys x 128 bytes
 constexpr uint32_t kQAtom = kH * 128u;  // 16 KiB
@@ -75,8 +77,8 @@ constexpr uint32_t kKOff = kPOff + kQAtom;
 constexpr uint32_t kXOff = kKOff + kSlots * kSlotBytes;      // two exchange buffers
 constexpr uint32_t kBarOff = kXOff + 2 * kXBytes;
 // barriers: q_full, qt_full, kv_full[3], kv_empty[3], s_full[2], s_free[2],
-// p_full, pv_done, x_full[2], x_free[2], drain
-constexpr int kNumBars = 2 + 2 * kSlots + 4 + 2 + 4 + 1;
+// p_full, pv_done, x_full[2], x_free[2], drain, x_read[2]
+constexpr int kNumBars = 2 + 2 * kSlots + 4 + 2 + 4 + 1 + 2;
 constexpr uint32_t kMiscOff = kBarOff + 8u * kNumBars;
 constexpr uint32_t kSmemBytes = 1024u + kMiscOff + 16u;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -118,6 +120,7 @@ struct Bars {
     __device__ uint32_t x_full(int i) const { return b + 8u * (8 + 2 * kSlots + i); }  // partner's partial here
     __device__ uint32_t x_free(int i) const { return b + 8u * (10 + 2 * kSlots + i); } // partner read ours
     __device__ uint32_t drain() const { return b + 8u * (12 + 2 * kSlots); }
+    __device__ uint32_t x_read(int i) const { return b + 8u * (13 + 2 * kSlots + i); } // we read the partner's
 };
 
 // One softmax thread: query head row r = 32 quarter + lane of the CTA's 128
@@ -211,7 +214,10 @@ __device__ __forceinline__ void softmax_rows(const MlaParams& p, const Bars& bar
             f[4 * c + 3] += v.w;
         }
         if (r == 0 && j + 2 < p.nblk) mbar_arrive_expect_tx(bar.x_full(i), kXBytes);  // for block j + 2
-        mbar_arrive_cluster(bar.x_free(i), peer);  // the partner may write block j + 2 here
+        // this warp has read the partner's partial: the relay thread tells
+        // the partner, which may then write block j + 2 here
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.x_read(i));
         // keys past Skv weigh nothing
         const int k0 = j * kN;
         if (k0 + kN > p.Skv) {
@@ -385,7 +391,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(bar.s_full(i), 1);
             mbar_init(bar.s_free(i), 8);    // every softmax and exchange warp
             mbar_init(bar.x_full(i), 1);    // armed by this CTA; the partner's bytes complete it
-            mbar_init(bar.x_free(i), 128);
+            mbar_init(bar.x_free(i), 1);    // the partner's relay thread
+            mbar_init(bar.x_read(i), 4);    // every softmax warp
         }
         mbar_init(bar.p_full(), 4);
         mbar_init(bar.pv_done(), 1);
@@ -411,6 +418,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp < kWarpLoad) {
         // ---------------------------------------------------- exchange --
         send_rows(p, bar, tmem, base, peer, warp - kWarpSend, lane, ctl);
+    } else if (warp == kWarpRelay) {
+        // ----------------------------------------------------- relay --
+        // A cluster-scope release arrive costs its thread about a
+        // microsecond; one thread here takes it for the softmax warps,
+        // which only arrive on the local x_read barrier.  Their reads of
+        // the partner's partial happen before this thread's release, which
+        // covers them.
+        if (lane == 0) {
+            for (int j = 0; j < p.nblk; ++j) {
+                const int i = j & 1;
+                if (!wait_bounded(bar.x_read(i), static_cast<uint32_t>(j >> 1) & 1u, ctl)) break;
+                mbar_arrive_cluster(bar.x_free(i), peer);
+            }
+        }
+        __syncwarp();
     } else if (warp == kWarpLoad) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
