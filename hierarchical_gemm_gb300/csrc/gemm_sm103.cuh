@@ -465,30 +465,37 @@ __device__ __forceinline__ void drain_unit(const GemmParams& p, const CUtensorMa
 // a_dst, B columns [col, col + kBCols) at b_dst, in the layout's operand
 // order.  kRemote: the completion goes to a barrier of the peer CTA (the
 // pair's leader), which needs the cta_group::2 form of the copy.
+template <bool kRemote>
+__device__ __forceinline__ void tma_ld(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0, int32_t c1) {
+    if constexpr (kRemote)
+        tma_load_2d_pair(dst, m, bar, c0, c1);
+    else
+        tma_load_2d(dst, m, bar, c0, c1);
+}
+template <int kLayout, int kBCols, bool kRemote, bool kF8 = false>
+__device__ __forceinline__ void load_b(uint32_t b_dst, const CUtensorMap* tmB, uint32_t bar, int kb, int32_t col) {
+    static_assert(!kF8 || b_kmajor(kLayout), "8-bit operands are K-major");
+    constexpr int kSK = slice_k<kF8>();
+    if constexpr (b_kmajor(kLayout)) {
+        tma_ld<kRemote>(b_dst, tmB, bar, kb * kSK, col);  // one 128-byte (K) x kBCols (N) box
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBCols / 64; ++j) tma_ld<kRemote>(b_dst + j * 8192u, tmB, bar, col + j * 64, kb * kBK);
+    }
+}
 template <int kLayout, int kBCols, bool kRemote, bool kF8 = false>
 __device__ __forceinline__ void load_slice(uint32_t a_dst, uint32_t b_dst, const CUtensorMap* tmA,
                                            const CUtensorMap* tmB, uint32_t bar, int kb, int32_t row,
                                            int32_t col) {
     static_assert(!kF8 || (a_kmajor(kLayout) && b_kmajor(kLayout)), "8-bit operands are K-major");
-    auto ld = [&](uint32_t dst, const CUtensorMap* m, int32_t c0, int32_t c1) {
-        if constexpr (kRemote)
-            tma_load_2d_pair(dst, m, bar, c0, c1);
-        else
-            tma_load_2d(dst, m, bar, c0, c1);
-    };
     constexpr int kSK = slice_k<kF8>();
     if constexpr (a_kmajor(kLayout)) {
-        ld(a_dst, tmA, kb * kSK, row);  // one 128-byte (K) x 128 (M) box
+        tma_ld<kRemote>(a_dst, tmA, bar, kb * kSK, row);  // one 128-byte (K) x 128 (M) box
     } else {
-        ld(a_dst, tmA, row, kb * kBK);  // two 64 (M) x 64 (K) boxes
-        ld(a_dst + 8192u, tmA, row + 64, kb * kBK);
+        tma_ld<kRemote>(a_dst, tmA, bar, row, kb * kBK);  // two 64 (M) x 64 (K) boxes
+        tma_ld<kRemote>(a_dst + 8192u, tmA, bar, row + 64, kb * kBK);
     }
-    if constexpr (b_kmajor(kLayout)) {
-        ld(b_dst, tmB, kb * kSK, col);  // one 128-byte (K) x kBCols (N) box
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBCols / 64; ++j) ld(b_dst + j * 8192u, tmB, col + j * 64, kb * kBK);
-    }
+    load_b<kLayout, kBCols, kRemote, kF8>(b_dst, tmB, bar, kb, col);
 }
 
 // The four MMAs of one K-slice held at a_addr / b_addr: 16-deep kind::f16

@@ -28,15 +28,21 @@
 
 namespace tsg {
 
+// BN = 512 (a "wide" tile): the tile's two 256-column halves are the two
+// accumulators of tensor memory (so one tile fills it and is not
+// double-buffered), each K slice's A feeds two N = 256 MMAs, and each CTA
+// holds two 128-column pieces of B, one per half.
 template <int BN>
 struct PairShape {
-    static_assert(BN == 128 || BN == 256, "pair tiles are 256 x 128 or 256 x 256");
+    static_assert(BN == 128 || BN == 256 || BN == 512, "pair tiles are 256 x 128, 256 x 256 or 256 x 512");
+    static constexpr bool kWide = BN == 512;
     static constexpr uint32_t kABytes = kBM * kBK * 2;      // this CTA's 128 rows: 16 KiB
     static constexpr uint32_t kBCols = BN / 2;              // this CTA's B columns
+    static constexpr uint32_t kPieceCols = kWide ? 128 : kBCols;  // B columns of one MMA's half
     static constexpr uint32_t kBBytes = kBCols * kBK * 2;   // kBCols / 64 boxes of 8 KiB
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kAccCols = BN <= 128 ? 128 : 256;
-    static constexpr uint32_t kTmemCols = 2 * kAccCols;
+    static constexpr uint32_t kTmemCols = kWide ? 512 : 2 * kAccCols;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
@@ -79,7 +85,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);                    // the leader's commit
-            mbar_init(tempty_bar(a), 2 * kEpiWarps);  // every epilogue warp of the pair
+            // every epilogue warp of the pair (wide tiles: accumulator a is
+            // drained by warpgroup a of each CTA)
+            mbar_init(tempty_bar(a), PS::kWide ? kEpiWarps : 2 * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -124,15 +132,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     } else {
                         const uint32_t a_dst = base + stage * PS::kStageBytes;
                         const int32_t arow = un.tm * (2 * kBM) + static_cast<int32_t>(half) * kBM;
-                        const int32_t bcol = un.tn * BN + static_cast<int32_t>(half) * PS::kBCols;
+                        // (wide tiles: this CTA's piece of each 256-column half)
+                        const int32_t bcol = un.tn * BN + static_cast<int32_t>(half) * PS::kPieceCols;
+                        constexpr uint32_t kPieceBytes = PS::kPieceCols * kBK * 2;
                         if (leader) {
                             mbar_arrive_expect_tx(full_bar(stage), 2u * PS::kStageBytes);
-                            load_slice<kLayout, PS::kBCols, false, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
-                                                                        full_bar(stage), kb, arow, bcol);
+                            load_slice<kLayout, PS::kPieceCols, false, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                            full_bar(stage), kb, arow, bcol);
+                            if constexpr (PS::kWide)
+                                load_b<kLayout, PS::kPieceCols, false, kF8>(a_dst + PS::kABytes + kPieceBytes, &tmB,
+                                                                            full_bar(stage), kb, bcol + 256);
                         } else {
-                            load_slice<kLayout, PS::kBCols, true, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
-                                                                       mapa_shared(full_bar(stage), 0u), kb, arow,
-                                                                       bcol);
+                            const uint32_t fb = mapa_shared(full_bar(stage), 0u);
+                            load_slice<kLayout, PS::kPieceCols, true, kF8>(a_dst, a_dst + PS::kABytes, &tmA, &tmB,
+                                                                           fb, kb, arow, bcol);
+                            if constexpr (PS::kWide)
+                                load_b<kLayout, PS::kPieceCols, true, kF8>(a_dst + PS::kABytes + kPieceBytes, &tmB,
+                                                                           fb, kb, bcol + 256);
                         }
                         outstanding |= 1u << stage;
                         out_parity = (out_parity & ~(1u << stage)) | (phase << stage);
@@ -161,7 +177,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int64_t j = 0; ok; ++j) {
                 Unit un;
                 if (!unit_at(p, cluster_id, nclusters, j, un)) break;
+                // a wide tile takes both accumulators, whose halves the two
+                // epilogue warpgroups free separately
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, ctl)) break;
+                if (PS::kWide && !wait_bounded(tempty_bar(1), acc_phase ^ 1u, ctl)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * PS::kAccCols;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
@@ -175,6 +194,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint32_t a_addr = base + stage * PS::kStageBytes;
                         mma_slice<kLayout, 2, kF8>(d_tmem, a_addr, a_addr + PS::kABytes, p.idesc,
                                               kb > un.kb0 ? 1u : 0u);
+                        if constexpr (PS::kWide)  // the tile's second 256 columns
+                            mma_slice<kLayout, 2, kF8>(d_tmem + 256u, a_addr,
+                                                       a_addr + PS::kABytes + PS::kPieceCols * kBK * 2, p.idesc,
+                                                       kb > un.kb0 ? 1u : 0u);
                         // slot free in both CTAs, whose slots these MMAs read
                         umma_commit_pair(empty_bar(stage), 0x3u);
                     }
@@ -185,7 +208,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 umma_commit_pair(tfull_bar(acc), 0x3u);
-                if (++acc == 2) {
+                if (PS::kWide) {
+                    acc_phase ^= 1u;  // (acc stays 0: one tile at a time)
+                } else if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -231,10 +256,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PS::kAccCols;
             // workspace tile and counter of this CTA's 128-row half
             const int64_t wh = un.slot * 2 + half;
-            const int a_now = acc;
+            // (wide tiles: warpgroup e/4 drains accumulator e/4, the tile's
+            // columns [256 (e/4), 256 (e/4) + 256), which are TMEM columns
+            // of the same numbers)
+            const int a_now = PS::kWide ? (e >> 2) : acc;
             drain_unit<BN, kOut>(p, &tmC, out, un, tbase, row0, row_local, wh, aux, c_begin,
                                  [&]() { release_acc(a_now); });
-            if (++acc == 2) {
+            if (PS::kWide) {
+                acc_phase ^= 1u;
+            } else if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }

@@ -32,6 +32,7 @@ int64_t kernel_2sm_smem_bytes(int block_n, int out_kind, int stages) {
     switch (block_n) {
         case 128: return pick(std::integral_constant<int, 128>{});
         case 256: return pick(std::integral_constant<int, 256>{});
+        case 512: return pick(std::integral_constant<int, 512>{});
         default: return -1;
     }
 }

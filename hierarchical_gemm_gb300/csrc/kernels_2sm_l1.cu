@@ -22,6 +22,7 @@ const void* kernel_2sm_layout1(int block_n, int out_kind) {
     switch (block_n) {
         case 128: return pick<128>(out_kind);
         case 256: return pick<256>(out_kind);
+        case 512: return pick<512>(out_kind);
         default: return nullptr;
     }
 }

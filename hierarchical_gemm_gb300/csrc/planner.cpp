@@ -224,9 +224,13 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     tsgemm_config_t f{};
     if (force) f = *force;
     if (f.block_m != 0 && f.block_m != 128 && f.block_m != 256) return TSGEMM_ERR_UNSUPPORTED;
-    if (f.block_n != 0 && (f.block_n % 64 != 0 || f.block_n < 64 || f.block_n > 256))
+    // (block_n 512: the 256 x 512 pair tile, forced only, whole tiles only)
+    const bool wide = f.block_n == 512;
+    if (f.block_n != 0 && !wide && (f.block_n % 64 != 0 || f.block_n < 64 || f.block_n > 256))
         return TSGEMM_ERR_UNSUPPORTED;
-    if (f.block_m == 256 && f.block_n != 0 && f.block_n != 128 && f.block_n != 256)
+    if (f.block_m == 256 && f.block_n != 0 && f.block_n != 128 && f.block_n != 256 && !wide)
+        return TSGEMM_ERR_UNSUPPORTED;
+    if (wide && (f.block_m != 256 || f.splits > 1 || f.split_tiles > 0 || f.cluster_split > 1))
         return TSGEMM_ERR_UNSUPPORTED;
     if (f.block_m == 256 && num_sms < 2) return TSGEMM_ERR_UNSUPPORTED;
     if (f.splits < 0 || f.stages < 0 || f.group_m < 0 || f.grid < 0 || f.timeout_ms < 0)
@@ -261,12 +265,13 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     int64_t best_st = 0, best_sk = 0;
     double best = 0;
     const int bms[2] = {256, 128};  // pairs first: ties go to the pair
-    const int bns[4] = {256, 192, 128, 64};
+    const int bns[5] = {512, 256, 192, 128, 64};
     for (int bm : bms) {
         if (f.block_m && bm != f.block_m) continue;
         if (bm == 256 && num_sms < 2) continue;
         for (int bn : bns) {
-            if (bm == 256 && bn != 128 && bn != 256) continue;
+            if (bn == 512 && !wide) continue;
+            if (bm == 256 && bn != 128 && bn != 256 && bn != 512) continue;
             if (f.block_n && bn != f.block_n) continue;
             if (!f.block_n && bn > n_pad && bn != 64 && !(bm == 256 && bn == 128)) continue;
             const int64_t slots = num_sms / (bm / kBM);
@@ -275,6 +280,20 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
                                       : static_cast<int>(std::min<int64_t>(
                                             std::min<int64_t>(kMaxSplits, slots), std::max<int64_t>(1, kblocks / 4)));
             const int smin = f.splits ? f.splits : 1;
+            if (bn == 512) {
+                // whole tiles (no split), stream-K only when forced
+                const int64_t sk = f.stream_k_tiles > 0 ? f.stream_k_tiles : 0;
+                if (sk > tiles || (sk > 0 && sk * kblocks < slots)) return TSGEMM_ERR_UNSUPPORTED;
+                const Estimate e = sk ? estimate_sk(M, N, K, dtype_in, dtype_out, bm, bn, sk, num_sms)
+                                      : estimate(M, N, K, dtype_in, dtype_out, bm, bn, 1, 0, num_sms);
+                best = e.cycles;
+                best_bm = bm;
+                best_bn = bn;
+                best_s = 1;
+                best_st = 0;
+                best_sk = sk;
+                continue;
+            }
             // stream-K: the tail wave, or the tail and one full wave before it
             // (so that whole-tile rounds stay whole), or a forced count
             if (f.stream_k_tiles != -1 && smin == 1 && !f.split_tiles) {
@@ -331,6 +350,28 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
         }
     }
     if (best_bn == 0) return TSGEMM_ERR_UNSUPPORTED;
+
+    // 256 x 512 pair tiles when the whole-tile schedule of them has at
+    // least four rounds and a last round at least two thirds full: a K
+    // slice's A then feeds two N = 256 MMAs (a quarter fewer operand bytes
+    // per flop), which pays while the tile's epilogue, no longer overlapped
+    // with the next tile, is a small part of a round and no stream-K is
+    // needed (a stream-K reduction of 256 x 512 partials costs more than
+    // it balances).  RRR and RCR layouts, as the planner's own choice only.
+    if (!f.block_m && !f.block_n && !f.splits && !f.split_tiles && f.stream_k_tiles <= 0 && best_bm == 256 &&
+        (layout == TSGEMM_LAYOUT_RRR || layout == TSGEMM_LAYOUT_RCR) && N >= 512 &&
+        (!f.stages || f.stages <= max_stages_for(256, 512, dtype_out))) {
+        const int64_t wide_tiles = ceil_div(M, 256) * ceil_div(N, 512);
+        const int64_t wide_slots = (f.grid ? f.grid : num_sms) / 2;
+        const int64_t rounds = wide_slots > 0 ? wide_tiles / wide_slots : 0;
+        const int64_t rem = wide_slots > 0 ? wide_tiles % wide_slots : 0;
+        if (rounds >= 4 && (rem == 0 || 3 * rem >= 2 * wide_slots)) {
+            best_bn = 512;
+            best_s = 1;
+            best_st = 0;
+            best_sk = 0;
+        }
+    }
 
     tsgemm_config_t c{};
     c.block_m = best_bm;

@@ -244,7 +244,8 @@ tsgemm_status_t tsgemm_plan_ex(tsgemm_plan_t* out, int64_t M, int64_t N, int64_t
     gp.full_tiles = ((M + cfg.block_m - 1) / cfg.block_m) * gp.tiles_n - cfg.split_tiles - cfg.stream_k_tiles;
     gp.sk_tiles = cfg.stream_k_tiles;
     gp.sk_work = cfg.stream_k_tiles * gp.kblocks;
-    gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n, layout);
+    // (a 256 x 512 pair tile is two N = 256 MMAs per K step)
+    gp.idesc = make_idesc(dtype_in, cfg.block_m, cfg.block_n == 512 ? 256 : cfg.block_n, layout);
     gp.csplit = cs;
     gp.C = nullptr;
     gp.ws = p->ws;
@@ -309,11 +310,13 @@ static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* 
     // dimension: 64 16-bit or 128 8-bit elements.
     //   A stored M x K: 128 B (K) x 128 (M) boxes;  A stored K x M: 64 (M) x 64 (K)
     //   B stored K x N: 64 (N) x 64 (K) boxes;      B stored N x K: 128 B (K) x
-    //   the CTA's columns (N) -- block_n, or block_n / 2 for a CTA pair
+    //   the CTA's columns (N) -- block_n, or block_n / 2 for a CTA pair, or
+    //   128 for a 256 x 512 pair tile (two pieces, one per MMA half)
     // (8-bit operands are always stored K-major, the first form of each).
     const cuuint32_t kbox = static_cast<cuuint32_t>(128 / eb);
     const bool ak = tsg::a_kmajor(p->layout), bk = tsg::b_kmajor(p->layout);
-    const cuuint32_t b_cols = static_cast<cuuint32_t>(p->cfg.block_m == 256 ? p->cfg.block_n / 2 : p->cfg.block_n);
+    const cuuint32_t b_cols = static_cast<cuuint32_t>(
+        p->cfg.block_m == 256 ? (p->cfg.block_n == 512 ? 128 : p->cfg.block_n / 2) : p->cfg.block_n);
     const bool ok_a = ak ? tile_map(&p->tmA, A, p->K, p->M, kbox, 128) : tile_map(&p->tmA, A, p->M, p->K, 64, 64);
     const bool ok_b = bk ? tile_map(&p->tmB, B, p->K, p->N, kbox, b_cols) : tile_map(&p->tmB, B, p->N, p->K, 64, 64);
     return ok_a && ok_b ? TSGEMM_OK : TSGEMM_ERR_CUDA;

@@ -94,7 +94,13 @@ typedef enum {
  * 0 is chosen by the planner; a non-zero field forces that value. */
 typedef struct {
     int32_t block_m;      /* rows of C per MMA tile: 128 (one SM) or 256 (SM pair) */
-    int32_t block_n;      /* columns of C per tile: 64, 128, 192 or 256 */
+    int32_t block_n;      /* columns of C per tile: 64, 128, 192 or 256; 512
+                             for a CTA pair (block_m 256) whose tile's two
+                             256-column halves fill tensor memory: each K
+                             slice's A feeds two N = 256 MMAs.  The planner
+                             takes 512 for whole-tile schedules of at least
+                             four rounds (RRR, RCR); forced, it runs whole
+                             tiles or stream-K, never a split. */
     int32_t splits;       /* K split factor S of the split tiles (1 = no split) */
     int32_t stages;       /* depth of the shared-memory operand ring */
     int32_t group_m;      /* tile rows per raster group (L2 reuse) */

@@ -97,7 +97,7 @@ def test_planner_invariants(ts, shape, sms):
     c = ts.choose_config(M, N, K, din, dout, sms)
     bm, bn = c["block_m"], c["block_n"]
     tiles = _ceil(M, bm) * _ceil(N, bn)
-    assert (bm, bn) in [(128, 64), (128, 128), (128, 192), (128, 256), (256, 128), (256, 256)]
+    assert (bm, bn) in [(128, 64), (128, 128), (128, 192), (128, 256), (256, 128), (256, 256), (256, 512)]
     st = c["split_tiles"]
     sk = c["stream_k_tiles"]
     per = bm // 128  # CTAs per unit
@@ -120,6 +120,34 @@ def test_planner_invariants(ts, shape, sms):
     # the ring is as deep as the shared memory allows
     assert smem + stage > 232448 or c["stages"] == 16
     assert c["timeout_ms"] == 1000
+
+
+def test_wide_pair_tiles_rule(ts):
+    # 256 x 512 pair tiles: chosen with at least four whole rounds and a last
+    # round at least two thirds full, never split, never stream-K
+    for M, N, K, din, lay in [(8192, 8192, 8192, "bf16", "rrr"), (16384, 16384, 8192, "bf16", "rrr"),
+                              (16384, 16384, 8192, "e4m3", "rcr"), (16384, 16384, 8192, "bf16", "rcr")]:
+        c = ts.choose_config(M, N, K, din, "bf16", 152, layout=lay)
+        assert (c["block_m"], c["block_n"]) == (256, 512), (M, N, K, din, lay)
+        assert c["splits"] == 1 and c["stream_k_tiles"] == 0 and c["workspace_bytes"] == 0
+        assert c["stages"] == 4 and c["grid"] == 152 and c["units"] == _ceil(M, 256) * _ceil(N, 512)
+    # too few rounds, a thin last round, the K x M layouts, forced fields
+    for M, N, K, lay, force in [(4096, 4096, 4096, "rrr", {}), (8192, 8704, 8192, "rrr", {}),
+                                (8192, 8192, 8192, "crr", {}), (8192, 8192, 8192, "rrr", dict(stages=6)),
+                                (8192, 8192, 8192, "rrr", dict(stream_k_tiles=36)),
+                                (8192, 8192, 8192, "rrr", dict(block_n=256))]:
+        c = ts.choose_config(M, N, K, "bf16", "bf16", 152, layout=lay, **force)
+        assert c["block_n"] != 512, (M, N, K, lay, force)
+    # forced: whole tiles or stream-K, pairs only, no split
+    c = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, block_m=256, block_n=512)
+    assert c["block_n"] == 512 and c["stream_k_tiles"] == 0 and c["units"] == 128
+    c = ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, block_m=256, block_n=512, stream_k_tiles=52)
+    assert c["stream_k_tiles"] == 52 and c["workspace_bytes"] == 2 * 76 * 256 * 512 * 4
+    for force in [dict(block_m=128, block_n=512), dict(block_m=256, block_n=512, splits=2),
+                  dict(block_n=512)]:
+        with pytest.raises(ts.TsgemmError) as e:
+            ts.choose_config(4096, 4096, 4096, "bf16", "bf16", 152, **force)
+        assert e.value.status == 2, force
 
 
 def test_planner_choices_for_the_workloads(ts):
