@@ -3,48 +3,47 @@
 //
 // It is the per-device block of the FlashMLA example of the TileScale
 // README (section "Example of FlashMLA"), laid out for sm_103a:
-//   * a CTA owns two tiles of 128 query rows (A and B) of one (batch, head);
-//     their Q is loaded once by TMA into shared memory (128-byte swizzle);
-//   * key and value blocks of 128 rows stream through rings of their own: a
-//     K slot is free once both tiles' S = Q K^T have read it, a V slot once
-//     both tiles' O += P V have;
-//   * per tile, S_j = Q K_j^T is computed by tcgen05.mma into the tile's
-//     tensor-memory score buffer (acc_s of the example); one warpgroup per
-//     tile, a thread per query row, reads its row of S_j, keeps the running
-//     maximum (scores_max) and row sum (logsum) in base-2 units, writes
-//     P_j = 2^(t - m) rounded to the 16-bit input format (acc_s_cast) back
-//     into the score buffer, two weights per 32-bit column, and, when its
-//     maximum has grown, rescales its row of the output accumulator
-//     (scores_scale);
-//   * O += P_j V_j is computed by tcgen05.mma with P read from tensor memory
-//     (A operand) and V from shared memory into the tile's tensor-memory
-//     accumulator (acc_o); at the end each thread divides its row by the row
-//     sum and stores it.
-// The two tiles ping-pong: while one tile's warpgroup computes its softmax,
-// the tensor cores run the other tile's P V and next S, so neither the
-// tensor cores nor the exponential units wait for each other.  (The
-// example splits one tile's acc_s between two warpgroups and all-gathers
-// it; two tiles need no exchange between the warpgroups at all.)
-// The rescale is lazy: a row keeps its old maximum until the new one exceeds
-// it by 2^8, so the output accumulator is read and rewritten only when a
-// row's scores jump; the weights then stay below 2^8, well inside the
-// 16-bit formats, and the final division uses the same maximum as every
-// weight, so the result is the same softmax.
+//   * a CTA owns one tile of 128 query rows of one (batch, head); its Q is
+//     loaded once by TMA into shared memory (128-byte swizzle);
+//   * key and value blocks of 128 rows stream through rings of their own;
+//   * S_j = Q K_j^T is computed by tcgen05.mma into one of two
+//     tensor-memory score buffers (acc_s of the example), block j into
+//     buffer j mod 2, so that S_{j+1} is ready while the softmax of block j
+//     runs;
+//   * as in the example, two warpgroups share the tile's score rows: each
+//     owns one half of every block's 128 keys (a thread per query row and
+//     half).  A warpgroup reads its half of the row of S_j, keeps its own
+//     running maximum (scores_max) and row sum (logsum) in base-2 units,
+//     and writes P_j = 2^(t - m) rounded to the 16-bit input format
+//     (acc_s_cast) over the scores it has read, two weights per 32-bit
+//     column;
+//   * each half has an output accumulator of its own in tensor memory
+//     (acc_o): O_h += P_j[:, half h] V_j[half h, :] by tcgen05.mma, P read
+//     from tensor memory (A operand), V from shared memory.  Instead of the
+//     example's all-gather of the block maximum, the halves keep separate
+//     maxima and combine once, at the end: with m = max(m_0, m_1),
+//     O = (2^(m_0 - m) O_0 + 2^(m_1 - m) O_1) / (2^(m_0 - m) l_0 + 2^(m_1 - m) l_1),
+//     the same softmax, and no exchange between the warpgroups per block.
+// With two score buffers the tensor cores compute S_{j+2} and the P V of
+// block j while the softmax of block j + 1 runs: a warpgroup's next block
+// never waits for its own P V.
+// The rescale is lazy: a half keeps its old maximum until the new one
+// exceeds it by 2^8, so its output accumulator is read and rewritten only
+// when a row's scores jump; the weights then stay below 2^8, well inside
+// the 16-bit formats.
 //
-// Warp roles, in three warpgroups: warps 0-3 run tile A's softmax and
-// epilogue, warps 4-7 tile B's (warp w reads tensor-memory lanes
-// 32 (w mod 4) .. +31); in the third, warp 8 lane 0 loads Q and the key
-// blocks, warp 9 lane 0 issues the MMAs, warp 10 lane 0 loads the value
-// blocks and warp 11 idles.  The third warpgroup gives most of its
-// registers to the other two (setmaxnreg): a softmax thread holds its whole
-// row of 128 scores.  Every wait is bounded in time (WaitCtl); a CTA that
-// gives up records a timeout, lets its copies and MMAs finish, frees tensor
-// memory and returns.
+// Warp roles: warps 0-3 run the first key half's softmax, warps 4-7 the
+// second's (warp w reads tensor-memory lanes 32 (w mod 4) .. +31); warp 8
+// lane 0 loads Q and the key blocks, warp 9 lane 0 issues the MMAs, warp 10
+// lane 0 loads the value blocks and warp 11 idles.  Every wait is bounded in
+// time (WaitCtl); a CTA that gives up records a timeout, lets its copies and
+// MMAs finish, frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "attn_common.h"
 #include "ptx.cuh"
@@ -54,37 +53,32 @@ namespace tsg {
 namespace attn {
 
 constexpr int kBQ = 128;                // query rows per tile (TMEM lanes)
-constexpr int kTiles = 2;               // query tiles per CTA
 constexpr int kBKV = 128;               // keys per block
+constexpr int kHalf = kBKV / 2;         // keys per softmax warpgroup
 constexpr int kD = 128;                 // head dimension
 constexpr int kThreads = 384;           // two softmax warpgroups; producers and MMA issuer
 constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
-// registers per thread after the split: 256 softmax threads at kRegsSoftmax
-// and 128 others at kRegsOther may not exceed what the CTA was launched with
-// (384 x the kernel's register count; the host checks this before a launch)
-constexpr int kRegsSoftmax = 208, kRegsOther = 64;
-constexpr int kRegPool = 256 * kRegsSoftmax + 128 * kRegsOther;
 constexpr uint32_t kAtom = 128u * 128u; // 128 rows x 128 bytes: one swizzle atom column
 constexpr uint32_t kTile = 2u * kAtom;  // 128 rows x 128 16-bit elements
-constexpr int kKSlots = 3;              // key ring depth
+constexpr int kKSlots = 2;              // key ring depth (one slot per score buffer)
 constexpr int kVSlots = 2;              // value ring depth
-constexpr uint32_t kQOff = 0;           // Q of tile A, then tile B
-constexpr uint32_t kKOff = kTiles * kTile;
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kKOff = kTile;
 constexpr uint32_t kVOff = kKOff + kKSlots * kTile;
 constexpr uint32_t kBarOff = kVOff + kVSlots * kTile;
-// barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], and per
-// tile s_full, p_full, p_free; drain
-constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + 3 * kTiles + 1;
+// barriers: q_full, k_full[2], v_full[2], v_empty[2], s_full[2],
+// p_full[2], o_final, drain
+constexpr int kNumBars = 1 + kKSlots + 2 * kVSlots + 2 + 2 + 2;
 constexpr uint32_t kMiscOff = kBarOff + 8u * kNumBars;
 constexpr uint32_t kSmemBytes = 1024u + kMiscOff + 16u;
-constexpr uint32_t kTmemCols = 512;     // S of tile t at columns 128 t, O of tile t at 256 + 128 t
+constexpr uint32_t kTmemCols = 512;     // S buffers at columns 0 and 128, O_0 at 256, O_1 at 384
 constexpr uint32_t kOCol = 256;
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct AttnParams {
     int32_t B, H, Sq, Sk;
-    int32_t nq;           // CTAs (pairs of query tiles) per (batch, head)
+    int32_t nq;           // CTAs (query tiles) per (batch, head)
     int32_t group;        // causal: (batch, head)s per chunk of the launch order
     int32_t causal;
     float scale_log2;     // scale * log2(e): scores to base-2 exponent units
@@ -113,28 +107,52 @@ __host__ __device__ constexpr uint32_t idesc(bool f16, bool b_nmajor) {
 }
 
 // Barrier addresses (8 bytes each, from `b`).
+// Block j uses score buffer, key slot and value slot j mod 2.  Few
+// barriers on purpose: each commit or wait the MMA issuer makes between
+// its MMAs holds up the tensor cores for tens of cycles.
 struct Bars {
     uint32_t b;
     __device__ uint32_t q_full() const { return b; }
     __device__ uint32_t k_full(int s) const { return b + 8u * (1 + s); }
-    __device__ uint32_t k_empty(int s) const { return b + 8u * (1 + kKSlots + s); }
-    __device__ uint32_t v_full(int s) const { return b + 8u * (1 + 2 * kKSlots + s); }
-    __device__ uint32_t v_empty(int s) const { return b + 8u * (1 + 2 * kKSlots + kVSlots + s); }
-    __device__ uint32_t s_full(int t) const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + t); }
-    __device__ uint32_t p_full(int t) const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + kTiles + t); }
-    // P V of tile t complete
-    __device__ uint32_t p_free(int t) const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + 2 * kTiles + t); }
-    __device__ uint32_t drain() const { return b + 8u * (1 + 2 * kKSlots + 2 * kVSlots + 3 * kTiles); }
+    __device__ uint32_t v_full(int s) const { return b + 8u * (1 + kKSlots + s); }
+    // P V of the block in value slot s complete (both halves): the slot is
+    // free, and the output accumulators hold that block
+    __device__ uint32_t v_empty(int s) const { return b + 8u * (1 + kKSlots + kVSlots + s); }
+    static constexpr int kS = 1 + kKSlots + 2 * kVSlots;
+    // S_j complete in buffer s = j mod 2; key slot s is free again
+    __device__ uint32_t s_full(int s) const { return b + 8u * (kS + s); }
+    // both halves' weights of the block in buffer s written
+    __device__ uint32_t p_full(int s) const { return b + 8u * (kS + 2 + s); }
+    // every MMA of the tile complete
+    __device__ uint32_t o_final() const { return b + 8u * (kS + 4); }
+    __device__ uint32_t drain() const { return b + 8u * (kS + 5); }
 };
 
-// One softmax thread: query row r of tile t (TMEM lane quarter q, lane l).
+// A bounded wait that first tests the phase without blocking (the common
+// case on the MMA issuer's path: the phase is already complete).
+__device__ __forceinline__ bool wait_quick(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+    return mbar_test_wait(bar, parity) || wait_bounded(bar, parity, ctl);
+}
+
+// Named barrier of the two warps (one per half) that read the same 32
+// tensor-memory lanes; ids 1-4 (0 is the CTA barrier).
+__device__ __forceinline__ void pair_sync(int quarter) {
+    asm volatile("barrier.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+}
+
+// One softmax thread: query row r (TMEM lane quarter q, lane l) of the tile,
+// keys [64 h, 64 h + 64) of every block.  `xch` is shared memory for the
+// final exchange of (m, l) with the other half (free once every MMA of the
+// tile is complete).
 template <bool kF16>
-__device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar, uint32_t tmem, int t, int q0,
-                                            int bh, int nkv, int quarter, int lane, const WaitCtl& ctl) {
+__device__ __forceinline__ void softmax_half(const AttnParams& p, const Bars& bar, uint32_t tmem, int h, int q0,
+                                             int bh, int nkv, int quarter, int lane, float* xch,
+                                             const WaitCtl& ctl) {
     const int r = quarter * 32 + lane;  // row within the tile
     const int qrow = q0 + r;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t scol = 128u * t, ocol = kOCol + 128u * t;
+    const uint32_t hcol = static_cast<uint32_t>(kHalf * h);  // this half's columns of a score buffer
+    const uint32_t ocol = kOCol + 128u * h;                   // this half's output accumulator
     const int kv_last = p.causal ? qrow + p.Sk - p.Sq : p.Sk - 1;  // last key this row sees
     const float c2 = p.scale_log2;
     // a bounded wait taken by lane 0 for the whole warp
@@ -143,55 +161,63 @@ __device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar
         if (lane == 0) good = wait_bounded(b, parity, ctl) ? 1 : 0;
         return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
-    float m_used = -INFINITY;  // base-2 maximum the weights are taken against
-    float l = 0.0f;            // sum of this row's weights
+    float m_used = -INFINITY;  // base-2 maximum this half's weights are taken against
+    float l = 0.0f;            // sum of this half's weights
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-        // S_j complete: every MMA issued before it is complete too (a
-        // commit covers all of them), in particular P V of block j - 1
-        if (!warp_wait(bar.s_full(t), static_cast<uint32_t>(j) & 1u)) {
+        const int sb = j & 1;
+        const uint32_t scol = 128u * static_cast<uint32_t>(sb) + hcol;
+        // S_j complete.  S_j was issued after both halves' P V of block
+        // j - 2, so that is complete too; P V of block j - 1 may still run.
+        if (!warp_wait(bar.s_full(sb), static_cast<uint32_t>(j >> 1) & 1u)) {
             ok = false;
             break;
         }
         tc_fence_after();
-        uint32_t s[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(s + 32 * c);
-            tmem_ld_32x32b_x32(trow + scol + 32u * c, part);
-        }
+        uint32_t s[kHalf];
+        tmem_ld_32x32b_x32(trow + scol, *reinterpret_cast<uint32_t(*)[32]>(s));
+        tmem_ld_32x32b_x32(trow + scol + 32u, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
         tmem_ld_wait();
         // keys past Sk or past the causal limit weigh nothing
-        const int k0 = j * kBKV;
-        if (!(k0 + kBKV - 1 <= kv_last && k0 + kBKV <= p.Sk)) {
+        const int k0 = j * kBKV + kHalf * h;
+        if (!(k0 + kHalf - 1 <= kv_last && k0 + kHalf <= p.Sk)) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
+            for (int c = 0; c < kHalf; ++c)
                 if (k0 + c > kv_last || k0 + c >= p.Sk) s[c] = __float_as_uint(-INFINITY);
         }
-        // row maximum: eight independent chains of three-input maxima, then
-        // a tree
+        // maximum of the 64 scores: eight independent chains of
+        // three-input maxima, then a tree
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
 #pragma unroll
-        for (int c = 8; c < 128; c += 16) {
+        for (int c = 8; c < 56; c += 16) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 asm("max.f32 %0, %1, %2, %3;"
                     : "=f"(mx[i])
                     : "f"(mx[i]), "f"(__uint_as_float(s[c + i])), "f"(__uint_as_float(s[c + 8 + i])));
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], __uint_as_float(s[56 + i]));
         const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m_used, mb * c2);  // (c2 > 0)
         const bool need = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-            // every lane of the warp moves to its own new maximum; O holds
-            // P_0 V_0 + ... + P_{j-1} V_{j-1}, complete (see above)
+            // every lane of the warp moves to its own new maximum
             const float alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m_new);
             if (m_new > -INFINITY) m_used = m_new;
             l *= alpha;
             if (j >= 1) {
+                // O_h holds P V of blocks 0 .. j-1 once P V of block j - 1
+                // is complete (that of j - 2 is, see above, so the parity
+                // names one completion of the slot's barrier)
+                if (!warp_wait(bar.v_empty((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
                 for (int c = 0; c < 128; c += 32) {
@@ -211,55 +237,66 @@ __device__ __forceinline__ void softmax_row(const AttnParams& p, const Bars& bar
         }
         // p = 2^(c2 s - m): one fused multiply-add per weight, two weights
         // per packed instruction; before any visible key, m = +inf makes
-        // every weight 0.  P_j goes back into the first 64 columns of the
-        // score buffer, two weights per column, 32 columns at a time.
+        // every weight 0.  The 64 weights go back over the first 32 of the
+        // scores just read, two weights per column.
         const float mneg = m_used == -INFINITY ? -INFINITY : -m_used;
         const float2 c22 = make_float2(c2, c2), mn2 = make_float2(mneg, mneg);
         float2 rsum[4];  // eight independent partial sums, added in a fixed order
 #pragma unroll
         for (int i = 0; i < 4; ++i) rsum[i] = make_float2(0.0f, 0.0f);
+        uint32_t w[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = 64 * h + 2 * i;
-                const float2 x = fma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c22, mn2);
-                const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                rsum[i & 3] = add2(rsum[i & 3], pw);
-                w[i] = kF16 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
-            }
-            tmem_st_32x32b_x32(trow + scol + 32u * h, w);
+        for (int i = 0; i < 32; ++i) {
+            const float2 x = fma2(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c22, mn2);
+            const float2 pw = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            rsum[i & 3] = add2(rsum[i & 3], pw);
+            w[i] = kF16 ? pack_f16x2(pw.x, pw.y) : pack_bf16x2(pw.x, pw.y);
         }
+        tmem_st_32x32b_x32(trow + scol, w);
         l += ((rsum[0].x + rsum[0].y) + (rsum[1].x + rsum[1].y)) + ((rsum[2].x + rsum[2].y) + (rsum[3].x + rsum[3].y));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar.p_full(t));
+        if (lane == 0) mbar_arrive(bar.p_full(sb));
     }
     // ---------------------------------------------------- epilogue --
-    // (S of the last block complete implies P V of the block before it is:
-    // the wait for the last P V below cannot be confused with an earlier one)
-    if (ok && nkv > 0 && !warp_wait(bar.p_free(t), static_cast<uint32_t>(nkv - 1) & 1u)) ok = false;
+    // Every MMA of the tile complete (P V of both halves, every block);
+    // then the two warps of this lane quarter swap (m, l) through shared
+    // memory.  Both warps pass the pair barrier exactly once, whatever
+    // their status, so that neither waits for the other forever.
+    if (ok && nkv > 0 && !warp_wait(bar.o_final(), 0u)) ok = false;
+    xch[2 * (128 * h + r)] = m_used;
+    xch[2 * (128 * h + r) + 1] = l;
+    pair_sync(quarter);
+    const float m_o = xch[2 * (128 * (h ^ 1) + r)], l_o = xch[2 * (128 * (h ^ 1) + r) + 1];
     if (!ok) return;
     tc_fence_after();
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+    const float m = fmaxf(m_used, m_o);
+    const float f_me = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m);
+    const float f_ot = m_o == -INFINITY ? 0.0f : ex2_approx(m_o - m);
+    const float lsum = l * f_me + l_o * f_ot;
+    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+    // this warp writes output columns [64 h, 64 h + 64) of its row, from
+    // both halves' accumulators
+    const float f0 = (h == 0 ? f_me : f_ot) * inv, f1 = (h == 0 ? f_ot : f_me) * inv;
+    const float2 f02 = make_float2(f0, f0), f12 = make_float2(f1, f1);
     uint16_t* orow = static_cast<uint16_t*>(p.O) + (static_cast<int64_t>(bh) * p.Sq + qrow) * kD;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
-        uint32_t o[32];
+    for (int c = kHalf * h; c < kHalf * h + kHalf; c += 32) {
+        uint32_t o0[32], o1[32];
         if (nkv > 0) {
-            tmem_ld_32x32b_x32(trow + ocol + c, o);
+            tmem_ld_32x32b_x32(trow + kOCol + c, o0);
+            tmem_ld_32x32b_x32(trow + kOCol + 128u + c, o1);
             tmem_ld_wait();
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
+            for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
         }
         uint32_t w[16];
-        const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float2 v = mul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), inv2);
+            const float2 a = mul2(make_float2(__uint_as_float(o0[2 * i]), __uint_as_float(o0[2 * i + 1])), f02);
+            const float2 v = fma2(make_float2(__uint_as_float(o1[2 * i]), __uint_as_float(o1[2 * i + 1])), f12, a);
             w[i] = kF16 ? pack_f16x2(v.x, v.y) : pack_bf16x2(v.x, v.y);
         }
         if (qrow < p.Sq) {
@@ -287,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     // Launch order.  Non-causal: (batch, head) by (batch, head), all CTAs
     // of one alike.  Causal: chunks of p.group (batch, head)s whose K and V
-    // fit in L2 together; within a chunk the longest query pairs first, one
+    // fit in L2 together; within a chunk the longest query tiles first, one
     // per (batch, head), so the launch ends on the shortest CTAs.
     int bh, qb;
     if (p.causal) {
@@ -301,26 +338,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         bh = blockIdx.x / p.nq;
         qb = p.nq - 1 - static_cast<int>(blockIdx.x % p.nq);
     }
-    const int q0 = qb * kTiles * kBQ;                                // first query row of tile A
-    const int n_a = kv_blocks(p, q0), n_b = kv_blocks(p, q0 + kBQ);  // blocks tiles A and B visit
-    const int nkv = max(n_a, n_b);                                   // blocks the CTA loads
-    auto n_t = [&](int t) { return t == 0 ? n_a : n_b; };
+    const int q0 = qb * kBQ;
+    const int nkv = kv_blocks(p, q0);  // key / value blocks the tile visits
 
     if (threadIdx.x == 0) {
         mbar_init(bar.q_full(), 1);
-        for (int s = 0; s < kKSlots; ++s) {
-            mbar_init(bar.k_full(s), 1);
-            mbar_init(bar.k_empty(s), 1);
-        }
+        for (int s = 0; s < kKSlots; ++s) mbar_init(bar.k_full(s), 1);
         for (int s = 0; s < kVSlots; ++s) {
             mbar_init(bar.v_full(s), 1);
             mbar_init(bar.v_empty(s), 1);
         }
-        for (int t = 0; t < kTiles; ++t) {
-            mbar_init(bar.s_full(t), 1);
-            mbar_init(bar.p_full(t), 4);  // every softmax warp of the tile
-            mbar_init(bar.p_free(t), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar.s_full(s), 1);
+            mbar_init(bar.p_full(s), 8);  // every softmax warp of both halves
         }
+        mbar_init(bar.o_final(), 1);
         mbar_init(bar.drain(), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -334,26 +366,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
-    // (each role's code sits in the branch of its register budget)
     if (warp < kWarpK) {
         // ---------------------------------------- softmax and epilogue --
-        setmaxnreg_inc<kRegsSoftmax>();
-        const int t = warp >> 2;
-        softmax_row<kF16>(p, bar, tmem, t, q0 + t * kBQ, bh, n_t(t), warp & 3, lane, ctl);
-    } else {
-    setmaxnreg_dec<kRegsOther>();
-    if (warp == kWarpK || warp == kWarpV) {
+        softmax_half<kF16>(p, bar, tmem, warp >> 2, q0, bh, nkv, warp & 3, lane,
+                           reinterpret_cast<float*>(base_ptr + kQOff), ctl);
+    } else if (warp == kWarpK || warp == kWarpV) {
         // --------------------------------- TMA producers: Q and K / V --
         const bool is_k = warp == kWarpK;
         if (lane == 0 && nkv > 0) {
             uint32_t outstanding = 0, out_par = 0;  // loads per slot
             if (is_k) {
-                mbar_arrive_expect_tx(bar.q_full(), kTiles * kTile);
-                for (int t = 0; t < kTiles; ++t) {
-                    const uint32_t qs = base + kQOff + t * kTile;
-                    tma_load_3d(qs, &tmQ, bar.q_full(), 0, q0 + t * kBQ, bh);
-                    tma_load_3d(qs + kAtom, &tmQ, bar.q_full(), 64, q0 + t * kBQ, bh);
-                }
+                mbar_arrive_expect_tx(bar.q_full(), kTile);
+                tma_load_3d(base + kQOff, &tmQ, bar.q_full(), 0, q0, bh);
+                tma_load_3d(base + kQOff + kAtom, &tmQ, bar.q_full(), 64, q0, bh);
             }
             const int slots = is_k ? kKSlots : kVSlots;
             const CUtensorMap* map = is_k ? &tmK : &tmV;
@@ -362,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ph = static_cast<uint32_t>(j / slots) & 1u;
                 const uint32_t dst = base + (is_k ? kKOff : kVOff) + st * kTile;
                 const uint32_t full = is_k ? bar.k_full(st) : bar.v_full(st);
-                if (!wait_bounded(is_k ? bar.k_empty(st) : bar.v_empty(st), ph ^ 1u, ctl)) break;
+                // a key slot is free once S of its previous block is complete
+                if (!wait_bounded(is_k ? bar.s_full(st) : bar.v_empty(st), ph ^ 1u, ctl)) break;
                 // tests only: the first CTA leaves its first key block unloaded
                 if (is_k && (p.debug_flags & 1) && blockIdx.x == 0 && j == 0) continue;
                 mbar_arrive_expect_tx(full, kTile);
@@ -382,68 +408,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------- MMA issuer --
         if (lane == 0 && nkv > 0) {
             constexpr uint32_t kIdS = idesc(kF16, false), kIdPV = idesc(kF16, true);
-            bool ok = wait_bounded(bar.q_full(), 0u, ctl);
-            // S_t(j) = Q_t K_j^T into tile t's score buffer: both operands
-            // K-major, two 64-wide swizzle columns of D, the k-th 16-deep
-            // step 32 bytes along a row.  The buffer held P_t(j-1), which
-            // P V of tile t (issued before) has read.
-            auto issue_s = [&](int t, int j) -> bool {
-                const int st = j % kKSlots;
-                if (!wait_bounded(bar.k_full(st), static_cast<uint32_t>(j / kKSlots) & 1u, ctl)) return false;
-                tc_fence_after();
-                const uint32_t qs = base + kQOff + t * kTile, ks = base + kKOff + st * kTile;
+            static_assert(kKSlots == 2 && kVSlots == 2, "block j uses score buffer, key slot and value slot j mod 2");
+            using C0 = std::integral_constant<int, 0>;
+            using C1 = std::integral_constant<int, 1>;
+            // Every shared-memory descriptor the loop uses is formed here,
+            // once, and every slot and buffer index below is a constant: an
+            // MMA whose descriptors are computed just before it issues only
+            // about every 120 cycles, against 64 for the tensor cores to run
+            // one of these 128 x 128 x 16 steps.
+            // S = Q K^T: both operands K-major, two 64-wide swizzle columns
+            // of D, the k-th 16-deep step 32 bytes along a row.  P V: V (128
+            // keys x 128 columns, columns contiguous) is the N-major B
+            // operand: 64-column boxes 16 KiB apart, 8-key groups 1 KiB
+            // apart, the k-th 16-key step 2 KiB on.
+            uint64_t qd[8], kd[kKSlots][8], vd[kVSlots][8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t ad = smem_desc_sw128(qs + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
-                    const uint64_t bd = smem_desc_sw128(ks + (k >> 2) * kAtom + (k & 3) * 32u, 16u, 1024u);
-                    umma_f16<1>(tmem + 128u * t, ad, bd, kIdS, k > 0 ? 1u : 0u);
-                }
-                umma_commit(bar.s_full(t));
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t c = (k >> 2) * kAtom + (k & 3) * 32u;
+                qd[k] = smem_desc_sw128(base + kQOff + c, 16u, 1024u);
+#pragma unroll
+                for (int s = 0; s < kKSlots; ++s) kd[s][k] = smem_desc_sw128(base + kKOff + s * kTile + c, 16u, 1024u);
+#pragma unroll
+                for (int s = 0; s < kVSlots; ++s)
+                    vd[s][k] = smem_desc_sw128(base + kVOff + s * kTile + k * 2048u, kAtom, 1024u);
+            }
+            bool ok = wait_bounded(bar.q_full(), 0u, ctl);
+            // S_j = Q K_j^T into score buffer b = j mod 2, from key slot b.
+            // The buffer held the weights of block j - 2, which both halves'
+            // P V (issued before) read.
+            auto issue_s = [&](auto bc, int j) -> bool {
+                constexpr int b = decltype(bc)::value;
+                if (!wait_quick(bar.k_full(b), static_cast<uint32_t>(j >> 1) & 1u, ctl)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) umma_f16<1>(tmem + 128u * b, qd[k], kd[b][k], kIdS, k > 0 ? 1u : 0u);
+                umma_commit(bar.s_full(b));  // (K_j read, too)
                 return true;
             };
-            // O_t += P_t(j) V_j: P (128 rows x 128 keys, two per 32-bit
-            // column) is the tensor-memory A operand in the first 64 columns
-            // of tile t's score buffer; V (128 keys x 128 columns, columns
-            // contiguous) the N-major B operand: 64-column boxes 16 KiB
-            // apart, 8-key groups 1 KiB apart, the k-th 16-key step 2 KiB on.
-            auto issue_pv = [&](int t, int j) -> bool {
-                const int vs_slot = j % kVSlots;
-                if (!wait_bounded(bar.v_full(vs_slot), static_cast<uint32_t>(j / kVSlots) & 1u, ctl) ||
-                    !wait_bounded(bar.p_full(t), static_cast<uint32_t>(j) & 1u, ctl))
+            // O_h += P_j[:, half h] V_j[half h, :]: half h's 64 weights (two
+            // per 32-bit column) are the tensor-memory A operand at column
+            // 64 h of score buffer b; half h takes V's 16-key steps 4 h ..
+            // 4 h + 3.  Block j (b = j mod 2): P V of both halves once both
+            // halves' weights are written, then S(j + 2) into the buffer
+            // they have read.
+            auto block = [&](auto bc, int j) -> bool {
+                constexpr int b = decltype(bc)::value;
+                if (!wait_quick(bar.v_full(b), static_cast<uint32_t>(j >> 1) & 1u, ctl) ||
+                    !wait_quick(bar.p_full(b), static_cast<uint32_t>(j >> 1) & 1u, ctl))
                     return false;
                 tc_fence_after();
-                const uint32_t vs = base + kVOff + vs_slot * kTile;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t bd = smem_desc_sw128(vs + k * 2048u, kAtom, 1024u);
-                    umma_f16_ta(tmem + kOCol + 128u * t, tmem + 128u * t + 8u * k, bd, kIdPV,
-                                (j > 0 || k > 0) ? 1u : 0u);
-                }
-                umma_commit(bar.p_free(t));
-                return true;
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_f16_ta(tmem + kOCol + 128u * h, tmem + 128u * b + 64u * h + 8u * k, vd[b][4 * h + k],
+                                    kIdPV, (j > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar.v_empty(b));  // V_j read; O holds block j
+                return j + 2 >= nkv || issue_s(bc, j + 2);
             };
-            // order: S_A(0), S_B(0); then per block j: P V_A(j), S_A(j+1),
-            // P V_B(j), S_B(j+1) -- while one tile's softmax runs, the
-            // tensor cores work on the other tile
-            for (int t = 0; ok && t < kTiles; ++t)
-                if (n_t(t) > 0) ok = issue_s(t, 0);
-            if (ok) umma_commit(bar.k_empty(0));
-            for (int j = 0; ok && j < nkv; ++j) {
-                for (int t = 0; ok && t < kTiles; ++t) {
-                    if (j >= n_t(t)) continue;
-                    ok = issue_pv(t, j);
-                    if (ok && j + 1 < n_t(t)) ok = issue_s(t, j + 1);
-                }
-                if (!ok) break;
-                umma_commit(bar.v_empty(j % kVSlots));                     // V_j read by both tiles
-                if (j + 1 < nkv) umma_commit(bar.k_empty((j + 1) % kKSlots));  // K_{j+1} too
-            }
+            ok = ok && issue_s(C0{}, 0) && (nkv < 2 || issue_s(C1{}, 1));
+            for (int j = 0; ok && j < nkv; j += 2) ok = block(C0{}, j) && (j + 1 >= nkv || block(C1{}, j + 1));
+            if (ok) umma_commit(bar.o_final());
             // every MMA issued above completes before tensor memory is freed
             umma_commit(bar.drain());
             wait_bounded(bar.drain(), 0u, ctl, false);
         }
         __syncwarp();
-    }
     }
 
     // ------------------------------------------------------------ exit --
@@ -560,15 +590,6 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
         DeviceState& ds = g_dev[dev];
         if (!status_word_locked(dev)) return TSGEMM_ERR_CUDA;
         if (!ds.attr[f16 ? 1 : 0]) {
-            // the warpgroups' register split must fit in what the CTA is
-            // launched with, or the softmax warps would wait for registers
-            // forever
-            cudaFuncAttributes fa{};
-            if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
-                (void)cudaGetLastError();
-                return TSGEMM_ERR_CUDA;
-            }
-            if (fa.numRegs * kThreads < kRegPool) return TSGEMM_ERR_UNSUPPORTED;
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kSmemBytes)) != cudaSuccess) {
                 (void)cudaGetLastError();
@@ -600,7 +621,7 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     prm.H = static_cast<int32_t>(H);
     prm.Sq = static_cast<int32_t>(Sq);
     prm.Sk = static_cast<int32_t>(Sk);
-    prm.nq = static_cast<int32_t>((Sq + kTiles * kBQ - 1) / (kTiles * kBQ));
+    prm.nq = static_cast<int32_t>((Sq + kBQ - 1) / kBQ);
     // about 64 MB of K and V per chunk of the causal launch order
     const int64_t kv_head_bytes = 2 * Sk * static_cast<int64_t>(D) * 2;
     prm.group = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(B * H, (64ll << 20) / kv_head_bytes)));

@@ -454,7 +454,7 @@ def test_attention_argument_checks(ts):
 def _causal_order(BH, nq, group):
     """The attention kernel's causal launch order, restated: CTA b takes
     chunk b // (group nq) of `group` (batch, head)s; within it the longest
-    query pairs (largest qb) come first, one per (batch, head)."""
+    query tiles (largest qb) come first, one per (batch, head)."""
     out = []
     for b in range(BH * nq):
         span = group * nq
@@ -469,7 +469,7 @@ def _causal_order(BH, nq, group):
 def test_causal_launch_order_covers_every_tile_once(BH, nq, group):
     order = _causal_order(BH, nq, group)
     assert sorted(order) == sorted((bh, qb) for bh in range(BH) for qb in range(nq))
-    # within each chunk the query pairs never grow along the launch order
+    # within each chunk the query tiles never grow along the launch order
     span = group * nq
     for c0 in range(0, BH * nq, span):
         qbs = [qb for _, qb in order[c0:c0 + span]]
