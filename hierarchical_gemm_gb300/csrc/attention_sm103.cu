@@ -359,6 +359,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
+        // The first copies leave before tensor memory is allocated and the
+        // CTA synchronises: Q and the first key and value blocks (the
+        // producers take over from the second block).
+        if (nkv > 0) {
+            mbar_arrive_expect_tx(bar.q_full(), kTile);
+            tma_load_3d(base + kQOff, &tmQ, bar.q_full(), 0, q0, bh);
+            tma_load_3d(base + kQOff + kAtom, &tmQ, bar.q_full(), 64, q0, bh);
+            // tests only: the first CTA leaves its first key block unloaded
+            if (!((p.debug_flags & 1) && blockIdx.x == 0)) {
+                mbar_arrive_expect_tx(bar.k_full(0), kTile);
+                tma_load_3d(base + kKOff, &tmK, bar.k_full(0), 0, 0, bh);
+                tma_load_3d(base + kKOff + kAtom, &tmK, bar.k_full(0), 64, 0, bh);
+            }
+            mbar_arrive_expect_tx(bar.v_full(0), kTile);
+            tma_load_3d(base + kVOff, &tmV, bar.v_full(0), 0, 0, bh);
+            tma_load_3d(base + kVOff + kAtom, &tmV, bar.v_full(0), 64, 0, bh);
+        }
     }
     if (warp == kWarpMma) tmem_alloc<1>(smem_u32(tmem_holder), kTmemCols);
     tc_fence_before();
@@ -374,23 +391,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // --------------------------------- TMA producers: Q and K / V --
         const bool is_k = warp == kWarpK;
         if (lane == 0 && nkv > 0) {
-            uint32_t outstanding = 0, out_par = 0;  // loads per slot
-            if (is_k) {
-                mbar_arrive_expect_tx(bar.q_full(), kTile);
-                tma_load_3d(base + kQOff, &tmQ, bar.q_full(), 0, q0, bh);
-                tma_load_3d(base + kQOff + kAtom, &tmQ, bar.q_full(), 64, q0, bh);
-            }
+            // block 0 (and Q) left with the CTA's first thread; its copies
+            // count as this thread's for the wait before exit
+            const bool skipped0 = is_k && (p.debug_flags & 1) && blockIdx.x == 0;
+            uint32_t outstanding = skipped0 ? 0u : 1u, out_par = 0;  // loads per slot
             const int slots = is_k ? kKSlots : kVSlots;
             const CUtensorMap* map = is_k ? &tmK : &tmV;
-            for (int j = 0; j < nkv; ++j) {
+            for (int j = 1; j < nkv; ++j) {
                 const int st = j % slots;
                 const uint32_t ph = static_cast<uint32_t>(j / slots) & 1u;
                 const uint32_t dst = base + (is_k ? kKOff : kVOff) + st * kTile;
                 const uint32_t full = is_k ? bar.k_full(st) : bar.v_full(st);
                 // a key slot is free once S of its previous block is complete
                 if (!wait_bounded(is_k ? bar.s_full(st) : bar.v_empty(st), ph ^ 1u, ctl)) break;
-                // tests only: the first CTA leaves its first key block unloaded
-                if (is_k && (p.debug_flags & 1) && blockIdx.x == 0 && j == 0) continue;
                 mbar_arrive_expect_tx(full, kTile);
                 tma_load_3d(dst, map, full, 0, j * kBKV, bh);
                 tma_load_3d(dst + kAtom, map, full, 64, j * kBKV, bh);
