@@ -61,6 +61,34 @@ def test_query_ranges_across_tiles(causal, Sq, Sk):
     _check((1, 2, Sq, D), (1, 2, Sk, D), "bf16", causal, seed=50 + Sq + Sk)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Sk", [64, 320, 448])
+def test_key_half_past_the_end(causal, Sk):
+    # each 128-key block is split between two softmax halves with their own
+    # maxima and accumulators; here the last block's second half (Sk = 64,
+    # 320) or part of it (448 = 3 x 128 + 64) holds no key, so that half
+    # keeps a maximum of -inf for that block (or for the whole row)
+    _check((1, 2, 192, D), (1, 2, Sk, D), "bf16", causal, seed=60 + Sk)
+
+
+def test_key_halves_with_far_apart_maxima():
+    # the second half of every 128-key block holds keys scaled up, so its
+    # running maximum sits far above the first half's and the final combine
+    # scales the first half's sum and output down by a large factor
+    B, H, Sq, Sk = 1, 2, 256, 512
+    Qb = _tensor((B, H, Sq, D), 91, "bf16")
+    k = oracle.decode(_tensor((B, H, Sk, D), 92, "bf16"), "bf16")
+    k *= np.where((np.arange(Sk) % 128) >= 64, 6.0, 1.0)[None, None, :, None]
+    Kb = synth.quantise(k, "bf16")
+    Vb = _tensor((B, H, Sk, D), 93, "bf16")
+    for causal in (False, True):
+        O, st = _run(Qb, Kb, Vb, "bf16", 0.125, causal)
+        assert st == 0
+        ref, bound = oracle.attention(Qb, Kb, Vb, "bf16", 0.125, causal)
+        ok, info = oracle.accept_attention(O, ref, bound, "bf16")
+        assert ok, (causal, info)
+
+
 def test_causal_rows_without_keys():
     # more queries than keys: the first Sq - Sk rows see no key and are zero
     O, ref = _check((1, 1, 300, D), (1, 1, 200, D), "bf16", True)
@@ -140,7 +168,7 @@ def test_tiny_scale_weights_near_one():
 @pytest.mark.parametrize("causal", [False, True])
 def test_full_size_workload_sampled_rows(causal):
     # the B = 4, H = 32, S = 4096 workload in the launch the benchmark
-    # times; sampled 128-row windows (both tiles of a CTA, a window across
+    # times; sampled 128-row windows (whole query tiles, a window across
     # two tiles, the last rows) of three heads against the oracle
     import torch
     from hierarchical_gemm_gb300 import tsgemm
@@ -171,9 +199,9 @@ def test_full_size_workload_sampled_rows(causal):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_single_query_row(causal):
-    # decode-like: one query row per (batch, head); the CTA's second query
-    # tile is empty and its first holds one valid row (causal: the row is
-    # the last query, so it sees every key)
+    # decode-like: one query row per (batch, head); the query tile holds
+    # one valid row (causal: the row is the last query, so it sees every
+    # key)
     _check((2, 4, 1, D), (2, 4, 1000, D), "bf16", causal, seed=40)
 
 
