@@ -30,9 +30,8 @@
  * Errors.  Argument errors are returned before anything is launched:
  * TSGEMM_ERR_INVALID_ARG (sizes < 1, null or overlapping pointers, a
  * non-finite scale), TSGEMM_ERR_ALIGNMENT, TSGEMM_ERR_UNSUPPORTED (D other
- * than 128, another dtype, a device other than compute capability 10.3,
- * or a build whose kernel register count cannot hold its warpgroups'
- * register split), TSGEMM_ERR_CUDA (a failed CUDA call or launch).
+ * than 128, another dtype, a device other than compute capability 10.3),
+ * TSGEMM_ERR_CUDA (a failed CUDA call or launch).
  * Every device wait is bounded (1 s); an expired wait writes
  * TSGEMM_ERR_TIMEOUT to `status` (a device int, cleared on `stream` before
  * the launch) or, when `status` is NULL, to a word of the library that
