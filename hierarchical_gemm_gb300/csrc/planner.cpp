@@ -380,10 +380,14 @@ tsgemm_status_t choose_config(int64_t M, int64_t N, int64_t K, int dtype_in, int
     const int smax_fit = max_stages_for(best_bm, best_bn, dtype_out);
     if (f.stages > smax_fit || (f.stages != 0 && f.stages < 2)) return TSGEMM_ERR_UNSUPPORTED;
     c.stages = f.stages ? f.stages : smax_fit;
-    // raster groups of 16 tile rows when stream-K is on: same box,
-    // alternating plans, 4096^3 bf16 89.1 against 90.5 us (mean of five),
-    // 6144^3 260.7 against 261.8, 4096 x 4096 x 8192 alike; 8 otherwise
-    c.group_m = f.group_m ? f.group_m : (best_sk > 0 ? 16 : 8);
+    // raster groups of 16 tile rows when stream-K is on or the tiles are
+    // 256 x 512 (same box, alternating plans: 4096^3 bf16 89.1 against
+    // 90.5 us, mean of five; 6144^3 260.7 against 261.8; 16384 x 16384 x
+    // 8192 bf16 2251-2264 against 2285-2304 us, E4M3 1177-1182 against
+    // 1193-1197, 1000 steps under the power cap 2444-2450 against
+    // 2470-2473 us with a quarter less DRAM traffic; 8192^3 alike); 8
+    // otherwise
+    c.group_m = f.group_m ? f.group_m : ((best_sk > 0 || best_bn == 512) ? 16 : 8);
     c.cluster_split = 1;
     const int64_t tiles = ceil_div(M, best_bm) * ceil_div(N, best_bn);
     c.split_tiles = best_s > 1 ? best_st : 0;
