@@ -83,7 +83,6 @@ struct AttnParams {
     int32_t causal;
     float scale_log2;     // scale * log2(e): scores to base-2 exponent units
     int32_t debug_flags;
-    void* O;
     int* status;
     uint64_t timeout_ns;
 };
@@ -142,12 +141,13 @@ __device__ __forceinline__ void pair_sync(int quarter) {
 
 // One softmax thread: query row r (TMEM lane quarter q, lane l) of the tile,
 // keys [64 h, 64 h + 64) of every block.  `xch` is shared memory for the
-// final exchange of (m, l) with the other half (free once every MMA of the
-// tile is complete).
+// final exchange of (m, l) with the other half, `stage` 4 KiB of shared
+// memory (1024-byte aligned) for the warp's part of the output tile; both
+// are free once every MMA of the tile is complete.
 template <bool kF16>
 __device__ __forceinline__ void softmax_half(const AttnParams& p, const Bars& bar, uint32_t tmem, int h, int q0,
-                                             int bh, int nkv, int quarter, int lane, float* xch,
-                                             const WaitCtl& ctl) {
+                                             int bh, int nkv, int quarter, int lane, float* xch, uint32_t stage,
+                                             const CUtensorMap* tmO, const WaitCtl& ctl) {
     const int r = quarter * 32 + lane;  // row within the tile
     const int qrow = q0 + r;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -260,17 +260,15 @@ __device__ __forceinline__ void softmax_half(const AttnParams& p, const Bars& ba
         if (lane == 0) mbar_arrive(bar.p_full(sb));
     }
     // ---------------------------------------------------- epilogue --
-    // Every MMA of the tile complete (P V of both halves, every block);
-    // then the two warps of this lane quarter swap (m, l) through shared
-    // memory.  Both warps pass the pair barrier exactly once, whatever
-    // their status, so that neither waits for the other forever.
-    if (ok && nkv > 0 && !warp_wait(bar.o_final(), 0u)) ok = false;
+    // The two warps of this lane quarter swap (m, l) through shared memory
+    // while P V of the last block still runs: `xch` lies in the Q tile,
+    // which no MMA reads once the loop above has seen every block's scores.
+    // Both warps pass the pair barrier exactly once, whatever their status,
+    // so that neither waits for the other forever.
     xch[2 * (128 * h + r)] = m_used;
     xch[2 * (128 * h + r) + 1] = l;
     pair_sync(quarter);
     const float m_o = xch[2 * (128 * (h ^ 1) + r)], l_o = xch[2 * (128 * (h ^ 1) + r) + 1];
-    if (!ok) return;
-    tc_fence_after();
     const float m = fmaxf(m_used, m_o);
     const float f_me = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - m);
     const float f_ot = m_o == -INFINITY ? 0.0f : ex2_approx(m_o - m);
@@ -280,37 +278,59 @@ __device__ __forceinline__ void softmax_half(const AttnParams& p, const Bars& ba
     // both halves' accumulators
     const float f0 = (h == 0 ? f_me : f_ot) * inv, f1 = (h == 0 ? f_ot : f_me) * inv;
     const float2 f02 = make_float2(f0, f0), f12 = make_float2(f1, f1);
-    uint16_t* orow = static_cast<uint16_t*>(p.O) + (static_cast<int64_t>(bh) * p.Sq + qrow) * kD;
-#pragma unroll 1
-    for (int c = kHalf * h; c < kHalf * h + kHalf; c += 32) {
-        uint32_t o0[32], o1[32];
-        if (nkv > 0) {
-            tmem_ld_32x32b_x32(trow + kOCol + c, o0);
-            tmem_ld_32x32b_x32(trow + kOCol + 128u + c, o1);
-            tmem_ld_wait();
-        } else {
+    // every MMA of the tile complete (P V of both halves, every block)
+    if (ok && nkv > 0 && !warp_wait(bar.o_final(), 0u)) ok = false;
+    if (!ok) return;
+    tc_fence_after();
+    // Both halves' 64 columns in one round trip to tensor memory: o[2 c + g]
+    // holds O_g's columns 64 h + 32 c .. +31.
+    uint32_t o[4][32];
+    if (nkv > 0) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
-        }
+        for (int k = 0; k < 4; ++k)
+            tmem_ld_32x32b_x32(trow + kOCol + 128u * static_cast<uint32_t>(k & 1) + hcol + 32u * static_cast<uint32_t>(k >> 1), o[k]);
+        tmem_ld_wait();
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[k][i] = 0u;
+    }
+    // The warp's 32 rows x 64 columns go to shared memory in the 128-byte
+    // swizzled layout of the output map (row `lane` at 128 lane bytes, its
+    // 16-byte chunk c at chunk c ^ (lane mod 8): a warp's stores then
+    // touch every bank four times) and leave in one tiled store.
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float2 a = mul2(make_float2(__uint_as_float(o0[2 * i]), __uint_as_float(o0[2 * i + 1])), f02);
-            const float2 v = fma2(make_float2(__uint_as_float(o1[2 * i]), __uint_as_float(o1[2 * i + 1])), f12, a);
+            const float2 a = mul2(make_float2(__uint_as_float(o[2 * c][2 * i]), __uint_as_float(o[2 * c][2 * i + 1])), f02);
+            const float2 v = fma2(make_float2(__uint_as_float(o[2 * c + 1][2 * i]), __uint_as_float(o[2 * c + 1][2 * i + 1])), f12, a);
             w[i] = kF16 ? pack_f16x2(v.x, v.y) : pack_bf16x2(v.x, v.y);
         }
-        if (qrow < p.Sq) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                st_global_v4(orow + c + 8 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) {
+            const uint32_t chunk = static_cast<uint32_t>(4 * c + v);
+            st_shared_v4(stage + 128u * static_cast<uint32_t>(lane) + ((chunk ^ (static_cast<uint32_t>(lane) & 7u)) << 4),
+                         w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
+    }
+    // rows past Sq are clipped by the store; a box wholly past it is skipped
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0 && q0 + 32 * quarter < p.Sq) {
+        tma_store_3d(tmO, stage, kHalf * h, q0 + 32 * quarter, bh);
+        bulk_commit_group();
+        bulk_wait_group_read<0>();  // shared memory stays valid until the store has read it
     }
 }
 
 template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const AttnParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -359,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
+        prefetch_tmap(&tmO);
         // The first copies leave before tensor memory is allocated and the
         // CTA synchronises: Q and the first key and value blocks (the
         // producers take over from the second block).
@@ -385,8 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     if (warp < kWarpK) {
         // ---------------------------------------- softmax and epilogue --
+        // the output tile is staged in the key ring: box half h (16 KiB),
+        // rows of lane quarter q (4 KiB)
         softmax_half<kF16>(p, bar, tmem, warp >> 2, q0, bh, nkv, warp & 3, lane,
-                           reinterpret_cast<float*>(base_ptr + kQOff), ctl);
+                           reinterpret_cast<float*>(base_ptr + kQOff),
+                           base + kKOff + 16384u * static_cast<uint32_t>(warp >> 2) + 4096u * static_cast<uint32_t>(warp & 3),
+                           &tmO, ctl);
     } else if (warp == kWarpK || warp == kWarpV) {
         // --------------------------------- TMA producers: Q and K / V --
         const bool is_k = warp == kWarpK;
@@ -614,20 +639,22 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     int* st = status ? status : g_dev[dev].status;
 
     // [B*H][S][D] as a 3-D tensor: a 64 (D) x 128 (rows) box never crosses
-    // into another (batch, head); rows past S read as zeros
+    // into another (batch, head); rows past S read as zeros.  O is stored
+    // in 64 x 32 boxes (one per softmax warp), rows past Sq not written.
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    auto map3 = [&](CUtensorMap* m, const void* ptr, int64_t S) {
+    auto map3 = [&](CUtensorMap* m, const void* ptr, int64_t S, cuuint32_t box_rows) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
                                     static_cast<cuuint64_t>(B * H)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S * D) * 2};
-        const cuuint32_t box[3] = {64, 128, 1};
+        const cuuint32_t box[3] = {64, box_rows, 1};
         const cuuint32_t estr[3] = {1, 1, 1};
         return enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
-    alignas(64) CUtensorMap tmQ, tmK, tmV;
-    if (!map3(&tmQ, Q, Sq) || !map3(&tmK, K, Sk) || !map3(&tmV, V, Sk)) return TSGEMM_ERR_CUDA;
+    alignas(64) CUtensorMap tmQ, tmK, tmV, tmO;
+    if (!map3(&tmQ, Q, Sq, 128) || !map3(&tmK, K, Sk, 128) || !map3(&tmV, V, Sk, 128) || !map3(&tmO, O, Sq, 32))
+        return TSGEMM_ERR_CUDA;
 
     AttnParams prm{};
     prm.B = static_cast<int32_t>(B);
@@ -641,7 +668,6 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     prm.causal = causal ? 1 : 0;
     prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     prm.debug_flags = debug_flags;
-    prm.O = O;
     prm.status = st;
     prm.timeout_ns = static_cast<uint64_t>(timeout_ms ? timeout_ms : 1000) * 1000000ull;
 
@@ -655,7 +681,7 @@ tsgemm_status_t tsattn_forward_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
     lc.blockDim = dim3(kThreads, 1, 1);
     lc.dynamicSmemBytes = kSmemBytes;
     lc.stream = s;
-    void* args[4] = {&tmQ, &tmK, &tmV, &prm};
+    void* args[5] = {&tmQ, &tmK, &tmV, &tmO, &prm};
     if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return TSGEMM_ERR_CUDA;
