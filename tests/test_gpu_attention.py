@@ -127,6 +127,13 @@ def test_larger_causal_and_repeatable_bits():
     assert ok, info
 
 
+def test_causal_chunks_with_a_ragged_last_chunk():
+    # the causal launch runs in chunks of (batch, head)s that share about
+    # 8 MiB of K and V (eight at Sk = 2048); nine of them leave a last chunk
+    # of one, and 1900 query rows a ragged last tile in every head
+    _check((3, 3, 1900, D), (3, 3, 2048, D), "bf16", True, seed=30)
+
+
 def test_uniform_queries_average_the_values():
     # Q = 0: every visible key weighs the same
     Qb = synth.quantise(np.zeros((1, 1, 256, D)), "bf16")
