@@ -297,14 +297,22 @@ static tsgemm_status_t encode_maps(tsgemm_plan_s* p, const void* A, const void* 
                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
     const int64_t eb = in8 ? 1 : 2;
     const cuuint32_t estr[2] = {1, 1};
+    // L2 fill size of the operand loads: the one-SM kernel (the HBM-bound
+    // skinny shapes) streams its operands and gains from 256-byte fills;
+    // the CTA-pair kernel takes plain sector fills (same box, alternating
+    // builds: 4096^3 bf16 86.7 us in 6 of 6 runs against 86.7-88.7 with
+    // 256-byte fills, 16384 x 16384 x 8192 2155-2158 against 2167 us, the
+    // E4M3 and long-K shapes alike; the skinny 128 x 28672 x 8192 shape
+    // 78.0-78.5 against 76.5-77.0 us with plain fills)
+    const CUtensorMapL2promotion prom =
+        p->cfg.block_m == 256 ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     auto tile_map = [&](CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, cuuint32_t box_inner,
                         cuuint32_t box_outer) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * eb)};
         const cuuint32_t box[2] = {box_inner, box_outer};
         return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                   CU_TENSOR_MAP_SWIZZLE_128B, prom, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
     // Every box is 128 bytes (one swizzle row) along the contiguous
     // dimension: 64 16-bit or 128 8-bit elements.
