@@ -62,6 +62,9 @@ ATTN_WORKLOADS = {
     # a smaller case for profiler captures (still 3 x 64 MiB, larger than L2)
     "attn_b2h16s4096d128_bf16": dict(
         index=9, B=2, H=16, Sq=4096, Sk=4096, D=128, dtype="bf16", causal=False),
+    # its causal twin, for profiler captures of the causal launch
+    "attn_b2h16s4096d128_causal_bf16": dict(
+        index=11, B=2, H=16, Sq=4096, Sk=4096, D=128, dtype="bf16", causal=True),
 }
 
 
